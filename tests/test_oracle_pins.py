@@ -1,0 +1,230 @@
+"""Pins for the fp64 oracle: facts the definition fixes, checked on the CPU.
+
+Each pin is chosen so that a plausible slip in the oracle (a dropped decay,
+delta formed from the undecayed state, readout before the update, a
+transposed state, a wrong key-head index, a wrong capture clamp) fails at
+least one of them.  Sources: the per-token gated delta rule of Gated DeltaNet;
+"[WebGPU EP] adds state update capacity support for GatedDeltaNet"
+(onnxruntime PR 32767), "Changes" and "Test Coverage".
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand_case(rng, T, Hk, Hv, dk, dv, unit_k=True, alpha_lo=0.6):
+    q = rng.standard_normal((T, Hk, dk))
+    k = rng.standard_normal((T, Hk, dk))
+    if unit_k:
+        k /= np.linalg.norm(k, axis=-1, keepdims=True)
+        q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    v = rng.standard_normal((T, Hv, dv))
+    alpha = rng.uniform(alpha_lo, 1.0, size=(T, Hv))
+    beta = rng.uniform(0.0, 1.0, size=(T, Hv))
+    S0 = 0.3 * rng.standard_normal((1, Hv, dv, dk))
+    return q, k, v, alpha, beta, S0
+
+
+def _rel(a, b):
+    return np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300)
+
+
+# --- worked example -------------------------------------------------------
+
+def test_hand_worked_example(oracle_mod):
+    g = json.load(open(os.path.join(GOLDEN, "hand_worked_T2_d2.json")))
+    q = np.array(g["q"])[:, None, :]
+    k = np.array(g["k"])[:, None, :]
+    v = np.array(g["v"])[:, None, :]
+    a = np.array(g["alpha"])[:, None]
+    b = np.array(g["beta"])[:, None]
+    S0 = np.array(g["S0"])[None, None]
+    dims = dict(B=1, Hk=1, Hv=1, dk=2, dv=2, T=2)
+    o, S, su = oracle_mod.recurrent(q, k, v, a, b, initial_state=S0, capacity=2,
+                                    capture_count=[2], **dims)
+    assert np.array_equal(o[:, 0, :], np.array(g["o"]))
+    assert np.array_equal(S[0, 0], np.array(g["S_final"]))
+    assert np.array_equal(su[0], np.array(g["state_update"]))
+    for C in (1, 2, 3):
+        oc, Sc = oracle_mod.chunked(q, k, v, a, b, initial_state=S0, chunk=C, **dims)
+        assert np.allclose(oc[:, 0, :], g["o"], rtol=0, atol=1e-14)
+        assert np.allclose(Sc[0, 0], g["S_final"], rtol=0, atol=1e-14)
+    Sr = oracle_mod.replay(S0, su, [2], B=1, Hk=1, Hv=1, dk=2, dv=2, capacity=2)
+    assert np.array_equal(Sr[0, 0], np.array(g["S_final"]))
+
+
+# --- closed forms -----------------------------------------------------------
+
+def test_identity_alpha1_beta0(oracle_mod):
+    """alpha = 1, beta = 0: the state never changes and o_t = S0 q_t."""
+    rng = np.random.default_rng(1)
+    T, Hk, Hv, dk, dv = 9, 1, 2, 6, 4
+    q, k, v, _, _, S0 = _rand_case(rng, T, Hk, Hv, dk, dv)
+    a = np.ones((T, Hv))
+    b = np.zeros((T, Hv))
+    dims = dict(B=1, Hk=Hk, Hv=Hv, dk=dk, dv=dv, T=T)
+    o, S, _ = oracle_mod.recurrent(q, k, v, a, b, initial_state=S0, scale=0.5, **dims)
+    assert np.array_equal(S, S0)
+    for h in range(Hv):
+        ref = 0.5 * np.einsum("ij,tj->ti", S0[0, h], q[:, 0, :])
+        assert _rel(o[:, h, :], ref) < 1e-15
+    oc, Sc = oracle_mod.chunked(q, k, v, a, b, initial_state=S0, scale=0.5,
+                                chunk=4, **dims)
+    assert _rel(Sc, S0) < 1e-15 and _rel(oc, o) < 1e-15
+
+
+def test_beta0_pure_decay(oracle_mod):
+    """beta = 0: S_t = (prod_{s<=t} alpha_s) S0 and o_t = S_t q_t."""
+    rng = np.random.default_rng(2)
+    T, Hk, Hv, dk, dv = 7, 1, 1, 5, 3
+    q, k, v, a, _, S0 = _rand_case(rng, T, Hk, Hv, dk, dv)
+    b = np.zeros((T, Hv))
+    o, S, _ = oracle_mod.recurrent(q, k, v, a, b, initial_state=S0, B=1, Hk=Hk,
+                                   Hv=Hv, dk=dk, dv=dv, T=T)
+    cum = np.cumprod(a[:, 0])
+    assert _rel(S[0, 0], cum[-1] * S0[0, 0]) < 1e-14
+    ref = cum[:, None] * np.einsum("ij,tj->ti", S0[0, 0], q[:, 0, :])
+    assert _rel(o[:, 0, :], ref) < 1e-14
+
+
+def test_delta_rule_writes_exactly(oracle_mod):
+    """beta = 1 and a unit key: after the update, S k_t = v_t.  Reading out
+    with q_t = k_t (scale 1) makes o_t that product, for every token."""
+    rng = np.random.default_rng(3)
+    T, Hk, Hv, dk, dv = 12, 1, 2, 8, 5
+    _, k, v, a, _, S0 = _rand_case(rng, T, Hk, Hv, dk, dv)
+    b = np.ones((T, Hv))
+    o, _, _ = oracle_mod.recurrent(k, k, v, a, b, initial_state=S0, B=1, Hk=Hk,
+                                   Hv=Hv, dk=dk, dv=dv, T=T)
+    assert np.max(np.abs(o - v)) < 1e-13
+
+
+def test_single_token_from_zero_state(oracle_mod):
+    """T = 1, S0 = 0: S = beta v k^T and o = beta (k . q) v."""
+    rng = np.random.default_rng(4)
+    Hk, Hv, dk, dv = 1, 1, 7, 3
+    q, k, v, a, b, _ = _rand_case(rng, 1, Hk, Hv, dk, dv)
+    o, S, _ = oracle_mod.recurrent(q, k, v, a, b, B=1, Hk=Hk, Hv=Hv, dk=dk,
+                                   dv=dv, T=1, scale=2.0)
+    assert _rel(S[0, 0], b[0, 0] * np.outer(v[0, 0], k[0, 0])) < 1e-15
+    ref = b[0, 0] * 2.0 * np.dot(k[0, 0], q[0, 0]) * v[0, 0]
+    assert _rel(o[0, 0], ref) < 1e-14
+
+
+# --- independent formulations ---------------------------------------------
+
+@pytest.mark.parametrize("T", [1, 2, 3, 4])
+def test_bruteforce_unrolled_products(oracle_mod, T):
+    """Unrolled products of explicit dk x dk matrices; dk != dv and a
+    non-symmetric S0 so that a transposed state cannot pass."""
+    rng = np.random.default_rng(10 + T)
+    Hk, Hv, dk, dv = 1, 1, 5, 3
+    q, k, v, a, b, S0 = _rand_case(rng, T, Hk, Hv, dk, dv, unit_k=False)
+    o, S, _ = oracle_mod.recurrent(q, k, v, a, b, initial_state=S0, B=1, Hk=Hk,
+                                   Hv=Hv, dk=dk, dv=dv, T=T, scale=0.7)
+    ob, Sb = oracle_mod.bruteforce_unrolled(q[:, 0], k[:, 0], v[:, 0], a[:, 0],
+                                            b[:, 0], S0[0, 0], scale=0.7)
+    assert _rel(S[0, 0], Sb) < 1e-13
+    assert _rel(o[:, 0, :], ob) < 1e-13
+
+
+@pytest.mark.parametrize("chunk,lengths", [(16, [37, 64]), (64, [130]),
+                                           (5, [23, 1, 10]), (1, [6])])
+def test_chunked_equals_recurrent(oracle_mod, chunk, lengths):
+    """The chunked UT/WY form and the per-token form agree in fp64, with a
+    ragged last chunk, ragged rows and three value heads per key head."""
+    rng = np.random.default_rng(20 + chunk)
+    Hk, Hv, dk, dv = 2, 6, 12, 10
+    T = sum(lengths)
+    q, k, v, a, b, _ = _rand_case(rng, T, Hk, Hv, dk, dv, alpha_lo=0.5)
+    S0 = 0.3 * rng.standard_normal((len(lengths), Hv, dv, dk))
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    dims = dict(B=len(lengths), Hk=Hk, Hv=Hv, dk=dk, dv=dv, cu_seqlens=cu)
+    o, S, _ = oracle_mod.recurrent(q, k, v, a, b, initial_state=S0, scale=0.9, **dims)
+    oc, Sc = oracle_mod.chunked(q, k, v, a, b, initial_state=S0, scale=0.9,
+                                chunk=chunk, **dims)
+    assert _rel(oc, o) < 1e-12
+    assert _rel(Sc, S) < 1e-12
+
+
+def test_replay_reproduces_every_accepted_prefix(oracle_mod):
+    """Replaying the first n captured factors from S0 gives the state the
+    recurrence reaches after n tokens, for every n, and the final state at n=T."""
+    rng = np.random.default_rng(30)
+    T, Hk, Hv, dk, dv = 7, 2, 4, 6, 5
+    q, k, v, a, b, S0 = _rand_case(rng, T, Hk, Hv, dk, dv)
+    dims = dict(B=1, Hk=Hk, Hv=Hv, dk=dk, dv=dv)
+    _, S_full, su = oracle_mod.recurrent(q, k, v, a, b, initial_state=S0, T=T,
+                                         capacity=T, capture_count=[T], **dims)
+    for n in range(T + 1):
+        _, S_n, _ = oracle_mod.recurrent(q[:n], k[:n], v[:n], a[:n], b[:n],
+                                         initial_state=S0, T=n, **dims)
+        S_r = oracle_mod.replay(S0, su, [n], capacity=T, **dims)
+        assert _rel(S_r, S_n) < 1e-13, n
+    assert _rel(oracle_mod.replay(S0, su, [T], capacity=T, **dims), S_full) < 1e-13
+
+
+def test_key_head_sharing(oracle_mod):
+    """Inverse GQA: with Hk = 2 and Hv = 6, value head h gives exactly what a
+    single-head run with key/query head h // 3 gives."""
+    rng = np.random.default_rng(40)
+    T, Hk, Hv, dk, dv = 9, 2, 6, 4, 3
+    q, k, v, a, b, S0 = _rand_case(rng, T, Hk, Hv, dk, dv)
+    o, S, su = oracle_mod.recurrent(q, k, v, a, b, initial_state=S0, B=1, Hk=Hk,
+                                    Hv=Hv, dk=dk, dv=dv, T=T, capacity=T,
+                                    capture_count=[T])
+    for h in range(Hv):
+        hk = h // 3
+        o1, S1, su1 = oracle_mod.recurrent(
+            q[:, hk:hk + 1], k[:, hk:hk + 1], v[:, h:h + 1], a[:, h:h + 1],
+            b[:, h:h + 1], initial_state=S0[:, h:h + 1], B=1, Hk=1, Hv=1,
+            dk=dk, dv=dv, T=T, capacity=T, capture_count=[T])
+        assert np.array_equal(o[:, h], o1[:, 0])
+        assert np.array_equal(S[0, h], S1[0, 0])
+        # decay of head h, key of head hk, delta of head h
+        assert np.array_equal(su[0, :, h], su1[0, :, 0])
+        assert np.array_equal(su[0, :, Hv + hk * dk:Hv + (hk + 1) * dk],
+                              su1[0, :, 1:1 + dk])
+        off = Hv + Hk * dk + h * dv
+        assert np.array_equal(su[0, :, off:off + dv], su1[0, :, 1 + dk:])
+
+
+# --- capture contract -------------------------------------------------------
+
+def test_capture_clamp_prefix_and_inactive(oracle_mod):
+    """Captured tokens are the first n_b = clamp(count, 0, min(capacity, T_b));
+    decay and key are the inputs themselves; slots >= n_b are untouched while
+    active; the inactive run zeroes the whole output."""
+    rng = np.random.default_rng(50)
+    lengths = [5, 5, 2, 6]
+    counts = [-1, 3, 100, 4]
+    cap = 4
+    Hk, Hv, dk, dv = 1, 2, 3, 2
+    T = sum(lengths)
+    q, k, v, a, b, _ = _rand_case(rng, T, Hk, Hv, dk, dv)
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    slot = Hv + Hk * dk + Hv * dv
+    sentinel = np.full((4, cap, slot), 12345.0)
+    dims = dict(B=4, Hk=Hk, Hv=Hv, dk=dk, dv=dv, cu_seqlens=cu)
+    o, S, su = oracle_mod.recurrent(q, k, v, a, b, capacity=cap,
+                                    capture_count=counts,
+                                    state_update=sentinel.copy(), **dims)
+    n = oracle_mod.capture_counts_clamped(counts, cap, lengths)
+    assert n == [0, 3, 2, 4]
+    for r in range(4):
+        for t in range(cap):
+            if t < n[r]:
+                tok = cu[r] + t
+                assert np.array_equal(su[r, t, :Hv], a[tok])
+                assert np.array_equal(su[r, t, Hv:Hv + dk], k[tok, 0])
+            else:
+                assert np.all(su[r, t] == 12345.0)
+    o2, S2, su0 = oracle_mod.recurrent(q, k, v, a, b, capacity=cap,
+                                       capture_count=counts, active=False,
+                                       state_update=sentinel.copy(), **dims)
+    assert np.all(su0 == 0.0)
+    assert np.array_equal(o2, o) and np.array_equal(S2, S)
