@@ -1,0 +1,303 @@
+// gdn_api.cu -- the C ABI of libgdn (include/gdn.h): argument validation,
+// buffer-overlap checks and kernel dispatch.  Host code only; every check
+// runs before anything is launched, so a rejected call has no side effects.
+#include <cstdint>
+#include <cstring>
+
+#include "gdn_internal.cuh"
+
+namespace gdn {
+
+// The library's device error word (GDN_DEVERR_* bits).  Its device address is
+// resolved once per device and handed to kernels in their parameter blocks.
+__device__ uint32_t g_device_errors = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+uint32_t *g_err_addr[kMaxDevices] = {};
+
+cudaError_t error_word(uint32_t **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (g_err_addr[dev] == nullptr) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_device_errors);
+        if (e != cudaSuccess) return e;
+        g_err_addr[dev] = static_cast<uint32_t *>(ptr);
+    }
+    *out = g_err_addr[dev];
+    return cudaSuccess;
+}
+
+size_t dtype_bytes(int dt) {
+    switch (dt) {
+        case GDN_F32: return 4;
+        case GDN_F16: return 2;
+        case GDN_BF16: return 2;
+        default: return 0;
+    }
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+struct Span {
+    const void *p;
+    size_t bytes;
+    bool is_output;
+};
+
+bool overlaps(const Span &a, const Span &b) {
+    if (a.p == nullptr || b.p == nullptr || a.bytes == 0 || b.bytes == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+// GDN_ERR_ALIAS if an output overlaps anything else, except the exact
+// in-place pair (same start, same size) `allow_a`/`allow_b` when given.
+int check_alias(const Span *s, int n, int allow_a, int allow_b) {
+    for (int i = 0; i < n; ++i)
+        for (int j = i + 1; j < n; ++j) {
+            if (!s[i].is_output && !s[j].is_output) continue;
+            if (!overlaps(s[i], s[j])) continue;
+            const bool pair = (i == allow_a && j == allow_b) || (i == allow_b && j == allow_a);
+            if (pair && s[i].p == s[j].p && s[i].bytes == s[j].bytes) continue;
+            return GDN_ERR_ALIAS;
+        }
+    return GDN_OK;
+}
+
+bool mul_ok(size_t a, size_t b, size_t *out) {
+    if (a != 0 && b > SIZE_MAX / a) return false;
+    *out = a * b;
+    return true;
+}
+
+// Sizes shared by prefill and recurrent calls.
+struct Shapes {
+    size_t total_T, qk_bytes, v_bytes, gate_bytes, s0_bytes, sf_bytes;
+};
+
+int check_common(const void *q, const void *k, const void *v, const void *alpha,
+                 const void *beta, const int32_t *cu, const float *s0,
+                 const int32_t *s0_idx, int n_s0, const float *sf, const void *out,
+                 int B, int T, int Hq, int Hk, int Hv, int dk, int dv, int dt_qkv,
+                 int dt_gate, Shapes *sh) {
+    if (B < 0 || T < 0 || Hk <= 0 || Hv <= 0 || dk <= 0 || dv <= 0) return GDN_ERR_INVALID_ARG;
+    if (Hq != Hk || Hv % Hk != 0) return GDN_ERR_INVALID_ARG;
+    if (dtype_bytes(dt_qkv) == 0 || dtype_bytes(dt_gate) == 0) return GDN_ERR_INVALID_ARG;
+    if (!(dk == 32 || dk == 64 || dk == 128) || !(dv == 32 || dv == 64 || dv == 128))
+        return GDN_ERR_UNSUPPORTED;
+    if (B > 65535 || Hv > 65535) return GDN_ERR_UNSUPPORTED;
+    size_t total_T = (cu == nullptr) ? (size_t)B * (size_t)T : (size_t)T;
+    if (B > 0 && total_T > 0) {
+        if (!q || !k || !v || !alpha || !beta || !out) return GDN_ERR_INVALID_ARG;
+    }
+    if (s0_idx != nullptr && s0 == nullptr) return GDN_ERR_INVALID_ARG;
+    if (s0 != nullptr) {
+        if (s0_idx == nullptr && n_s0 < B) return GDN_ERR_INVALID_ARG;
+        if (n_s0 < 0) return GDN_ERR_INVALID_ARG;
+    }
+    const void *a16[] = {q, k, v, alpha, beta, out, s0, sf};
+    for (const void *p : a16)
+        if (p && !aligned(p, 16)) return GDN_ERR_ALIGN;
+    if ((cu && !aligned(cu, 4)) || (s0_idx && !aligned(s0_idx, 4))) return GDN_ERR_ALIGN;
+
+    const size_t st = (size_t)Hv * dv * dk * sizeof(float);
+    sh->total_T = total_T;
+    if (!mul_ok(total_T, (size_t)Hk * dk * dtype_bytes(dt_qkv), &sh->qk_bytes)) return GDN_ERR_INVALID_ARG;
+    if (!mul_ok(total_T, (size_t)Hv * dv * dtype_bytes(dt_qkv), &sh->v_bytes)) return GDN_ERR_INVALID_ARG;
+    if (!mul_ok(total_T, (size_t)Hv * dtype_bytes(dt_gate), &sh->gate_bytes)) return GDN_ERR_INVALID_ARG;
+    sh->s0_bytes = s0 ? (size_t)(s0_idx ? n_s0 : (n_s0 > B ? n_s0 : B)) * st : 0;
+    sh->sf_bytes = sf ? (size_t)B * st : 0;
+    return GDN_OK;
+}
+
+}  // namespace
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" {
+
+const char *gdn_status_string(int status) {
+    switch (status) {
+        case GDN_OK: return "ok";
+        case GDN_ERR_INVALID_ARG: return "invalid argument";
+        case GDN_ERR_UNSUPPORTED: return "unsupported size, chunk or dtype";
+        case GDN_ERR_ALIAS: return "an output buffer overlaps another buffer";
+        case GDN_ERR_ALIGN: return "misaligned pointer";
+        case GDN_ERR_CUDA: return "CUDA launch or runtime error";
+        case GDN_ERR_TIMEOUT: return "a kernel abandoned a bounded wait";
+        case GDN_ERR_WORKSPACE: return "workspace missing or too small";
+        default: return "unknown status";
+    }
+}
+
+int gdn_recurrent_capture(const void *q, const void *k, const void *v, const void *alpha,
+                          const void *beta, const int32_t *cu_seqlens,
+                          const float *initial_state, const int32_t *initial_state_indices,
+                          int num_initial_states, float *final_state, void *out, int B, int T,
+                          int Hq, int Hk, int Hv, int dk, int dv, float scale, int dtype_qkv,
+                          int dtype_gate, int state_update_capacity,
+                          const int32_t *capture_count, const int32_t *state_update_active,
+                          float *state_update, void *stream) {
+    Shapes sh;
+    int st = check_common(q, k, v, alpha, beta, cu_seqlens, initial_state, initial_state_indices,
+                          num_initial_states, final_state, out, B, T, Hq, Hk, Hv, dk, dv,
+                          dtype_qkv, dtype_gate, &sh);
+    if (st != GDN_OK) return st;
+    const int cap = state_update_capacity;
+    if (cap < 0) return GDN_ERR_INVALID_ARG;
+    if (cap > 0 && (capture_count == nullptr || state_update == nullptr)) return GDN_ERR_INVALID_ARG;
+    if (state_update && !aligned(state_update, 16)) return GDN_ERR_ALIGN;
+    if ((capture_count && !aligned(capture_count, 4)) ||
+        (state_update_active && !aligned(state_update_active, 4)))
+        return GDN_ERR_ALIGN;
+    if (final_state != nullptr && final_state == initial_state && initial_state_indices != nullptr)
+        return GDN_ERR_ALIAS;
+    size_t su_bytes = 0;
+    if (cap > 0 && !mul_ok((size_t)B * cap, GDN_STATE_UPDATE_SLOT(Hk, Hv, dk, dv) * sizeof(float), &su_bytes))
+        return GDN_ERR_INVALID_ARG;
+    const size_t sf_in_place = (final_state == initial_state) ? sh.sf_bytes : 0;
+    Span spans[] = {
+        {q, sh.qk_bytes, false},                        // 0
+        {k, sh.qk_bytes, false},                        // 1
+        {v, sh.v_bytes, false},                         // 2
+        {alpha, sh.gate_bytes, false},                  // 3
+        {beta, sh.gate_bytes, false},                   // 4
+        {cu_seqlens, cu_seqlens ? (size_t)(B + 1) * 4 : 0, false},
+        {initial_state, sf_in_place ? sf_in_place : sh.s0_bytes, false},  // 6
+        {initial_state_indices, initial_state_indices ? (size_t)B * 4 : 0, false},
+        {capture_count, cap > 0 ? (size_t)B * 4 : 0, false},
+        {state_update_active, state_update_active ? 4u : 0u, false},
+        {final_state, sh.sf_bytes, true},               // 10
+        {out, sh.v_bytes, true},
+        {state_update, su_bytes, true},
+    };
+    st = check_alias(spans, (int)(sizeof(spans) / sizeof(spans[0])), 6, 10);
+    if (st != GDN_OK) return st;
+    if (B == 0) return GDN_OK;
+
+    RecurrentParams p;
+    p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.beta = beta;
+    p.cu_seqlens = cu_seqlens;
+    p.s0 = initial_state; p.s0_idx = initial_state_indices; p.n_s0 = num_initial_states;
+    p.s_final = final_state; p.out = out;
+    p.B = B; p.T = T; p.Hk = Hk; p.Hv = Hv; p.dk = dk; p.dv = dv;
+    p.scale = scale; p.dt_qkv = dtype_qkv; p.dt_gate = dtype_gate;
+    p.capacity = cap; p.capture_count = capture_count; p.active = state_update_active;
+    p.su = cap > 0 ? state_update : nullptr;
+    if (error_word(&p.err) != cudaSuccess) return GDN_ERR_CUDA;
+    return launch_recurrent(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int gdn_replay_state_updates(const float *state_in, float *state_out, const float *state_update,
+                             int state_update_capacity, const int32_t *accepted_count, int B,
+                             int Hk, int Hv, int dk, int dv, void *stream) {
+    if (B < 0 || Hk <= 0 || Hv <= 0 || dk <= 0 || dv <= 0 || Hv % Hk != 0) return GDN_ERR_INVALID_ARG;
+    if (state_update_capacity < 0) return GDN_ERR_INVALID_ARG;
+    if (!(dk == 32 || dk == 64 || dk == 128) || !(dv == 32 || dv == 64 || dv == 128))
+        return GDN_ERR_UNSUPPORTED;
+    if (B > 65535 || Hv > 65535) return GDN_ERR_UNSUPPORTED;
+    if (B > 0 && (!state_in || !state_out || !accepted_count)) return GDN_ERR_INVALID_ARG;
+    if (B > 0 && state_update_capacity > 0 && !state_update) return GDN_ERR_INVALID_ARG;
+    if ((state_in && !aligned(state_in, 16)) || (state_out && !aligned(state_out, 16)) ||
+        (state_update && !aligned(state_update, 16)) ||
+        (accepted_count && !aligned(accepted_count, 4)))
+        return GDN_ERR_ALIGN;
+    const size_t sbytes = (size_t)B * Hv * dv * dk * sizeof(float);
+    const size_t su_bytes = (size_t)B * state_update_capacity *
+                            GDN_STATE_UPDATE_SLOT(Hk, Hv, dk, dv) * sizeof(float);
+    Span spans[] = {
+        {state_in, sbytes, false},
+        {state_update, su_bytes, false},
+        {accepted_count, (size_t)B * 4, false},
+        {state_out, sbytes, true},
+    };
+    int st = check_alias(spans, 4, 0, 3);
+    if (st != GDN_OK) return st;
+    if (B == 0) return GDN_OK;
+    ReplayParams p;
+    p.s_in = state_in; p.s_out = state_out; p.su = state_update;
+    p.capacity = state_update_capacity; p.accepted = accepted_count;
+    p.B = B; p.Hk = Hk; p.Hv = Hv; p.dk = dk; p.dv = dv;
+    if (error_word(&p.err) != cudaSuccess) return GDN_ERR_CUDA;
+    return launch_replay(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+size_t gdn_prefill_workspace_size(int B, int T, int Hk, int Hv, int dk, int dv, int chunk,
+                                  int dtype_qkv) {
+    if (B < 0 || T < 0 || Hk <= 0 || Hv <= 0 || dk <= 0 || dv <= 0 || chunk <= 0 ||
+        dtype_bytes(dtype_qkv) == 0)
+        return (size_t)-1;
+    return 0;
+}
+
+int gdn_prefill_chunked(const void *q, const void *k, const void *v, const void *alpha,
+                        const void *beta, const int32_t *cu_seqlens, const float *initial_state,
+                        const int32_t *initial_state_indices, int num_initial_states,
+                        float *final_state, void *out, int B, int T, int Hq, int Hk, int Hv,
+                        int dk, int dv, int chunk, float scale, int dtype_qkv, int dtype_gate,
+                        void *workspace, size_t workspace_bytes, void *stream) {
+    Shapes sh;
+    int st = check_common(q, k, v, alpha, beta, cu_seqlens, initial_state, initial_state_indices,
+                          num_initial_states, final_state, out, B, T, Hq, Hk, Hv, dk, dv,
+                          dtype_qkv, dtype_gate, &sh);
+    if (st != GDN_OK) return st;
+    if (!(chunk == 16 || chunk == 32 || chunk == 64)) return GDN_ERR_UNSUPPORTED;
+    if (!prefill_simt_supported(dk, dv, chunk)) return GDN_ERR_UNSUPPORTED;
+    if (final_state != nullptr && final_state == initial_state && initial_state_indices != nullptr)
+        return GDN_ERR_ALIAS;
+    const size_t need = gdn_prefill_workspace_size(B, T, Hk, Hv, dk, dv, chunk, dtype_qkv);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return GDN_ERR_WORKSPACE;
+    if (workspace && !aligned(workspace, 16)) return GDN_ERR_ALIGN;
+    const size_t sf_in_place = (final_state == initial_state) ? sh.sf_bytes : 0;
+    Span spans[] = {
+        {q, sh.qk_bytes, false},
+        {k, sh.qk_bytes, false},
+        {v, sh.v_bytes, false},
+        {alpha, sh.gate_bytes, false},
+        {beta, sh.gate_bytes, false},
+        {cu_seqlens, cu_seqlens ? (size_t)(B + 1) * 4 : 0, false},
+        {initial_state, sf_in_place ? sf_in_place : sh.s0_bytes, false},  // 6
+        {initial_state_indices, initial_state_indices ? (size_t)B * 4 : 0, false},
+        {final_state, sh.sf_bytes, true},                                  // 8
+        {out, sh.v_bytes, true},
+        {workspace, need, true},
+    };
+    st = check_alias(spans, (int)(sizeof(spans) / sizeof(spans[0])), 6, 8);
+    if (st != GDN_OK) return st;
+    if (B == 0) return GDN_OK;
+
+    PrefillParams p;
+    p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.beta = beta;
+    p.cu_seqlens = cu_seqlens;
+    p.s0 = initial_state; p.s0_idx = initial_state_indices; p.n_s0 = num_initial_states;
+    p.s_final = final_state; p.out = out;
+    p.B = B; p.T = T; p.Hk = Hk; p.Hv = Hv; p.dk = dk; p.dv = dv; p.chunk = chunk;
+    p.scale = scale; p.dt_qkv = dtype_qkv; p.dt_gate = dtype_gate;
+    p.ws = workspace; p.ws_bytes = workspace_bytes;
+    if (error_word(&p.err) != cudaSuccess) return GDN_ERR_CUDA;
+    return launch_prefill_simt(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK
+                                                                                    : GDN_ERR_CUDA;
+}
+
+int gdn_device_errors(void *stream, uint32_t *flags) {
+    if (flags == nullptr) return GDN_ERR_INVALID_ARG;
+    *flags = 0;
+    uint32_t *addr = nullptr;
+    if (error_word(&addr) != cudaSuccess) return GDN_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
+    uint32_t host = 0;
+    if (cudaMemcpy(&host, addr, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess) return GDN_ERR_CUDA;
+    const uint32_t zero = 0;
+    if (cudaMemcpy(addr, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return GDN_ERR_CUDA;
+    *flags = host;
+    return (host & GDN_DEVERR_TIMEOUT) ? GDN_ERR_TIMEOUT : GDN_OK;
+}
+
+}  // extern "C"

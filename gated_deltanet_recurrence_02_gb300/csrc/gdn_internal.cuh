@@ -1,0 +1,147 @@
+// gdn_internal.cuh -- parameter blocks, launchers and small device helpers
+// shared by the libgdn kernels.  Not part of the public ABI (include/gdn.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gdn.h"
+
+namespace gdn {
+
+// Every parameter block carries `err`: the device address of the library's
+// error word (GDN_DEVERR_* bits), resolved by the host layer per device.
+
+// ---------------------------------------------------------------- params --
+
+struct RecurrentParams {
+    const void *q, *k, *v, *alpha, *beta;
+    const int32_t *cu_seqlens;
+    const float *s0;
+    const int32_t *s0_idx;
+    int n_s0;
+    float *s_final;
+    void *out;
+    int B, T, Hk, Hv, dk, dv;
+    float scale;
+    int dt_qkv, dt_gate;
+    int capacity;
+    const int32_t *capture_count;
+    const int32_t *active;
+    float *su;
+    uint32_t *err;
+};
+
+struct ReplayParams {
+    const float *s_in;
+    float *s_out;
+    const float *su;
+    int capacity;
+    const int32_t *accepted;
+    int B, Hk, Hv, dk, dv;
+    uint32_t *err;
+};
+
+struct PrefillParams {
+    const void *q, *k, *v, *alpha, *beta;
+    const int32_t *cu_seqlens;
+    const float *s0;
+    const int32_t *s0_idx;
+    int n_s0;
+    float *s_final;
+    void *out;
+    int B, T, Hk, Hv, dk, dv, chunk;
+    float scale;
+    int dt_qkv, dt_gate;
+    void *ws;
+    size_t ws_bytes;
+    uint32_t *err;
+};
+
+// Launchers: enqueue on `stream`, return cudaGetLastError().
+cudaError_t launch_recurrent(const RecurrentParams &p, cudaStream_t stream);
+cudaError_t launch_replay(const ReplayParams &p, cudaStream_t stream);
+cudaError_t launch_prefill_simt(const PrefillParams &p, cudaStream_t stream);
+bool prefill_simt_supported(int dk, int dv, int chunk);
+
+// ------------------------------------------------------------- helpers --
+
+__device__ __forceinline__ float ld_f(const float *p) { return *p; }
+__device__ __forceinline__ float ld_f(const __half *p) { return __half2float(*p); }
+__device__ __forceinline__ float ld_f(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+
+// Four consecutive elements widened to fp32 (p 16-byte aligned for float,
+// 8-byte aligned for the 16-bit types).
+__device__ __forceinline__ float4 ld4(const float *p) {
+    return *reinterpret_cast<const float4 *>(p);
+}
+__device__ __forceinline__ float4 ld4(const __half *p) {
+    uint2 u = *reinterpret_cast<const uint2 *>(p);
+    float2 a = __half22float2(*reinterpret_cast<__half2 *>(&u.x));
+    float2 b = __half22float2(*reinterpret_cast<__half2 *>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ float4 ld4(const __nv_bfloat16 *p) {
+    uint2 u = *reinterpret_cast<const uint2 *>(p);
+    float2 a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&u.x));
+    float2 b = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// Store fp32 as the output type, round-to-nearest-even.
+__device__ __forceinline__ void st_out(float *p, float x) { *p = x; }
+__device__ __forceinline__ void st_out(__half *p, float x) { *p = __float2half_rn(x); }
+__device__ __forceinline__ void st_out(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+
+// Gate value (alpha / beta) of runtime dtype `dt` at element `idx`.
+__device__ __forceinline__ float ld_gate(const void *p, long idx, int dt) {
+    if (dt == GDN_F32) return reinterpret_cast<const float *>(p)[idx];
+    if (dt == GDN_F16) return __half2float(reinterpret_cast<const __half *>(p)[idx]);
+    return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[idx]);
+}
+
+// Token range [tok0, tok0 + len) of row b.  With cu_seqlens, T is the
+// total token count the host validated the buffers for, and the bounds read
+// from the device are clamped to [0, T] so that no access leaves the inputs.
+__device__ __forceinline__ void row_range(const int32_t *cu, int b, int T,
+                                          long &tok0, int &len) {
+    if (cu == nullptr) {
+        tok0 = (long)b * T;
+        len = T;
+        return;
+    }
+    const long total = T;
+    long a = cu[b], e = cu[b + 1];
+    a = a < 0 ? 0 : (a > total ? total : a);
+    e = e < a ? a : (e > total ? total : e);
+    tok0 = a;
+    len = (int)(e - a);
+}
+
+// Initial-state matrix of (row b, head h) or nullptr for zeros.
+__device__ __forceinline__ const float *initial_state_ptr(const float *s0, const int32_t *idx,
+                                                          int n_s0, int b, int h, int Hv,
+                                                          int dv, int dk, uint32_t *err) {
+    if (s0 == nullptr) return nullptr;
+    long src = b;
+    if (idx != nullptr) {
+        src = idx[b];
+        if (src < 0 || src >= n_s0) {
+            atomicOr(err, (uint32_t)GDN_DEVERR_BAD_INDEX);
+            return nullptr;
+        }
+    }
+    return s0 + ((src * Hv + h) * (long)dv) * dk;
+}
+
+template <int W>
+__device__ __forceinline__ float group_sum(float x) {
+    // butterfly sum over aligned groups of W lanes (W a power of two <= 32)
+#pragma unroll
+    for (int o = W / 2; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+}  // namespace gdn

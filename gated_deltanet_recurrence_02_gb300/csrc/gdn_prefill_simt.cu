@@ -1,0 +1,298 @@
+// gdn_prefill_simt.cu -- chunked prefill on CUDA cores, fp32 throughout.
+//
+// "Enable the native Kev example on NVIDIA GPUs through ExecuTorch's AOTI CUDA
+// backend" (executorch issue 23097), work list: chunked GDN prefill with an
+// explicit initial and final state and an FP32 recurrence.  This is the
+// general-shape path (any dk, dv in {32, 64, 128}, chunk in {16, 32, 64}, any
+// storage dtype); the tensor-core kernel takes the dk = dv = 128, chunk = 64,
+// 16-bit case.
+//
+// One CTA (256 threads) carries a 32-row tile of one (row b, value head h)
+// state through all chunks of that row.  Inside a chunk of n tokens with start
+// state S0 and local log-decay sums g_t (gamma_t = e^{g_t}):
+//   A[t][i] = beta_t e^{g_t - g_i} k_t.k_i  (i < t),  P[t][i] = e^{g_t - g_i} q_t.k_i  (i <= t)
+//   R       = diag(beta) (V - diag(gamma) K S0^T)          [n x 32]
+//   Delta   = (I + A)^{-1} R                               forward substitution
+//   O       = diag(gamma) Q S0^T + P Delta
+//   S_end   = gamma_n S0 + Delta^T diag(e^{g_n - g}) K
+// (the UT/WY form; Delta equals U - W S0^T with U = T diag(beta) V and
+// W = T diag(beta gamma) K).  A ragged last chunk is padded with identity
+// tokens (k = q = v = 0, alpha = 1, beta = 0), which leave S unchanged and
+// whose outputs are not stored.  Precondition: every alpha in (0, 1].
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kDVT = 32;  // state rows per CTA
+
+template <int DK, int C>
+struct SimtSmem {
+    static constexpr int KS = DK + 4;   // row stride of S, K, Q
+    static constexpr int DS = kDVT + 4; // row stride of V/R/Delta, O
+    static constexpr int AS = C + 1;    // row stride of A, P
+    static constexpr int kFloats = kDVT * KS + 2 * C * KS + 2 * C * DS + 2 * C * AS + 4 * C;
+    static constexpr size_t kBytes = sizeof(float) * kFloats;
+};
+
+template <int DK, int C, typename TQ>
+__global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(const PrefillParams p) {
+    using L = SimtSmem<DK, C>;
+    constexpr int KS = L::KS, DS = L::DS, AS = L::AS;
+    extern __shared__ float4 smem4[];
+    float *Ss = reinterpret_cast<float *>(smem4);  // [32][KS]
+    float *Ks = Ss + kDVT * KS;                    // [C][KS]
+    float *Qs = Ks + C * KS;                       // [C][KS]  (scaled q)
+    float *Vs = Qs + C * KS;                       // [C][DS]  V tile -> R -> Delta
+    float *Os = Vs + C * DS;                       // [C][DS]  diag(gamma) Q S0^T
+    float *As = Os + C * DS;                       // [C][AS]
+    float *Ps = As + C * AS;                       // [C][AS]
+    float *lg = Ps + C * AS;                       // [C] log alpha, then g
+    float *bt = lg + C;                            // [C] beta
+    float *eg = bt + C;                            // [C] e^{g_t}
+    float *wg = eg + C;                            // [C] e^{g_last - g_t}
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int Hv = p.Hv, Hk = p.Hk, dv = p.dv;
+    const int hk = h / (Hv / Hk);
+    const int row0 = tile * kDVT;
+    long tok0;
+    int Tb;
+    row_range(p.cu_seqlens, b, p.T, tok0, Tb);
+
+    const TQ *qb = reinterpret_cast<const TQ *>(p.q);
+    const TQ *kb = reinterpret_cast<const TQ *>(p.k);
+    const TQ *vb = reinterpret_cast<const TQ *>(p.v);
+    TQ *ob = reinterpret_cast<TQ *>(p.out);
+    const float scale = p.scale;
+
+    const float *s0 = initial_state_ptr(p.s0, p.s0_idx, p.n_s0, b, h, Hv, dv, DK, p.err);
+    for (int e = tid; e < kDVT * DK / 4; e += kThreads) {
+        const int i = e / (DK / 4), j = (e % (DK / 4)) * 4;
+        float4 x = s0 ? *reinterpret_cast<const float4 *>(s0 + (long)(row0 + i) * DK + j)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4 *>(Ss + i * KS + j) = x;
+    }
+
+    for (int c0 = 0; c0 < Tb; c0 += C) {
+        const int n = (Tb - c0 < C) ? (Tb - c0) : C;
+        // ---- 1. stage the chunk (identity tokens past n) -------------------
+        for (int e = tid; e < C * DK / 4; e += kThreads) {
+            const int t = e / (DK / 4), j = (e % (DK / 4)) * 4;
+            float4 kk = make_float4(0.f, 0.f, 0.f, 0.f), qq = kk;
+            if (t < n) {
+                const long off = ((tok0 + c0 + t) * Hk + hk) * DK + j;
+                kk = ld4(kb + off);
+                qq = ld4(qb + off);
+                qq.x *= scale; qq.y *= scale; qq.z *= scale; qq.w *= scale;
+            }
+            *reinterpret_cast<float4 *>(Ks + t * KS + j) = kk;
+            *reinterpret_cast<float4 *>(Qs + t * KS + j) = qq;
+        }
+        for (int e = tid; e < C * kDVT; e += kThreads) {
+            const int t = e / kDVT, i = e % kDVT;
+            Vs[t * DS + i] = (t < n) ? ld_f(vb + ((tok0 + c0 + t) * Hv + h) * (long)dv + row0 + i) : 0.f;
+        }
+        for (int t = tid; t < C; t += kThreads) {
+            const long g = (tok0 + c0 + t) * Hv + h;
+            lg[t] = (t < n) ? logf(ld_gate(p.alpha, g, p.dt_gate)) : 0.f;
+            bt[t] = (t < n) ? ld_gate(p.beta, g, p.dt_gate) : 0.f;
+        }
+        __syncthreads();
+
+        // ---- 2. cumulative log decay (warp 0) ------------------------------
+        if (warp == 0) {
+            float x0 = (lane < C) ? lg[lane] : 0.f;
+            float x1 = (lane + 32 < C) ? lg[lane + 32] : 0.f;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                float y0 = __shfl_up_sync(0xffffffffu, x0, o);
+                float y1 = __shfl_up_sync(0xffffffffu, x1, o);
+                if (lane >= o) { x0 += y0; x1 += y1; }
+            }
+            x1 += __shfl_sync(0xffffffffu, x0, 31);
+            const float glast = (C > 32) ? __shfl_sync(0xffffffffu, x1, (C - 33) & 31)
+                                         : __shfl_sync(0xffffffffu, x0, (C - 1) & 31);
+            if (lane < C) { lg[lane] = x0; eg[lane] = expf(x0); wg[lane] = expf(glast - x0); }
+            if (lane + 32 < C) { lg[lane + 32] = x1; eg[lane + 32] = expf(x1); wg[lane + 32] = expf(glast - x1); }
+        }
+        __syncthreads();
+
+        // ---- 3a. A and P, 4x4 register blocks -------------------------------
+        constexpr int NB = C / 4;
+        for (int blk = tid; blk < NB * NB; blk += kThreads) {
+            const int t0 = (blk / NB) * 4, i0 = (blk % NB) * 4;
+            float kk[4][4] = {}, qk[4][4] = {};
+            if (i0 <= t0 + 3) {
+                for (int j = 0; j < DK; j += 4) {
+                    float4 kt[4], qt[4], ki[4];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        kt[r] = *reinterpret_cast<const float4 *>(Ks + (t0 + r) * KS + j);
+                        qt[r] = *reinterpret_cast<const float4 *>(Qs + (t0 + r) * KS + j);
+                        ki[r] = *reinterpret_cast<const float4 *>(Ks + (i0 + r) * KS + j);
+                    }
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            kk[r][c] += kt[r].x * ki[c].x + kt[r].y * ki[c].y + kt[r].z * ki[c].z + kt[r].w * ki[c].w;
+                            qk[r][c] += qt[r].x * ki[c].x + qt[r].y * ki[c].y + qt[r].z * ki[c].z + qt[r].w * ki[c].w;
+                        }
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int t = t0 + r, i = i0 + c;
+                    const float decay = (i <= t) ? expf(lg[t] - lg[i]) : 0.f;
+                    As[t * AS + i] = (i < t) ? bt[t] * decay * kk[r][c] : 0.f;
+                    Ps[t * AS + i] = (i <= t) ? decay * qk[r][c] : 0.f;
+                }
+        }
+
+        // ---- 3b. R (in place over V) and the inter-chunk readout ------------
+        constexpr int NB2 = (C / 4) * (kDVT / 4);
+        for (int w = tid; w < 2 * NB2; w += kThreads) {
+            const int kind = w / NB2, blk = w % NB2;
+            const int t0 = (blk / (kDVT / 4)) * 4, i0 = (blk % (kDVT / 4)) * 4;
+            const float *src = kind == 0 ? Ks : Qs;
+            float acc[4][4] = {};
+            for (int j = 0; j < DK; j += 4) {
+                float4 x[4], s[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    x[r] = *reinterpret_cast<const float4 *>(src + (t0 + r) * KS + j);
+                    s[r] = *reinterpret_cast<const float4 *>(Ss + (i0 + r) * KS + j);
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        acc[r][c] += x[r].x * s[c].x + x[r].y * s[c].y + x[r].z * s[c].z + x[r].w * s[c].w;
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int t = t0 + r, i = i0 + c;
+                    if (kind == 0)
+                        Vs[t * DS + i] = bt[t] * (Vs[t * DS + i] - eg[t] * acc[r][c]);
+                    else
+                        Os[t * DS + i] = eg[t] * acc[r][c];
+                }
+        }
+        __syncthreads();
+
+        // ---- 4. Delta = (I + A)^{-1} R: warp w owns columns 4w .. 4w+3 ------
+        {
+            const int part = lane & 7, i = warp * 4 + (lane >> 3);
+            for (int t = 0; t < C; ++t) {
+                float acc = 0.f;
+                for (int s = part; s < t; s += 8) acc += As[t * AS + s] * Vs[s * DS + i];
+                acc = group_sum<8>(acc);
+                if (part == 0) Vs[t * DS + i] -= acc;
+                __syncwarp();
+            }
+        }
+        __syncthreads();
+
+        // ---- 5a. outputs O = Os + P Delta -----------------------------------
+        for (int e = tid; e < C * kDVT; e += kThreads) {
+            const int t = e / kDVT, i = e % kDVT;
+            if (t < n) {
+                float acc = Os[t * DS + i];
+                for (int s = 0; s <= t; ++s) acc += Ps[t * AS + s] * Vs[s * DS + i];
+                st_out(ob + ((tok0 + c0 + t) * Hv + h) * (long)dv + row0 + i, acc);
+            }
+        }
+        // ---- 5b. S <- e^{g_last} S + Delta^T diag(e^{g_last - g}) K ----------
+        {
+            const float glast = eg[C - 1];
+            for (int blk = tid; blk < kDVT * DK / 16; blk += kThreads) {
+                const int i0 = (blk / (DK / 4)) * 4, j0 = (blk % (DK / 4)) * 4;
+                float4 acc[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    float4 s = *reinterpret_cast<const float4 *>(Ss + (i0 + r) * KS + j0);
+                    acc[r] = make_float4(glast * s.x, glast * s.y, glast * s.z, glast * s.w);
+                }
+                for (int s = 0; s < C; ++s) {
+                    const float4 d = *reinterpret_cast<const float4 *>(Vs + s * DS + i0);
+                    const float4 kk = *reinterpret_cast<const float4 *>(Ks + s * KS + j0);
+                    const float w = wg[s];
+                    const float dd[4] = {w * d.x, w * d.y, w * d.z, w * d.w};
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        acc[r].x += dd[r] * kk.x;
+                        acc[r].y += dd[r] * kk.y;
+                        acc[r].z += dd[r] * kk.z;
+                        acc[r].w += dd[r] * kk.w;
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    *reinterpret_cast<float4 *>(Ss + (i0 + r) * KS + j0) = acc[r];
+            }
+        }
+        __syncthreads();
+    }
+
+    if (p.s_final != nullptr) {
+        float *sf = p.s_final + (((long)b * Hv + h) * dv + row0) * DK;
+        for (int e = tid; e < kDVT * DK / 4; e += kThreads) {
+            const int i = e / (DK / 4), j = (e % (DK / 4)) * 4;
+            *reinterpret_cast<float4 *>(sf + (long)i * DK + j) =
+                *reinterpret_cast<const float4 *>(Ss + i * KS + j);
+        }
+    }
+}
+
+template <int DK, int C, typename TQ>
+cudaError_t launch_t(const PrefillParams &p, cudaStream_t stream) {
+    auto kern = prefill_simt_kernel<DK, C, TQ>;
+    const size_t bytes = SimtSmem<DK, C>::kBytes;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.dv / kDVT, p.Hv, p.B);
+    kern<<<grid, kThreads, bytes, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <int DK, int C>
+cudaError_t launch_c(const PrefillParams &p, cudaStream_t stream) {
+    switch (p.dt_qkv) {
+        case GDN_F32: return launch_t<DK, C, float>(p, stream);
+        case GDN_F16: return launch_t<DK, C, __half>(p, stream);
+        default: return launch_t<DK, C, __nv_bfloat16>(p, stream);
+    }
+}
+
+template <int DK>
+cudaError_t launch_dk(const PrefillParams &p, cudaStream_t stream) {
+    switch (p.chunk) {
+        case 16: return launch_c<DK, 16>(p, stream);
+        case 32: return launch_c<DK, 32>(p, stream);
+        default: return launch_c<DK, 64>(p, stream);
+    }
+}
+
+}  // namespace
+
+bool prefill_simt_supported(int dk, int dv, int chunk) {
+    return (dk == 32 || dk == 64 || dk == 128) && (dv == 32 || dv == 64 || dv == 128) &&
+           (chunk == 16 || chunk == 32 || chunk == 64);
+}
+
+cudaError_t launch_prefill_simt(const PrefillParams &p, cudaStream_t stream) {
+    switch (p.dk) {
+        case 32: return launch_dk<32>(p, stream);
+        case 64: return launch_dk<64>(p, stream);
+        default: return launch_dk<128>(p, stream);
+    }
+}
+
+}  // namespace gdn

@@ -1,0 +1,187 @@
+"""ctypes binding of libgdn (include/gdn.h): argument marshalling only.
+
+Every entry point keeps its C name.  Tensors are torch CUDA tensors (the
+library only sees their device pointers); shapes give the head counts and
+head sizes; the stream defaults to torch's current stream.  Outputs the caller
+does not pass are allocated here with torch (device memory is the only thing
+torch provides on this path).  Every step of the computation runs in the
+library's CUDA kernels; there is no other implementation to fall back to, so
+a missing library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+GDN_OK = 0
+GDN_F32, GDN_F16, GDN_BF16 = 0, 1, 2
+GDN_DEVERR_BAD_INDEX, GDN_DEVERR_TIMEOUT = 1, 2
+_DT = {torch.float32: GDN_F32, torch.float16: GDN_F16, torch.bfloat16: GDN_BF16}
+
+_lib = None
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libgdn.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"libgdn.so is not built ({path}); run "
+            "`python -c 'import __graft_entry__ as g; g.build()'` first")
+    L = ctypes.CDLL(path)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.gdn_prefill_workspace_size.argtypes = [i, i, i, i, i, i, i, i]
+    L.gdn_prefill_workspace_size.restype = sz
+    L.gdn_prefill_chunked.argtypes = [vp] * 8 + [i, vp, vp] + [i] * 8 + [f, i, i, vp, sz, vp]
+    L.gdn_prefill_chunked.restype = i
+    L.gdn_recurrent_capture.argtypes = ([vp] * 8 + [i, vp, vp] + [i] * 7 + [f, i, i]
+                                        + [i, vp, vp, vp, vp])
+    L.gdn_recurrent_capture.restype = i
+    L.gdn_replay_state_updates.argtypes = [vp, vp, vp, i, vp, i, i, i, i, i, vp]
+    L.gdn_replay_state_updates.restype = i
+    L.gdn_device_errors.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    L.gdn_device_errors.restype = i
+    L.gdn_status_string.argtypes = [i]
+    L.gdn_status_string.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def status_string(status: int) -> str:
+    return lib().gdn_status_string(int(status)).decode()
+
+
+def _p(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("libgdn takes device tensors")
+    if not t.is_contiguous():
+        raise ValueError("libgdn takes contiguous tensors")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str):
+    if status != GDN_OK:
+        raise GdnError(status, where)
+
+
+def slot_width(Hk: int, Hv: int, dk: int, dv: int) -> int:
+    """Floats per captured token: Hv decays, Hk*dk keys, Hv*dv deltas."""
+    return Hv + Hk * dk + Hv * dv
+
+
+def gdn_prefill_workspace_size(B, T, Hk, Hv, dk, dv, chunk, dtype_qkv) -> int:
+    return int(lib().gdn_prefill_workspace_size(B, T, Hk, Hv, dk, dv, chunk,
+                                                _DT.get(dtype_qkv, dtype_qkv)))
+
+
+def _dims(q, v, B, T, cu_seqlens):
+    total_T, Hk, dk = q.shape
+    _, Hv, dv = v.shape
+    if cu_seqlens is None and T is None:
+        T = total_T // B if B else 0
+    if cu_seqlens is not None:
+        T = total_T
+    return int(T), int(Hk), int(dk), int(Hv), int(dv)
+
+
+def gdn_prefill_chunked(q, k, v, alpha, beta, *, B: int, T: Optional[int] = None,
+                        cu_seqlens=None, initial_state=None,
+                        initial_state_indices=None, final_state=None, out=None,
+                        chunk: int = 64, scale: float = 1.0, workspace=None,
+                        want_final_state: bool = True, stream=None):
+    """Chunked prefill.  Returns (out, final_state)."""
+    T, Hk, dk, Hv, dv = _dims(q, v, B, T, cu_seqlens)
+    if out is None:
+        out = torch.empty_like(v)
+    if final_state is None and want_final_state:
+        final_state = torch.empty((B, Hv, dv, dk), dtype=torch.float32, device=v.device)
+    n0 = initial_state.shape[0] if initial_state is not None else 0
+    need = gdn_prefill_workspace_size(B, T, Hk, Hv, dk, dv, chunk, q.dtype)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=v.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().gdn_prefill_chunked(
+        _p(q), _p(k), _p(v), _p(alpha), _p(beta), _p(cu_seqlens), _p(initial_state),
+        _p(initial_state_indices), n0, _p(final_state), _p(out), B, T, Hk, Hk, Hv,
+        dk, dv, chunk, scale, _DT[q.dtype], _DT[alpha.dtype], _p(workspace),
+        ws_bytes, _stream(stream))
+    _check(st, "gdn_prefill_chunked")
+    return out, final_state
+
+
+def gdn_recurrent_capture(q, k, v, alpha, beta, *, B: int, T: Optional[int] = None,
+                          cu_seqlens=None, initial_state=None,
+                          initial_state_indices=None, final_state=None, out=None,
+                          scale: float = 1.0, state_update_capacity: int = 0,
+                          capture_count=None, state_update_active=None,
+                          state_update=None, want_final_state: bool = True,
+                          stream=None):
+    """Recurrent path with compact capture.  Returns (out, final_state,
+    state_update).  final_state may be initial_state itself (in place)."""
+    T, Hk, dk, Hv, dv = _dims(q, v, B, T, cu_seqlens)
+    if out is None:
+        out = torch.empty_like(v)
+    if final_state is None and want_final_state:
+        final_state = torch.empty((B, Hv, dv, dk), dtype=torch.float32, device=v.device)
+    cap = int(state_update_capacity)
+    if cap > 0 and state_update is None:
+        state_update = torch.empty((B, cap, slot_width(Hk, Hv, dk, dv)),
+                                   dtype=torch.float32, device=v.device)
+    n0 = initial_state.shape[0] if initial_state is not None else 0
+    st = lib().gdn_recurrent_capture(
+        _p(q), _p(k), _p(v), _p(alpha), _p(beta), _p(cu_seqlens), _p(initial_state),
+        _p(initial_state_indices), n0, _p(final_state), _p(out), B, T, Hk, Hk, Hv,
+        dk, dv, scale, _DT[q.dtype], _DT[alpha.dtype], cap, _p(capture_count),
+        _p(state_update_active), _p(state_update), _stream(stream))
+    _check(st, "gdn_recurrent_capture")
+    return out, final_state, state_update
+
+
+def gdn_replay_state_updates(state_in, state_update, accepted_count, *,
+                             state_update_capacity: int, Hk: int,
+                             state_out=None, stream=None):
+    """Replay the first accepted_count[b] captured slots onto state_in.
+    Returns state_out (state_in itself is allowed, in place)."""
+    B, Hv, dv, dk = state_in.shape
+    if state_out is None:
+        state_out = torch.empty_like(state_in)
+    st = lib().gdn_replay_state_updates(
+        _p(state_in), _p(state_out), _p(state_update), int(state_update_capacity),
+        _p(accepted_count), B, int(Hk), Hv, dk, dv, _stream(stream))
+    _check(st, "gdn_replay_state_updates")
+    return state_out
+
+
+def gdn_device_errors(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the GDN_DEVERR_* bits."""
+    flags = ctypes.c_uint32(0)
+    st = lib().gdn_device_errors(_stream(stream), ctypes.byref(flags))
+    if st not in (GDN_OK,):
+        raise GdnError(st, "gdn_device_errors")
+    return int(flags.value)

@@ -1,0 +1,388 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle on
+the same seeded inputs, for every workload, plus edge cases.
+
+Sources: the per-token gated delta rule of Gated DeltaNet; "[WebGPU EP] adds
+state update capacity support for GatedDeltaNet" (onnxruntime PR 32767),
+"Changes" and "Test Coverage" (compare only captured ranges while active, the
+whole buffer is zero while inactive, ragged capacity-7 cases with zero /
+partial / full counts, the fp16 Hq=2 / Hv=6 / 128 case); "Enable the native
+Kev example on NVIDIA GPUs through ExecuTorch's AOTI CUDA backend"
+(executorch issue 23097), work list (chunk boundaries, repeated prefix reuse).
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import TOL, TOL_CAPTURE, Guarded, rel, to_dev
+
+pytestmark = pytest.mark.gpu
+THREADS = min(32, os.cpu_count() or 4)
+
+
+@pytest.fixture(scope="module")
+def gdn():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gated_deltanet_recurrence_02_gb300 import build, gdn as g
+    build.build()
+    g.lib()
+    return g
+
+
+@pytest.fixture(scope="module")
+def W():
+    from gated_deltanet_recurrence_02_gb300.inputs import WORKLOADS
+    return WORKLOADS
+
+
+def _mk(w, **over):
+    from gated_deltanet_recurrence_02_gb300.inputs import make_inputs
+    kw = {k: w[k] for k in ("lengths", "Hk", "Hv", "dk", "dv", "dtype_qkv", "dtype_gate")}
+    kw.update(over)
+    return make_inputs(w["seed"], **kw)
+
+
+def _prefix_state(oracle_mod, x, b, n):
+    """Oracle state of row b after its first n tokens."""
+    t0 = int(x.cu_seqlens[b])
+    sl = slice(t0, t0 + n)
+    _, S, _ = oracle_mod.recurrent(x.q[sl], x.k[sl], x.v[sl], x.alpha[sl], x.beta[sl], B=1,
+                                   Hk=x.Hk, Hv=x.Hv, dk=x.dk, dv=x.dv, T=n,
+                                   initial_state=None if x.initial_state is None
+                                   else x.initial_state[b:b + 1])
+    return S[0]
+
+
+def _check_capture(su_gpu: Guarded, su_ref, counts, x, cap):
+    n = [max(0, min(int(c), cap, L)) for c, L in zip(counts, x.lengths)]
+    Hv, Hk, dk = x.Hv, x.Hk, x.dk
+    su = su_gpu.t
+    for b, nb in enumerate(n):
+        if nb > 0:
+            g = su[b, :nb].cpu().double().numpy()
+            r = su_ref[b, :nb]
+            # decay and key: exact widenings of the inputs
+            assert np.array_equal(g[:, :Hv + Hk * dk], r[:, :Hv + Hk * dk]), b
+            assert rel(su[b, :nb, Hv + Hk * dk:], r[:, Hv + Hk * dk:]) < TOL_CAPTURE, b
+        if nb < cap:
+            assert bool(torch.all(su_gpu.untouched((b, slice(nb, cap)))).item()), \
+                f"row {b}: uncaptured slots were written"
+    assert su_gpu.guards_intact()
+    return n
+
+
+# ---------------------------------------------------------------- tiny fp32
+
+def test_tiny_f32_recurrent_capture_replay(gdn, W, oracle_mod):
+    w = W["tiny_f32"]
+    x = _mk(w)
+    g = to_dev(x)
+    B, T, cap, counts = 2, 64, w["capacity"], w["capture_count"]
+    out = Guarded(tuple(x.v.shape), x.v.dtype)
+    fs = Guarded((B, x.Hv, x.dv, x.dk), torch.float32)
+    su = Guarded((B, cap, gdn.slot_width(x.Hk, x.Hv, x.dk, x.dv)), torch.float32)
+    cc = torch.tensor(counts, dtype=torch.int32, device="cuda")
+    gdn.gdn_recurrent_capture(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=B, T=T,
+                              initial_state=g["initial_state"], final_state=fs.t, out=out.t,
+                              state_update_capacity=cap, capture_count=cc, state_update=su.t)
+    torch.cuda.synchronize()
+    ro, rS, rsu = oracle_mod.recurrent(x.q, x.k, x.v, x.alpha, x.beta, B=B, Hk=x.Hk, Hv=x.Hv,
+                                       dk=x.dk, dv=x.dv, T=T, initial_state=x.initial_state,
+                                       capacity=cap, capture_count=counts)
+    assert rel(out.t, ro) < TOL[torch.float32]
+    assert rel(fs.t, rS) < TOL[torch.float32]
+    assert out.guards_intact() and fs.guards_intact()
+    n = _check_capture(su, rsu, counts, x, cap)
+    assert n == [3, 7]
+    # replay every accepted prefix (row 0 accepts at most its 3 captured tokens)
+    for m in range(cap + 1):
+        acc = [min(m, n[0]), m]
+        Sr = gdn.gdn_replay_state_updates(g["initial_state"], su.t,
+                                          torch.tensor(acc, dtype=torch.int32, device="cuda"),
+                                          state_update_capacity=cap, Hk=x.Hk)
+        for b in range(B):
+            assert rel(Sr[b], _prefix_state(oracle_mod, x, b, acc[b])) < TOL[torch.float32], (m, b)
+
+
+def test_tiny_f32_prefill_chunk16(gdn, W, oracle_mod):
+    w = W["tiny_f32"]
+    x = _mk(w)
+    g = to_dev(x)
+    out = Guarded(tuple(x.v.shape), x.v.dtype)
+    fs = Guarded((2, x.Hv, x.dv, x.dk), torch.float32)
+    gdn.gdn_prefill_chunked(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=2, T=64,
+                            initial_state=g["initial_state"], final_state=fs.t, out=out.t,
+                            chunk=w["chunk"])
+    torch.cuda.synchronize()
+    ro, rS = oracle_mod.chunked(x.q, x.k, x.v, x.alpha, x.beta, B=2, Hk=x.Hk, Hv=x.Hv,
+                                dk=x.dk, dv=x.dv, T=64, chunk=w["chunk"],
+                                initial_state=x.initial_state)
+    assert rel(out.t, ro) < TOL[torch.float32]
+    assert rel(fs.t, rS) < TOL[torch.float32]
+    assert out.guards_intact() and fs.guards_intact()
+
+
+# ------------------------------------------------- Qwen-like fp16 capture
+
+def test_qwenlike_f16_capture_inactive_replay(gdn, W, oracle_mod):
+    w = W["ragged_capture_qwenlike_f16"]
+    x = _mk(w)
+    g = to_dev(x)
+    B, T, cap, counts = 3, 8, w["capacity"], w["capture_count"]
+    slot = gdn.slot_width(x.Hk, x.Hv, x.dk, x.dv)
+    cc = torch.tensor(counts, dtype=torch.int32, device="cuda")
+    ro, rS, rsu = oracle_mod.recurrent(x.q, x.k, x.v, x.alpha, x.beta, B=B, Hk=x.Hk, Hv=x.Hv,
+                                       dk=x.dk, dv=x.dv, T=T, initial_state=x.initial_state,
+                                       capacity=cap, capture_count=counts)
+    outs = []
+    for active in (1, 0):
+        out = Guarded(tuple(x.v.shape), x.v.dtype)
+        fs = Guarded((B, x.Hv, x.dv, x.dk), torch.float32)
+        su = Guarded((B, cap, slot), torch.float32)
+        act = torch.tensor([active], dtype=torch.int32, device="cuda")
+        gdn.gdn_recurrent_capture(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=B, T=T,
+                                  initial_state=g["initial_state"], final_state=fs.t,
+                                  out=out.t, state_update_capacity=cap, capture_count=cc,
+                                  state_update_active=act, state_update=su.t)
+        torch.cuda.synchronize()
+        assert rel(out.t, ro) < TOL[torch.float16]
+        assert rel(fs.t, rS) < TOL[torch.float16]
+        assert out.guards_intact() and fs.guards_intact() and su.guards_intact()
+        outs.append((out.t.clone(), fs.t.clone()))
+        if active:
+            n = _check_capture(su, rsu, counts, x, cap)
+            assert n == [0, 4, 7]
+            su_active = su
+        else:
+            assert bool(torch.all(su.t == 0).item()), "inactive capture must be all zero"
+    # the flag changes nothing but the capture buffer
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    for m in range(cap + 1):
+        acc = [min(m, nb) for nb in n]
+        Sr = gdn.gdn_replay_state_updates(g["initial_state"], su_active.t,
+                                          torch.tensor(acc, dtype=torch.int32, device="cuda"),
+                                          state_update_capacity=cap, Hk=x.Hk)
+        for b in range(B):
+            assert rel(Sr[b], _prefix_state(oracle_mod, x, b, acc[b])) < TOL[torch.float16], (m, b)
+
+
+# ---------------------------------------------------- prefill T = 4100
+
+def test_prefill_T4100_bf16(gdn, W, oracle_mod):
+    w = W["prefill_T4100"]
+    x = _mk(w)
+    g = to_dev(x)
+    out = Guarded(tuple(x.v.shape), x.v.dtype)
+    fs = Guarded((1, x.Hv, x.dv, x.dk), torch.float32)
+    gdn.gdn_prefill_chunked(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=1, T=4100,
+                            initial_state=g["initial_state"], final_state=fs.t, out=out.t,
+                            chunk=w["chunk"])
+    o2, S2, _ = gdn.gdn_recurrent_capture(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=1,
+                                          T=4100, initial_state=g["initial_state"])
+    assert gdn.gdn_device_errors() == 0
+    ro, rS, _ = oracle_mod.recurrent(x.q, x.k, x.v, x.alpha, x.beta, B=1, Hk=x.Hk, Hv=x.Hv,
+                                     dk=x.dk, dv=x.dv, T=4100, initial_state=x.initial_state,
+                                     threads=THREADS)
+    assert out.guards_intact() and fs.guards_intact()
+    e_o, e_S = rel(out.t, ro), rel(fs.t, rS)
+    assert e_o < TOL[torch.bfloat16] and e_S < TOL[torch.bfloat16], (e_o, e_S)
+    # the per-token path on the same inputs
+    assert rel(o2, ro) < TOL[torch.bfloat16] and rel(S2, rS) < TOL[torch.bfloat16]
+    # per-chunk check of the ragged tail (last 4 tokens) and the first chunk
+    assert rel(out.t[-4:], ro[-4:]) < TOL[torch.bfloat16]
+    assert rel(out.t[:64], ro[:64]) < TOL[torch.bfloat16]
+
+
+# ------------------------------------------------ prefix snapshot reuse
+
+def test_prefix_snapshot_reuse_B12(gdn, W, oracle_mod):
+    from gated_deltanet_recurrence_02_gb300.inputs import make_inputs, ragged_lengths
+    w = W["prefix_snapshot_B12"]
+    dims = dict(Hk=w["Hk"], Hv=w["Hv"], dk=w["dk"], dv=w["dv"])
+    pre = make_inputs(w["seed"], lengths=[w["prefix_len"]], dtype_qkv=w["dtype_qkv"],
+                      dtype_gate=w["dtype_gate"], zero_state=True, **dims)
+    lens = ragged_lengths(w["seed"] + 1, w["B"], w["lo"], w["hi"])
+    x = make_inputs(w["seed"] + 2, lengths=lens, dtype_qkv=w["dtype_qkv"],
+                    dtype_gate=w["dtype_gate"], zero_state=True, **dims)
+    gp, g = to_dev(pre), to_dev(x)
+    B = w["B"]
+    # snapshot from the prefix, on each side
+    _, snap = gdn.gdn_prefill_chunked(gp["q"], gp["k"], gp["v"], gp["alpha"], gp["beta"], B=1,
+                                      T=w["prefix_len"], chunk=w["chunk"])
+    _, rsnap, _ = oracle_mod.recurrent(pre.q, pre.k, pre.v, pre.alpha, pre.beta, B=1,
+                                       T=w["prefix_len"], threads=THREADS, **dims)
+    torch.cuda.synchronize()
+    assert rel(snap, rsnap) < TOL[torch.bfloat16]
+    before = snap.clone()
+    idx = torch.zeros(B, dtype=torch.int32, device="cuda")
+    results = []
+    for _ in range(2):
+        o, fs = gdn.gdn_prefill_chunked(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=B,
+                                        cu_seqlens=g["cu_seqlens"], initial_state=snap,
+                                        initial_state_indices=idx, chunk=w["chunk"])
+        results.append((o.clone(), fs.clone()))
+    torch.cuda.synchronize()
+    assert torch.equal(snap.view(torch.int32), before.view(torch.int32)), "snapshot was modified"
+    assert torch.equal(results[0][0], results[1][0]) and torch.equal(results[0][1], results[1][1])
+    ro, rS, _ = oracle_mod.recurrent(x.q, x.k, x.v, x.alpha, x.beta, B=B,
+                                     cu_seqlens=x.cu_seqlens.numpy(), initial_state=rsnap,
+                                     initial_state_indices=[0] * B, threads=THREADS, **dims)
+    o, fs = results[0]
+    cu = x.cu_seqlens.tolist()
+    for b in range(B):
+        assert rel(o[cu[b]:cu[b + 1]], ro[cu[b]:cu[b + 1]]) < TOL[torch.bfloat16], b
+        assert rel(fs[b], rS[b]) < TOL[torch.bfloat16], b
+    assert gdn.gdn_device_errors() == 0
+
+
+# ------------------------------------------------------ decode B = 256
+
+def test_decode_B256_64_steps_sampled(gdn, W, oracle_mod):
+    from gated_deltanet_recurrence_02_gb300.inputs import capture_counts, make_inputs
+    w = W["decode_B256"]
+    B, steps, cap = w["B"], w["steps"], w["capacity"]
+    dims = dict(Hk=w["Hk"], Hv=w["Hv"], dk=w["dk"], dv=w["dv"])
+    x = make_inputs(w["seed"], lengths=[steps] * B, dtype_qkv=w["dtype_qkv"],
+                    dtype_gate=w["dtype_gate"], **dims)
+    counts = capture_counts(w["seed"] + 1, B, cap)
+    # step-major device copies: token t of every row, contiguous per step
+    def step_major(t):
+        return t.view(B, steps, *t.shape[1:]).transpose(0, 1).contiguous().cuda()
+    q, k, v, a, bt = (step_major(getattr(x, n)) for n in ("q", "k", "v", "alpha", "beta"))
+    S = x.initial_state.cuda()
+    cc = counts.cuda()
+    out = torch.empty_like(v)
+    su = torch.empty((B, cap, 16 * 128 + 32 + 32 * 128), dtype=torch.float32, device="cuda")
+    for t in range(steps):
+        gdn.gdn_recurrent_capture(q[t], k[t], v[t], a[t], bt[t], B=B, T=1, initial_state=S,
+                                  final_state=S, out=out[t], state_update_capacity=cap,
+                                  capture_count=cc, state_update=su)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    units = [(int(b), int(h)) for b, h in zip(rng.integers(0, B, 24), rng.integers(0, 32, 24))]
+    units += [(0, 0), (B - 1, 31)]
+    ro, rS, rsu = oracle_mod.recurrent(x.q, x.k, x.v, x.alpha, x.beta, B=B, T=steps,
+                                       initial_state=x.initial_state, capacity=steps,
+                                       capture_count=[steps] * B, units=units,
+                                       threads=THREADS, **dims)
+    Hv, Hk, dk, dv = 32, 16, 128, 128
+    o_rows = out.transpose(0, 1)  # [B, steps, Hv, dv]
+    ro = ro.reshape(B, steps, Hv, dv)
+    for b, h in units:
+        assert rel(S[b, h], rS[b, h]) < TOL[torch.bfloat16], (b, h)
+        assert rel(o_rows[b, :, h], ro[b, :, h]) < TOL[torch.bfloat16], (b, h)
+        if int(counts[b]) >= 1:  # the last step captured its token in slot 0
+            g = su[b, 0].cpu().double().numpy()
+            r = rsu[b, steps - 1]
+            assert g[h] == r[h]
+            hk = h // 2
+            if h % 2 == 0:
+                assert np.array_equal(g[Hv + hk * dk:Hv + (hk + 1) * dk],
+                                      r[Hv + hk * dk:Hv + (hk + 1) * dk])
+            off = Hv + Hk * dk + h * dv
+            assert rel(su[b, 0, off:off + dv], r[off:off + dv]) < TOL_CAPTURE
+    # inactive at full size: the whole buffer is cleared
+    act = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gdn.gdn_recurrent_capture(q[0], k[0], v[0], a[0], bt[0], B=B, T=1, initial_state=S,
+                              want_final_state=False, state_update_capacity=cap,
+                              capture_count=cc, state_update_active=act, state_update=su)
+    torch.cuda.synchronize()
+    assert bool(torch.all(su == 0).item())
+
+
+def test_decode_replay_B256(gdn, W, oracle_mod):
+    """Replay at decode shapes: capture 4 tokens, then replay accepted ~ U{0..4}."""
+    from gated_deltanet_recurrence_02_gb300.inputs import capture_counts, make_inputs
+    w = W["decode_B256"]
+    B, cap = w["B"], w["capacity"]
+    dims = dict(Hk=w["Hk"], Hv=w["Hv"], dk=w["dk"], dv=w["dv"])
+    x = make_inputs(w["seed"] + 10, lengths=[cap] * B, dtype_qkv="bf16", dtype_gate="bf16",
+                    **dims)
+    g = to_dev(x)
+    cc = torch.full((B,), cap, dtype=torch.int32, device="cuda")
+    _, _, su = gdn.gdn_recurrent_capture(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=B,
+                                         T=cap, initial_state=g["initial_state"],
+                                         state_update_capacity=cap, capture_count=cc,
+                                         want_final_state=False)
+    acc = capture_counts(w["seed"] + 11, B, cap)
+    Sr = gdn.gdn_replay_state_updates(g["initial_state"], su, acc.cuda(),
+                                      state_update_capacity=cap, Hk=16)
+    # in place on a copy gives the same bytes
+    S_ip = g["initial_state"].clone()
+    gdn.gdn_replay_state_updates(S_ip, su, acc.cuda(), state_update_capacity=cap, Hk=16,
+                                 state_out=S_ip)
+    torch.cuda.synchronize()
+    assert torch.equal(S_ip, Sr)
+    rng = np.random.default_rng(6)
+    for b in [int(v) for v in rng.integers(0, B, 12)]:
+        ref = _prefix_state(oracle_mod, x, b, int(acc[b]))
+        assert rel(Sr[b], ref) < TOL[torch.bfloat16], b
+
+
+# ------------------------------------------------------------ edge cases
+
+@pytest.mark.parametrize("dk,dv", [(32, 64), (64, 32), (128, 64), (64, 128)])
+@pytest.mark.parametrize("chunk", [16, 32, 64])
+def test_prefill_shapes_and_tails(gdn, oracle_mod, dk, dv, chunk):
+    from gated_deltanet_recurrence_02_gb300.inputs import make_inputs
+    lengths = [1, chunk - 1, chunk, chunk + 1, 0, 2 * chunk + 3]
+    x = make_inputs(77 + dk + dv + chunk, lengths=lengths, Hk=2, Hv=4, dk=dk, dv=dv,
+                    dtype_qkv="f32", dtype_gate="f32")
+    g = to_dev(x)
+    o, fs = gdn.gdn_prefill_chunked(g["q"], g["k"], g["v"], g["alpha"], g["beta"],
+                                    B=len(lengths), cu_seqlens=g["cu_seqlens"],
+                                    initial_state=g["initial_state"], chunk=chunk)
+    o2, fs2, _ = gdn.gdn_recurrent_capture(g["q"], g["k"], g["v"], g["alpha"], g["beta"],
+                                           B=len(lengths), cu_seqlens=g["cu_seqlens"],
+                                           initial_state=g["initial_state"])
+    torch.cuda.synchronize()
+    ro, rS, _ = oracle_mod.recurrent(x.q, x.k, x.v, x.alpha, x.beta, B=len(lengths), Hk=2,
+                                     Hv=4, dk=dk, dv=dv, cu_seqlens=x.cu_seqlens.numpy(),
+                                     initial_state=x.initial_state)
+    for got_o, got_S in ((o, fs), (o2, fs2)):
+        assert rel(got_o, ro) < TOL[torch.float32]
+        assert rel(got_S, rS) < TOL[torch.float32]
+    # the empty row keeps its initial state exactly
+    assert torch.equal(fs[4], g["initial_state"][4]) and torch.equal(fs2[4], g["initial_state"][4])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_no_initial_state_and_in_place(gdn, oracle_mod, dtype):
+    from gated_deltanet_recurrence_02_gb300.inputs import make_inputs
+    x = make_inputs(91, lengths=[70, 70], Hk=2, Hv=6, dk=128, dv=128, dtype_qkv=dtype,
+                    dtype_gate=dtype)
+    g = to_dev(x)
+    tol = TOL[torch.bfloat16]
+    # zero initial state (NULL pointer)
+    o, fs = gdn.gdn_prefill_chunked(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=2, T=70,
+                                    chunk=64)
+    ro, rS, _ = oracle_mod.recurrent(x.q, x.k, x.v, x.alpha, x.beta, B=2, Hk=2, Hv=6, dk=128,
+                                     dv=128, T=70)
+    assert rel(o, ro) < tol and rel(fs, rS) < tol
+    # in place, both entry points
+    S1 = g["initial_state"].clone()
+    gdn.gdn_prefill_chunked(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=2, T=70,
+                            initial_state=S1, final_state=S1, chunk=64)
+    S2 = g["initial_state"].clone()
+    gdn.gdn_recurrent_capture(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=2, T=70,
+                              initial_state=S2, final_state=S2)
+    torch.cuda.synchronize()
+    ro, rS, _ = oracle_mod.recurrent(x.q, x.k, x.v, x.alpha, x.beta, B=2, Hk=2, Hv=6, dk=128,
+                                     dv=128, T=70, initial_state=x.initial_state)
+    assert rel(S1, rS) < tol and rel(S2, rS) < tol
+
+
+def test_bad_snapshot_index_sets_flag(gdn):
+    from gated_deltanet_recurrence_02_gb300.inputs import make_inputs
+    x = make_inputs(5, lengths=[3, 3], Hk=1, Hv=2, dk=32, dv=32, dtype_qkv="f32",
+                    dtype_gate="f32", n_states=1)
+    g = to_dev(x)
+    idx = torch.tensor([0, 5], dtype=torch.int32, device="cuda")
+    gdn.gdn_device_errors()
+    gdn.gdn_recurrent_capture(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=2, T=3,
+                              initial_state=g["initial_state"], initial_state_indices=idx)
+    flags = gdn.gdn_device_errors()
+    assert flags & gdn.GDN_DEVERR_BAD_INDEX
+    assert gdn.gdn_device_errors() == 0

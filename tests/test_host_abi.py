@@ -1,0 +1,151 @@
+"""Host-side checks of the C ABI: the library loads, exports every entry
+point that include/gdn.h declares, and rejects bad arguments before any
+launch.  No GPU is touched: every call here fails validation first, and the
+fake device addresses are never dereferenced."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from gated_deltanet_recurrence_02_gb300 import build, gdn
+    build.build()
+    return gdn.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    return sorted(set(re.findall(r"GDN_API\s+[\w\s\*]*?\b(gdn_\w+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared()
+    assert len(names) >= 6
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    from gated_deltanet_recurrence_02_gb300 import gdn
+    assert gdn.status_string(0) == "ok"
+    for s in range(1, 8):
+        assert gdn.status_string(s) not in ("ok", "unknown status")
+
+
+A = 1 << 32  # fake, 16-byte aligned "device" addresses, far apart
+GiB = 1 << 30
+
+
+def rec(L, **kw):
+    a = dict(q=A, k=A + GiB, v=A + 2 * GiB, alpha=A + 3 * GiB, beta=A + 4 * GiB, cu=None,
+             s0=A + 5 * GiB, idx=None, n0=2, sf=A + 6 * GiB, out=A + 7 * GiB, B=2, T=8,
+             Hq=2, Hk=2, Hv=6, dk=128, dv=128, scale=1.0, dtq=2, dtg=2, cap=4,
+             cc=A + 8 * GiB, act=None, su=A + 9 * GiB)
+    a.update(kw)
+    return L.gdn_recurrent_capture(a["q"], a["k"], a["v"], a["alpha"], a["beta"], a["cu"],
+                                   a["s0"], a["idx"], a["n0"], a["sf"], a["out"], a["B"],
+                                   a["T"], a["Hq"], a["Hk"], a["Hv"], a["dk"], a["dv"],
+                                   a["scale"], a["dtq"], a["dtg"], a["cap"], a["cc"],
+                                   a["act"], a["su"], None)
+
+
+def pre(L, **kw):
+    a = dict(q=A, k=A + GiB, v=A + 2 * GiB, alpha=A + 3 * GiB, beta=A + 4 * GiB, cu=None,
+             s0=A + 5 * GiB, idx=None, n0=1, sf=A + 6 * GiB, out=A + 7 * GiB, B=1, T=100,
+             Hq=16, Hk=16, Hv=32, dk=128, dv=128, chunk=64, scale=1.0, dtq=2, dtg=0,
+             ws=None, wsb=0)
+    a.update(kw)
+    return L.gdn_prefill_chunked(a["q"], a["k"], a["v"], a["alpha"], a["beta"], a["cu"],
+                                 a["s0"], a["idx"], a["n0"], a["sf"], a["out"], a["B"],
+                                 a["T"], a["Hq"], a["Hk"], a["Hv"], a["dk"], a["dv"],
+                                 a["chunk"], a["scale"], a["dtq"], a["dtg"], a["ws"],
+                                 a["wsb"], None)
+
+
+def rep(L, **kw):
+    a = dict(si=A, so=A + GiB, su=A + 2 * GiB, cap=4, acc=A + 3 * GiB, B=2, Hk=2, Hv=6,
+             dk=128, dv=128)
+    a.update(kw)
+    return L.gdn_replay_state_updates(a["si"], a["so"], a["su"], a["cap"], a["acc"], a["B"],
+                                      a["Hk"], a["Hv"], a["dk"], a["dv"], None)
+
+
+INVALID, UNSUP, ALIAS, ALIGN, WS = 1, 2, 3, 4, 7
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Hq=1), INVALID),                   # Hq != Hk
+    (dict(Hv=5), INVALID),                   # Hv % Hk != 0
+    (dict(B=-1), INVALID),
+    (dict(T=-3), INVALID),
+    (dict(cap=-1), INVALID),
+    (dict(cc=None), INVALID),                # capacity > 0 needs capture_count
+    (dict(su=None), INVALID),                # ... and the output buffer
+    (dict(q=None), INVALID),
+    (dict(dtq=7), INVALID),
+    (dict(dk=96), UNSUP),
+    (dict(dv=256), UNSUP),
+    (dict(q=A + 8), ALIGN),
+    (dict(su=A + 9 * GiB + 4), ALIGN),
+    (dict(cc=A + 8 * GiB + 2), ALIGN),
+    (dict(out=A + 16), ALIAS),               # out overlaps q
+    (dict(su=A + 7 * GiB + 64), ALIAS),      # capture overlaps out
+    (dict(sf=A + 5 * GiB + 4096), ALIAS),    # partial overlap with the initial state
+    (dict(sf=A + 5 * GiB, idx=A + 10 * GiB), ALIAS),  # in place with shared snapshots
+    (dict(s0=None, idx=A + 10 * GiB), INVALID),
+    (dict(n0=1), INVALID),                   # fewer initial states than rows
+])
+def test_recurrent_rejects(L, kw, code):
+    assert rec(L, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(chunk=48), UNSUP),
+    (dict(chunk=128), UNSUP),
+    (dict(Hq=8), INVALID),
+    (dict(dk=16), UNSUP),
+    (dict(alpha=A + 3 * GiB + 8), ALIGN),
+    (dict(out=A + 2 * GiB), ALIAS),          # out is v
+    (dict(sf=A + 7 * GiB + 128), ALIAS),     # final state overlaps out
+    (dict(dtg=3), INVALID),
+])
+def test_prefill_rejects(L, kw, code):
+    assert pre(L, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(cap=-2), INVALID),
+    (dict(Hv=7), INVALID),
+    (dict(dk=48), UNSUP),
+    (dict(so=A + 16), ALIAS),                # partial in-place overlap
+    (dict(so=A + 2 * GiB), ALIAS),           # output over the factors
+    (dict(si=A + 4), ALIGN),
+    (dict(acc=None), INVALID),
+])
+def test_replay_rejects(L, kw, code):
+    assert rep(L, **kw) == code
+
+
+def test_empty_batch_is_a_no_op(L):
+    # B = 0 passes validation and returns before any CUDA call.
+    assert rec(L, B=0, T=0) == 0
+    assert pre(L, B=0, T=0) == 0
+    assert rep(L, B=0) == 0
+
+
+def test_workspace_size_query(L):
+    assert L.gdn_prefill_workspace_size(1, 4100, 16, 32, 128, 128, 64, 2) != ctypes.c_size_t(-1).value
+    assert L.gdn_prefill_workspace_size(-1, 4100, 16, 32, 128, 128, 64, 2) == ctypes.c_size_t(-1).value
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    from gated_deltanet_recurrence_02_gb300 import build, gdn
+    monkeypatch.setattr(build, "LIB", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(gdn, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        gdn.lib()
