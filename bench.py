@@ -1,0 +1,585 @@
+#!/usr/bin/env python
+"""Benchmark of the gated delta-rule hot path on one GB300.
+
+One step is one pass of the whole path over one batch of synthetic input:
+  1. chunked prefill     B=1, T=4100, Hk=16, Hv=32, dk=dv=128, chunk 64, bf16
+                         q/k/v, fp32 alpha/beta, random fp32 initial state;
+  2. decode with capture B=256 rows, 64 sequential single-token calls, same
+                         heads, bf16 q/k/v/alpha/beta, the fp32 state updated
+                         in place in HBM, capacity 4, capture_count ~ U{0..4};
+  3. replay              the decode state, capacity 4, accepted ~ U{0..4},
+                         written to a separate output state.
+The headline `value` is the decode phase's state throughput (algorithmic
+bytes moved per second: state read + write, token vectors, outputs and
+captured factors).  Prefill tokens/s and replay GB/s ride along in
+"prefill" / "replay".  Inputs are resident in HBM before the timed region;
+the decode state (512 MiB) is larger than L2, and the L2 is flushed (a
+256 MiB write) before every prefill, outside the phase timers.
+
+`--impl reference` times the fp64 CPU oracle on a bounded sample of the same
+decode workload instead (rank 0 only).  Multi-GPU (torchrun): every rank runs
+the same per-GPU workload on its own rows (weak scaling, no data-path
+collective); only the barrier and the max/sum of timings cross ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GDN prefill tokens/s & decode state GB/s on 1 GB300, % of roofline"
+
+# workload shapes
+DEC = dict(B=256, steps=64, Hk=16, Hv=32, dk=128, dv=128, cap=4, seed=1004)
+PRE = dict(T=4100, Hk=16, Hv=32, dk=128, dv=128, chunk=64, seed=1002)
+REP_SEED = 2004
+CPU_SAMPLE_ROWS = 128  # oracle sample: 128 rows x 32 heads x 64 tokens
+
+
+# ----------------------------------------------------------- distributed --
+
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, 0
+    import torch
+    import torch.distributed as dist
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    dist.init_process_group(backend=backend)
+    return dist.get_rank(), dist.get_world_size(), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def reduce_scalar(x: float, op: str, device=None) -> float:
+    """max / sum of a per-rank scalar over all ranks (identity when alone)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        reasons = sorted({self.NAMES[i] for r in rows for i in range(4)
+                          if r[5 + i].lower().startswith("active")})
+        top = sorted(sm)[len(sm) // 2:] if sm else []  # samples under load
+        return {"sm_mhz": statistics.median(top) if top else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+# ------------------------------------------------------------- workloads --
+
+def decode_bytes(counts, d=DEC) -> int:
+    """Algorithmic bytes of ONE decode call over all rows: fp32 state read and
+    written, bf16 q, k, v, alpha, beta read, bf16 o written, int32 counts read,
+    and the captured slot (decay, keys, deltas in fp32) of every row whose
+    clamped count is >= 1 (T = 1 per call)."""
+    B, Hk, Hv, dk, dv = d["B"], d["Hk"], d["Hv"], d["dk"], d["dv"]
+    state = 2 * B * Hv * dv * dk * 4
+    vecs = B * (2 * Hk * dk + 2 * Hv * dv + 2 * Hv) * 2 + B * 4
+    slot = (Hv + Hk * dk + Hv * dv) * 4
+    cap_rows = sum(1 for c in counts if min(max(int(c), 0), d["cap"], 1) >= 1)
+    return state + vecs + cap_rows * slot
+
+
+def replay_bytes(accepted, d=DEC) -> int:
+    """State read + write for every row, plus the slots each row replays."""
+    B, Hk, Hv, dk, dv = d["B"], d["Hk"], d["Hv"], d["dk"], d["dv"]
+    slot = (Hv + Hk * dk + Hv * dv) * 4
+    return 2 * B * Hv * dv * dk * 4 + sum(min(max(int(a), 0), d["cap"]) for a in accepted) * slot + B * 4
+
+
+def prefill_bytes_flops(p=PRE):
+    """Minimum HBM bytes and the chunked form's flops of one prefill call."""
+    T, Hk, Hv, dk, dv, C = p["T"], p["Hk"], p["Hv"], p["dk"], p["dv"], p["chunk"]
+    byts = (2 * T * Hk * dk * 2 + 2 * T * Hv * dv * 2 + 2 * T * Hv * 4
+            + 2 * Hv * dv * dk * 4)
+    flops = T * Hv * (6 * dk * dv + 10 * C * dk)
+    return byts, flops
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------ our arm ----
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from gated_deltanet_recurrence_02_gb300 import gdn
+    from gated_deltanet_recurrence_02_gb300.inputs import capture_counts, make_inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    gdn.lib()
+    stream = torch.cuda.current_stream()
+    d = dict(DEC, B=args.decode_rows)
+    do_pre, do_dec, do_rep = (args.only in ("all", ph) for ph in ("prefill", "decode", "replay"))
+    B, S_, Hk, Hv, dk, dv, cap = d["B"], d["steps"], d["Hk"], d["Hv"], d["dk"], d["dv"], d["cap"]
+
+    # ---- decode inputs (step-major on the device) ----
+    x = make_inputs(d["seed"] + 100 * rank, lengths=[S_] * B, Hk=Hk, Hv=Hv, dk=dk, dv=dv,
+                    dtype_qkv="bf16", dtype_gate="bf16")
+    counts = capture_counts(d["seed"] + 1 + 100 * rank, B, cap)
+
+    def step_major_host(t):
+        return t.view(B, S_, *t.shape[1:]).transpose(0, 1).contiguous()
+    hq, hk_, hv, ha, hb = (step_major_host(getattr(x, n)) for n in ("q", "k", "v", "alpha", "beta"))
+    S0_host = x.initial_state
+    q, k, v, a, bt = (t.to(dev) for t in (hq, hk_, hv, ha, hb))
+    S = S0_host.to(dev)
+    cc = counts.to(dev)
+    out = torch.empty_like(v)
+    slot = gdn.slot_width(Hk, Hv, dk, dv)
+    su = torch.empty((B, cap, slot), dtype=torch.float32, device=dev)
+
+    # ---- replay inputs: a capacity-4 capture of 4 tokens, accepted ~ U{0..4}
+    xr = make_inputs(REP_SEED + 100 * rank, lengths=[cap] * B, Hk=Hk, Hv=Hv, dk=dk, dv=dv,
+                     dtype_qkv="bf16", dtype_gate="bf16", zero_state=True)
+    gr = {n: getattr(xr, n).to(dev) for n in ("q", "k", "v", "alpha", "beta")}
+    su_r = torch.empty((B, cap, slot), dtype=torch.float32, device=dev)
+    gdn.gdn_recurrent_capture(gr["q"], gr["k"], gr["v"], gr["alpha"], gr["beta"], B=B, T=cap,
+                              state_update_capacity=cap,
+                              capture_count=torch.full((B,), cap, dtype=torch.int32, device=dev),
+                              state_update=su_r, want_final_state=False)
+    accepted = capture_counts(REP_SEED + 1 + 100 * rank, B, cap)
+    acc_d = accepted.to(dev)
+    S_rep = torch.empty_like(S)
+
+    # ---- prefill inputs ----
+    p = PRE
+    xp = make_inputs(p["seed"] + 100 * rank, lengths=[p["T"]], Hk=p["Hk"], Hv=p["Hv"],
+                     dk=p["dk"], dv=p["dv"], dtype_qkv="bf16", dtype_gate="f32")
+    gp = {n: getattr(xp, n).to(dev) for n in ("q", "k", "v", "alpha", "beta", "initial_state")}
+    p_out = torch.empty_like(gp["v"])
+    p_fs = torch.empty((1, p["Hv"], p["dv"], p["dk"]), dtype=torch.float32, device=dev)
+    ws_n = gdn.gdn_prefill_workspace_size(1, p["T"], p["Hk"], p["Hv"], p["dk"], p["dv"],
+                                          p["chunk"], torch.bfloat16)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def prefill():
+        gdn.gdn_prefill_chunked(gp["q"], gp["k"], gp["v"], gp["alpha"], gp["beta"], B=1,
+                                T=p["T"], initial_state=gp["initial_state"], final_state=p_fs,
+                                out=p_out, chunk=p["chunk"], workspace=ws)
+
+    def decode_call(t):
+        gdn.gdn_recurrent_capture(q[t], k[t], v[t], a[t], bt[t], B=B, T=1, initial_state=S,
+                                  final_state=S, out=out[t], state_update_capacity=cap,
+                                  capture_count=cc, state_update=su)
+
+    def replay():
+        gdn.gdn_replay_state_updates(S, su_r, acc_d, state_update_capacity=cap, Hk=Hk,
+                                     state_out=S_rep)
+
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    n_ev = S_ + 4
+    ev = [[E() for _ in range(n_ev)] for _ in range(args.steps)]
+
+    def step(evs=None):
+        flush.fill_(1)
+        if evs: evs[0].record(stream)
+        if do_pre:
+            prefill()
+        if evs: evs[1].record(stream)
+        for t in range(S_):
+            if do_dec:
+                decode_call(t)
+            if evs: evs[2 + t].record(stream)
+        if do_rep:
+            replay()
+        if evs: evs[2 + S_].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for s in range(args.steps):
+        step(ev[s])
+    torch.cuda.synchronize()
+    barrier()
+    t_wall = time.perf_counter() - t_wall
+    clocks = sampler.stop() if sampler else None
+
+    pre_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)]
+    dec_launch_ms = [ev[s][1 + t].elapsed_time(ev[s][2 + t])
+                     for s in range(args.steps) for t in range(S_)]
+    dec_ms = [ev[s][1].elapsed_time(ev[s][1 + S_]) for s in range(args.steps)]
+    rep_ms = [ev[s][1 + S_].elapsed_time(ev[s][2 + S_]) for s in range(args.steps)]
+    assert torch.isfinite(out).all() and torch.isfinite(S).all() and torch.isfinite(p_out.float()).all()
+
+    if args.only != "all":
+        # profiling mode: one phase only, no JSON contract line
+        return {"only": args.only, "decode_rows": B, "prefill_ms": statistics.mean(pre_ms),
+                "decode_ms": statistics.mean(dec_ms), "replay_ms": statistics.mean(rep_ms)}
+    dec_bytes_call = decode_bytes(counts.tolist(), d)
+    dec_total_bytes = dec_bytes_call * S_ * args.steps
+    dec_time = reduce_scalar(sum(dec_ms) / 1e3, "max", dev)
+    all_bytes = reduce_scalar(dec_total_bytes, "sum", dev)
+    value = all_bytes / dec_time / 1e9
+
+    hbm_peak, tf_peak, peak_kind = load_peaks()
+    launch_avg_s = statistics.mean(dec_launch_ms) / 1e3
+    achieved = dec_bytes_call / launch_avg_s / 1e9
+    pb, pf = prefill_bytes_flops()
+    pre_avg_s = statistics.mean(pre_ms) / 1e3
+    pre_time = reduce_scalar(sum(pre_ms) / 1e3, "max", dev)
+    pre_tokens = reduce_scalar(p["T"] * args.steps, "sum", dev)
+    rep_bytes_call = replay_bytes(accepted.tolist())
+    rep_avg_s = statistics.mean(rep_ms) / 1e3
+    ms_per_step = (sum(pre_ms) + sum(dec_ms) + sum(rep_ms)) / args.steps
+    ms_per_step = reduce_scalar(ms_per_step, "max", dev)
+
+    # ---- end to end through the public API with host buffers (decode) ----
+    e2e = run_e2e(args, gdn, dev, stream, hq, hk_, hv, ha, hb, S0_host, counts, d)
+    e2e_pre = run_e2e_prefill(args, gdn, dev, stream, xp)
+
+    line = None
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "storage_dtype": "bf16",
+            "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), "
+                    "beta=sigmoid(N(0,1)), alpha=exp(-U(0.01,0.5)), S0=0.1*N(0,1))",
+            "config": {
+                "workload": "decode_B256: B=256 rows x 64 single-token steps, Hq=Hk=16, Hv=32, "
+                            "dk=dv=128, bf16 q/k/v/alpha/beta, fp32 state in place, capture "
+                            "capacity 4, capture_count~U{0..4}; plus prefill_T4100 and replay",
+                "B": B, "steps_per_call_chain": S_, "Hk": Hk, "Hv": Hv, "dk": dk, "dv": dv,
+                "capacity": cap,
+                "l2": "decode state 512 MiB > L2 (inputs larger than L2); "
+                      "L2 flushed by a 256 MiB write before each prefill",
+                "parallelism": f"replicas x{world} (rows independent)",
+            },
+            "roofline": {
+                "kernel": "recurrent_kernel<128,bf16> (decode, T=1)",
+                "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
+                "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
+                "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                "algorithmic_bytes_per_launch": dec_bytes_call,
+                "avg_launch_us": round(launch_avg_s * 1e6, 2),
+            },
+            "prefill": {
+                "workload": "prefill_T4100: B=1, T=4100, Hk=16, Hv=32, d=128, chunk 64, bf16 "
+                            "q/k/v, fp32 alpha/beta and state",
+                "value": round(pre_tokens / pre_time, 1), "unit": "tokens/s",
+                "avg_launch_us": round(pre_avg_s * 1e6, 2),
+                "roofline": {
+                    "bound": "hbm", "achieved": round(pb / pre_avg_s / 1e9, 1),
+                    "peak": hbm_peak, "unit": "GB/s",
+                    "frac": round(pb / pre_avg_s / 1e9 / hbm_peak, 4),
+                    "algorithmic_bytes_per_launch": pb,
+                    "tensor_frac": round(pf / pre_avg_s / 1e12 / tf_peak, 4),
+                    "algorithmic_flops_per_launch": pf, "traffic": None,
+                },
+                "e2e": e2e_pre,
+            },
+            "replay": {
+                "value": round(rep_bytes_call / rep_avg_s / 1e9, 1), "unit": "GB/s",
+                "avg_launch_us": round(rep_avg_s * 1e6, 2),
+                "frac": round(rep_bytes_call / rep_avg_s / 1e9 / hbm_peak, 4),
+                "algorithmic_bytes_per_launch": rep_bytes_call,
+            },
+            "e2e": e2e,
+            "gpu_launches": args.steps * (PREFILL_LAUNCHES + S_ + 1),
+            "clocks": clocks,
+            "wall_s_timed_region": round(t_wall, 4),
+        }
+    return line
+
+
+PREFILL_LAUNCHES = 1  # kernels one gdn_prefill_chunked call launches on this workload
+
+
+def run_e2e(args, gdn, dev, stream, hq, hk_, hv, ha, hb, S0_host, counts, d):
+    """Decode through the public API with host-resident data: every step copies
+    the initial state and the 64 tokens' inputs from pinned host memory, runs
+    the 64 calls, and copies the final state, outputs and capture back."""
+    import torch
+    B, S_, cap = d["B"], d["steps"], d["cap"]
+    pin = lambda t: t.pin_memory()  # noqa: E731
+    h_in = [pin(t) for t in (hq, hk_, hv, ha, hb)]
+    h_S0, h_cc = pin(S0_host), pin(counts)
+    d_in = [torch.empty_like(t, device=dev) for t in h_in]
+    d_S = torch.empty_like(h_S0, device=dev)
+    d_cc = torch.empty_like(h_cc, device=dev)
+    d_out = torch.empty_like(d_in[2])
+    slot = gdn.slot_width(d["Hk"], d["Hv"], d["dk"], d["dv"])
+    d_su = torch.empty((B, cap, slot), dtype=torch.float32, device=dev)
+    h_S = torch.empty_like(h_S0).pin_memory()
+    h_out = torch.empty_like(d_out, device="cpu").pin_memory()
+    h_su = torch.empty_like(d_su, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in h_in) + h_S0.numel() * 4 + h_cc.numel() * 4
+    d2h = h_S.numel() * 4 + h_out.numel() * h_out.element_size() + h_su.numel() * 4
+
+    def one():
+        for dt, ht in zip(d_in, h_in):
+            dt.copy_(ht, non_blocking=True)
+        d_S.copy_(h_S0, non_blocking=True)
+        d_cc.copy_(h_cc, non_blocking=True)
+        q, k, v, a, bt = d_in
+        for t in range(S_):
+            gdn.gdn_recurrent_capture(q[t], k[t], v[t], a[t], bt[t], B=B, T=1, initial_state=d_S,
+                                      final_state=d_S, out=d_out[t], state_update_capacity=cap,
+                                      capture_count=d_cc, state_update=d_su)
+        h_S.copy_(d_S, non_blocking=True)
+        h_out.copy_(d_out, non_blocking=True)
+        h_su.copy_(d_su, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(1, args.steps // 2)
+    e0.record(stream)
+    for _ in range(n):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sec = e0.elapsed_time(e1) / 1e3
+    byts = decode_bytes(counts.tolist(), d) * S_ * n
+    val = reduce_scalar(byts, "sum", dev) / reduce_scalar(sec, "max", dev) / 1e9
+    return {"value": round(val, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": n}
+
+
+def run_e2e_prefill(args, gdn, dev, stream, xp):
+    """Prefill through the public API with host-resident inputs and results."""
+    import torch
+    names = ("q", "k", "v", "alpha", "beta", "initial_state")
+    h = {n: getattr(xp, n).pin_memory() for n in names}
+    dd = {n: torch.empty_like(h[n], device=dev) for n in names}
+    d_out = torch.empty_like(dd["v"])
+    d_fs = torch.empty_like(dd["initial_state"])
+    h_out = torch.empty_like(d_out, device="cpu").pin_memory()
+    h_fs = torch.empty_like(d_fs, device="cpu").pin_memory()
+    T = PRE["T"]
+
+    def one():
+        for n in names:
+            dd[n].copy_(h[n], non_blocking=True)
+        gdn.gdn_prefill_chunked(dd["q"], dd["k"], dd["v"], dd["alpha"], dd["beta"], B=1, T=T,
+                                initial_state=dd["initial_state"], final_state=d_fs, out=d_out,
+                                chunk=PRE["chunk"])
+        h_out.copy_(d_out, non_blocking=True)
+        h_fs.copy_(d_fs, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(1, args.steps)
+    e0.record(stream)
+    for _ in range(n):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sec = e0.elapsed_time(e1) / 1e3
+    val = reduce_scalar(T * n, "sum", dev) / reduce_scalar(sec, "max", dev)
+    return {"value": round(val, 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in h.values())),
+            "d2h_bytes_per_step": int(h_out.numel() * 2 + h_fs.numel() * 4)}
+
+
+# ------------------------------------------------------ oracle (CPU) arm --
+
+def oracle_decode_sample(rows: int, seed: int):
+    """Inputs of a bounded slice of the decode workload: `rows` rows, all 32
+    heads, 64 tokens each (the same per-row recipe as the GPU run)."""
+    from gated_deltanet_recurrence_02_gb300.inputs import make_inputs
+    d = DEC
+    return make_inputs(seed, lengths=[d["steps"]] * rows, Hk=d["Hk"], Hv=d["Hv"], dk=d["dk"],
+                       dv=d["dv"], dtype_qkv="bf16", dtype_gate="bf16")
+
+
+def time_oracle_decode(x, rows: int, threads: int):
+    import oracle
+    from gated_deltanet_recurrence_02_gb300.inputs import capture_counts
+    d = DEC
+    counts = capture_counts(d["seed"] + 1, rows, d["cap"]).tolist()
+    t0 = time.perf_counter()
+    oracle.recurrent(x.q, x.k, x.v, x.alpha, x.beta, B=rows, T=d["steps"], Hk=d["Hk"],
+                     Hv=d["Hv"], dk=d["dk"], dv=d["dv"], initial_state=x.initial_state,
+                     capacity=d["cap"], capture_count=counts, threads=threads)
+    sec = time.perf_counter() - t0
+    # the same algorithmic bytes per (row, step) as the GPU figure
+    byts = decode_bytes(counts, dict(d, B=rows)) * d["steps"]
+    return byts / sec / 1e9, sec
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline():
+    import oracle
+    oracle.build()
+    cores = cpu_cores()
+    rows = CPU_SAMPLE_ROWS
+    x = oracle_decode_sample(rows, DEC["seed"])
+    val, sec = time_oracle_decode(x, rows, cores)
+    return {"value": round(val, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"decode: {rows} of 256 rows x 32 heads x 64 single-token steps "
+                      f"(fp64 C oracle, {cores} threads over (row, head) units, "
+                      f"{sec:.2f} s wall)"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    cores = cpu_cores()
+    rows = 16
+    x = oracle_decode_sample(rows, DEC["seed"])
+    for _ in range(args.warmup):
+        time_oracle_decode(x, rows, cores)
+    vals, secs = [], []
+    for _ in range(args.steps):
+        v, s = time_oracle_decode(x, rows, cores)
+        vals.append(v)
+        secs.append(s)
+    value = statistics.median(vals)
+    sample = (f"decode: {rows} of 256 rows x 32 heads x 64 single-token steps per step "
+              f"(fp64 C oracle, {cores} threads)")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(statistics.median(secs) * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": "decode_B256 (bounded sample on host cores)", "B": rows,
+                   "steps_per_call_chain": DEC["steps"], "Hk": DEC["Hk"], "Hv": DEC["Hv"],
+                   "dk": DEC["dk"], "dv": DEC["dv"], "capacity": DEC["cap"]},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "replay"], default="all",
+                    help="profiling aid: run one phase only (prints timings, not the contract line)")
+    ap.add_argument("--decode-rows", type=int, default=DEC["B"],
+                    help="profiling aid: rows of the decode / replay phases (default 256)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local_rank = dist_init()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    line = run_ours(args, rank, world, local_rank)
+    if args.only != "all" or args.decode_rows != DEC["B"]:
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline()
+        else:
+            line["cpu_baseline"] = None
+        print(json.dumps(line), flush=True)
+    barrier()
+
+
+if __name__ == "__main__":
+    main()
