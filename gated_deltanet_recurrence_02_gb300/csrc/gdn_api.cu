@@ -229,10 +229,12 @@ int gdn_replay_state_updates(const float *state_in, float *state_out, const floa
 }
 
 size_t gdn_prefill_workspace_size(int B, int T, int Hk, int Hv, int dk, int dv, int chunk,
-                                  int dtype_qkv) {
+                                  int dtype_qkv, int varlen) {
     if (B < 0 || T < 0 || Hk <= 0 || Hv <= 0 || dk <= 0 || dv <= 0 || chunk <= 0 ||
         dtype_bytes(dtype_qkv) == 0)
         return (size_t)-1;
+    if (prefill_tc_supported(dk, dv, chunk, dtype_qkv))
+        return prefill_tc_workspace_bytes(B, T, Hv, varlen != 0);
     return 0;
 }
 
@@ -248,10 +250,12 @@ int gdn_prefill_chunked(const void *q, const void *k, const void *v, const void 
                           dtype_qkv, dtype_gate, &sh);
     if (st != GDN_OK) return st;
     if (!(chunk == 16 || chunk == 32 || chunk == 64)) return GDN_ERR_UNSUPPORTED;
-    if (!prefill_simt_supported(dk, dv, chunk)) return GDN_ERR_UNSUPPORTED;
+    const bool use_tc = prefill_tc_supported(dk, dv, chunk, dtype_qkv);
+    if (!use_tc && !prefill_simt_supported(dk, dv, chunk)) return GDN_ERR_UNSUPPORTED;
     if (final_state != nullptr && final_state == initial_state && initial_state_indices != nullptr)
         return GDN_ERR_ALIAS;
-    const size_t need = gdn_prefill_workspace_size(B, T, Hk, Hv, dk, dv, chunk, dtype_qkv);
+    const size_t need =
+        gdn_prefill_workspace_size(B, T, Hk, Hv, dk, dv, chunk, dtype_qkv, cu_seqlens != nullptr);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return GDN_ERR_WORKSPACE;
     if (workspace && !aligned(workspace, 16)) return GDN_ERR_ALIGN;
     const size_t sf_in_place = (final_state == initial_state) ? sh.sf_bytes : 0;
@@ -281,8 +285,9 @@ int gdn_prefill_chunked(const void *q, const void *k, const void *v, const void 
     p.scale = scale; p.dt_qkv = dtype_qkv; p.dt_gate = dtype_gate;
     p.ws = workspace; p.ws_bytes = workspace_bytes;
     if (error_word(&p.err) != cudaSuccess) return GDN_ERR_CUDA;
-    return launch_prefill_simt(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK
-                                                                                    : GDN_ERR_CUDA;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = use_tc ? launch_prefill_tc(p, s) : launch_prefill_simt(p, s);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 int gdn_device_errors(void *stream, uint32_t *flags) {

@@ -65,6 +65,9 @@ cudaError_t launch_recurrent(const RecurrentParams &p, cudaStream_t stream);
 cudaError_t launch_replay(const ReplayParams &p, cudaStream_t stream);
 cudaError_t launch_prefill_simt(const PrefillParams &p, cudaStream_t stream);
 bool prefill_simt_supported(int dk, int dv, int chunk);
+cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t stream);
+bool prefill_tc_supported(int dk, int dv, int chunk, int dt_qkv);
+size_t prefill_tc_workspace_bytes(int B, int T, int Hv, bool varlen);
 
 // ------------------------------------------------------------- helpers --
 

@@ -1,0 +1,711 @@
+// gdn_prefill_tc.cu -- chunked prefill on the 5th-generation tensor cores
+// (tcgen05 MMA, TMEM accumulators, TMA), for dk = dv = 128, chunk 64, bf16 or
+// fp16 inputs.
+//
+// "Enable the native Kev example on NVIDIA GPUs through ExecuTorch's AOTI CUDA
+// backend" (executorch issue 23097), work list: a chunked GDN prefill with an
+// explicit initial and final state and an FP32 recurrence under 16-bit
+// weights.  Chunk form (per chunk of n <= 64 tokens, start state S0, local
+// log-decay sums g_t, gamma_t = e^{g_t}, w_t = e^{g_last - g_t}):
+//   A[t][i] = beta_t e^{g_t - g_i} k_t.k_i (i < t),   T = (I + A)^{-1}
+//   U = T diag(beta) V,   W = T diag(beta gamma) K,   P'[t][i] = e^{g_t - g_i} q_t.k_i (i <= t)
+//   Delta = U - W S0^T
+//   O     = diag(gamma) Q S0^T + P' Delta
+//   S_end = gamma_last S0 + Delta^T diag(w) K
+//
+// Phase A (prefill_intra_kernel, one CTA per (chunk, value head), all chunks in
+// parallel): [K;Q] K^T on the tensor cores, A and P' from it, T by forward
+// substitution in fp32, then U and W on the tensor cores with T split into a
+// bf16 hi part and a bf16 lo part (so T keeps ~16 bits).  Writes W, P' and U as
+// ready-made shared-memory operand images plus gamma / w into the workspace.
+//
+// Phase B (prefill_carry_kernel, one CTA per (value head, 64-row dv tile,
+// row), serial over chunks): per chunk two dependent tensor-core steps,
+//   D1 = [Q; W] S^T                       (M=128: Q S^T and W S^T at once)
+//   Delta = U - (W S^T)                   (threads, fp32)
+//   D2 = K^T diag(w) Delta,  D3 = P' Delta (tensor cores)
+//   S <- gamma_last S + D2,  O = gamma (Q S^T) + D3
+// The state tile lives in fp32 registers (thread j owns column j of S, i.e.
+// row j of S^T, for the tile's 64 rows) and is re-packed to bf16/fp16 in
+// shared memory as the next chunk's MMA operand.  Chunk operands stream in
+// through a two-stage TMA / bulk-copy ring.
+//
+// Ragged chunks: tokens t >= n get alpha = 1 and beta = 0, which makes their
+// rows of T the identity rows and their U, W, Delta rows zero, so whatever the
+// loads bring into those rows (zeros past the end of the tensor, the next row's
+// tokens otherwise) never reaches S or a stored output.  Precondition: every
+// alpha in (0, 1].
+//
+// Every mbarrier wait is bounded; on timeout the CTA raises
+// GDN_DEVERR_TIMEOUT, waits (bounded) for its copies in flight, releases its
+// TMEM and exits.
+#include <cstring>
+#include <mutex>
+
+#include "gdn_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace gdn {
+namespace {
+
+using namespace tc;
+
+constexpr int C = 64;    // chunk
+constexpr int D = 128;   // dk = dv
+constexpr int DVT = 64;  // state rows per phase-B CTA
+constexpr uint64_t kWaitNs = 1000000000ull;
+
+// Workspace record per (chunk, value head), bytes.
+constexpr uint32_t REC_W = 0;         // W image: 2 SW128 blocks (dk 0-63, 64-127) x 64 rows
+constexpr uint32_t REC_P = 16384;     // P' image: 1 SW128 block, 64 rows
+constexpr uint32_t REC_U = 24576;     // U images: 2 dv tiles x SW128 block of 64 rows
+constexpr uint32_t REC_VEC = 40960;   // gamma[64], w[64], gamma_last
+constexpr uint32_t REC_BYTES = 41984;
+
+template <typename E>
+struct Elem;
+template <>
+struct Elem<__nv_bfloat16> {
+    static constexpr bool kBf16 = true;
+    __device__ static uint32_t pack2(float a, float b) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    __device__ static float2 unpack2(uint32_t u) {
+        return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&u));
+    }
+    __device__ static float round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+};
+template <>
+struct Elem<__half> {
+    static constexpr bool kBf16 = false;
+    __device__ static uint32_t pack2(float a, float b) {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    __device__ static float2 unpack2(uint32_t u) { return __half22float2(*reinterpret_cast<__half2 *>(&u)); }
+    __device__ static float round(float x) { return __half2float(__float2half_rn(x)); }
+};
+
+// Eight fp32 values -> eight 16-bit elements in one 16-byte vector.
+template <typename E>
+__device__ __forceinline__ uint4 pack8(const float *v) {
+    return make_uint4(Elem<E>::pack2(v[0], v[1]), Elem<E>::pack2(v[2], v[3]), Elem<E>::pack2(v[4], v[5]),
+                      Elem<E>::pack2(v[6], v[7]));
+}
+template <typename E>
+__device__ __forceinline__ void unpack8(uint4 u, float *v) {
+    float2 a = Elem<E>::unpack2(u.x), b = Elem<E>::unpack2(u.y), c = Elem<E>::unpack2(u.z),
+           d = Elem<E>::unpack2(u.w);
+    v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y; v[4] = c.x; v[5] = c.y; v[6] = d.x; v[7] = d.y;
+}
+
+// Byte offset of the 16-byte chunk holding elements [8*q, 8*q+8) of row r.
+__device__ __forceinline__ uint32_t sw128_chunk(int r, int q) {
+    return (uint32_t)(r * 128 + (((q ^ (r & 7)) & 7) << 4));
+}
+
+// ---- chunk bookkeeping ------------------------------------------------------
+
+__device__ __forceinline__ int n_chunks(int len) { return (len + C - 1) / C; }
+
+// First global chunk index of row b.
+__device__ __forceinline__ long chunk_base(const int32_t *cu, int B, int T, int b) {
+    if (cu == nullptr) return (long)b * n_chunks(T);
+    long acc = 0;
+    for (int r = 0; r < b; ++r) {
+        long tok0;
+        int len;
+        row_range(cu, r, T, tok0, len);
+        acc += n_chunks(len);
+    }
+    return acc;
+}
+
+// Global chunk index -> (row, chunk in row); false past the last chunk.
+__device__ __forceinline__ bool chunk_of(const int32_t *cu, int B, int T, long gc, int &b, int &c) {
+    if (cu == nullptr) {
+        const int nc = n_chunks(T);
+        if (nc == 0) return false;
+        b = (int)(gc / nc);
+        c = (int)(gc % nc);
+        return b < B;
+    }
+    long acc = 0;
+    for (int r = 0; r < B; ++r) {
+        long tok0;
+        int len;
+        row_range(cu, r, T, tok0, len);
+        const int nc = n_chunks(len);
+        if (gc < acc + nc) {
+            b = r;
+            c = (int)(gc - acc);
+            return true;
+        }
+        acc += nc;
+    }
+    return false;
+}
+
+struct TcMaps {
+    CUtensorMap q, k, v;
+};
+
+// ============================================================ phase A ====
+
+constexpr uint32_t A_KQ = 0;          // [K;Q] image, 2 K-blocks of 128 rows (32 KB)
+constexpr uint32_t A_V = 32768;       // V image, 2 dv blocks of 64 rows (16 KB)
+constexpr uint32_t A_IMG = 49152;     // [T*beta ; T*beta*gamma] hi (16 KB) | lo (16 KB); At aliases it
+constexpr uint32_t A_T = 81920;       // T fp32 [64][68]
+constexpr uint32_t A_VEC = A_T + 64 * 68 * 4;  // g, beta, gamma, w: 4 x 64 floats
+constexpr uint32_t A_BAR = A_VEC + 1024;
+constexpr uint32_t A_SMEM = A_BAR + 64 + 1024;  // + alignment slack
+constexpr int AT_LD = 68;
+
+template <typename E>
+__global__ void __launch_bounds__(128, 2)
+prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap mq,
+                     const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sKQ = sm + A_KQ;
+    uint8_t *sV = sm + A_V;
+    uint8_t *sImg = sm + A_IMG;
+    float *At = reinterpret_cast<float *>(sm + A_IMG);
+    float *sT = reinterpret_cast<float *>(sm + A_T);
+    float *vg = reinterpret_cast<float *>(sm + A_VEC);
+    float *vbeta = vg + 64, *vgam = vg + 128, *vw = vg + 192;
+    uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + A_BAR);
+    uint64_t *bar_mma = bar_ld + 1;
+    uint32_t *slot = reinterpret_cast<uint32_t *>(bar_ld + 2);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.y, Hv = p.Hv, Hk = p.Hk;
+    const int hk = h / (Hv / Hk);
+    int b, c;
+    if (!chunk_of(p.cu_seqlens, p.B, p.T, blockIdx.x, b, c)) return;
+    long rtok0;
+    int len;
+    row_range(p.cu_seqlens, b, p.T, rtok0, len);
+    const long tok0 = rtok0 + (long)c * C;
+    const int n = min(C, len - c * C);
+    uint8_t *rec = reinterpret_cast<uint8_t *>(p.ws) +
+                   ((size_t)(chunk_base(p.cu_seqlens, p.B, p.T, b) + c) * Hv + h) * REC_BYTES;
+
+    if (tid == 0) {
+        prefetch_tensormap(&mq);
+        prefetch_tensormap(&mk);
+        prefetch_tensormap(&mv);
+        mbar_init(bar_ld, 1);
+        mbar_init(bar_mma, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        tmem_alloc(slot, 256);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_arrive_expect_tx(bar_ld, 32768 + 16384);
+        tma_load_3d(sKQ, &mk, 0, hk, (int)tok0, bar_ld);
+        tma_load_3d(sKQ + 16384, &mk, 64, hk, (int)tok0, bar_ld);
+        tma_load_3d(sKQ + 8192, &mq, 0, hk, (int)tok0, bar_ld);
+        tma_load_3d(sKQ + 24576, &mq, 64, hk, (int)tok0, bar_ld);
+        tma_load_3d(sV, &mv, 0, h, (int)tok0, bar_ld);
+        tma_load_3d(sV + 8192, &mv, 64, h, (int)tok0, bar_ld);
+    }
+    if (tid < C) {
+        const long gi = (tok0 + tid) * Hv + h;
+        vg[tid] = (tid < n) ? logf(ld_gate(p.alpha, gi, p.dt_gate)) : 0.f;
+        vbeta[tid] = (tid < n) ? ld_gate(p.beta, gi, p.dt_gate) : 0.f;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        float x0 = vg[lane], x1 = vg[lane + 32];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            float y0 = __shfl_up_sync(0xffffffffu, x0, o);
+            float y1 = __shfl_up_sync(0xffffffffu, x1, o);
+            if (lane >= o) { x0 += y0; x1 += y1; }
+        }
+        x1 += __shfl_sync(0xffffffffu, x0, 31);
+        const float glast = __shfl_sync(0xffffffffu, x1, 31);
+        vg[lane] = x0;
+        vg[lane + 32] = x1;
+        const float g0 = expf(x0), g1 = expf(x1), w0 = expf(glast - x0), w1 = expf(glast - x1);
+        vgam[lane] = g0; vgam[lane + 32] = g1; vw[lane] = w0; vw[lane + 32] = w1;
+        float *rv = reinterpret_cast<float *>(rec + REC_VEC);
+        rv[lane] = g0; rv[lane + 32] = g1; rv[64 + lane] = w0; rv[96 + lane] = w1;
+        if (lane == 0) rv[128] = expf(glast);
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tbase = *slot;
+    const uint32_t lane_base = tbase + ((uint32_t)(32 * warp) << 16);
+    const bool kbf = Elem<E>::kBf16;
+    bool ok = mbar_wait(bar_ld, 0, kWaitNs);
+
+    // ---- [K; Q] K^T -> TMEM cols [0, 64): rows 0-63 K K^T, rows 64-127 Q K^T
+    if (ok && tid == 0) {
+        fence_after_sync();
+        const uint32_t s = smem_u32(sKQ);
+        const uint32_t id = idesc_f16(128, 64, false, false, kbf);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+            mma_f16(tbase, desc_sw128(s + off, 16, 1024), desc_sw128(s + off, 16, 1024), id, k > 0);
+        }
+        mma_commit(bar_mma);
+    }
+    ok = ok && mbar_wait(bar_mma, 0, kWaitNs);
+    fence_after_sync();
+    if (ok) {
+        if (warp < 2) {
+            // A, stored transposed: At[i][t] = A[t][i]
+            const int t = tid;
+            const float gt = vg[t], bt = vbeta[t];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float v[32];
+                tmem_ld32(lane_base + 32 * hh, v);
+#pragma unroll
+                for (int ii = 0; ii < 32; ++ii) {
+                    const int i = 32 * hh + ii;
+                    At[i * AT_LD + t] = (i < t) ? bt * expf(gt - vg[i]) * v[ii] : 0.f;
+                }
+            }
+        } else {
+            // P' image straight to the workspace
+            const int t = tid - 64;
+            const float gt = vg[t];
+            uint8_t *dst = rec + REC_P;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float v[32];
+                tmem_ld32(lane_base + 32 * hh, v);
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8) {
+                    float pv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int i = 32 * hh + 8 * q8 + e;
+                        pv[e] = (i <= t) ? expf(gt - vg[i]) * v[8 * q8 + e] : 0.f;
+                    }
+                    *reinterpret_cast<uint4 *>(dst + sw128_chunk(t, 4 * hh + q8)) = pack8<E>(pv);
+                }
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- T = (I + A)^{-1}: thread c < 64 solves column c, right-looking ----
+    if (ok && warp < 2) {
+        const int col = tid;
+        float acc[64];
+#pragma unroll
+        for (int r = 0; r < 64; ++r) acc[r] = 0.f;
+#pragma unroll
+        for (int t = 0; t < 64; ++t) {
+            const float xt = (t < col) ? 0.f : ((t == col) ? 1.f : -acc[t]);
+            sT[t * AT_LD + col] = xt;
+#pragma unroll
+            for (int r4 = ((t + 1) >> 2) << 2; r4 < 64; r4 += 4) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(At + t * AT_LD + r4);
+                acc[r4 + 0] = fmaf(a4.x, xt, acc[r4 + 0]);
+                acc[r4 + 1] = fmaf(a4.y, xt, acc[r4 + 1]);
+                acc[r4 + 2] = fmaf(a4.z, xt, acc[r4 + 2]);
+                acc[r4 + 3] = fmaf(a4.w, xt, acc[r4 + 3]);
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- operand images [T diag(beta) ; T diag(beta gamma)], hi and lo parts
+    if (ok) {
+        const int t = tid & 63, which = tid >> 6, r = which * 64 + t;
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) {
+            float hi[8], lo[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int s = 8 * q8 + e;
+                const float val = sT[t * AT_LD + s] * (which ? vbeta[s] * vgam[s] : vbeta[s]);
+                hi[e] = Elem<E>::round(val);
+                lo[e] = val - hi[e];
+            }
+            *reinterpret_cast<uint4 *>(sImg + sw128_chunk(r, q8)) = pack8<E>(hi);
+            *reinterpret_cast<uint4 *>(sImg + 16384 + sw128_chunk(r, q8)) = pack8<E>(lo);
+        }
+    }
+    fence_proxy_async();
+    fence_before_sync();
+    __syncthreads();
+
+    // ---- U = [T b ; T b g] V (rows 0-63 used) -> TMEM cols [64, 192)
+    if (ok && tid == 0) {
+        fence_after_sync();
+        const uint32_t si = smem_u32(sImg), sv = smem_u32(sV);
+        const uint32_t id = idesc_f16(128, 128, false, true, kbf);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint64_t bd = desc_sw128(sv + k * 2048, 8192, 1024);
+            mma_f16(tbase + 64, desc_sw128(si + k * 32, 16, 1024), bd, id, k > 0);
+            mma_f16(tbase + 64, desc_sw128(si + 16384 + k * 32, 16, 1024), bd, id, 1);
+        }
+        mma_commit(bar_mma);
+    }
+    ok = ok && mbar_wait(bar_mma, 1, kWaitNs);
+    fence_after_sync();
+    if (ok && warp < 2) {
+        const int t = tid;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            float v[32];
+            tmem_ld32(lane_base + 64 + 32 * q4, v);
+            uint8_t *dst = rec + REC_U + (q4 >> 1) * 8192;
+#pragma unroll
+            for (int q8 = 0; q8 < 4; ++q8)
+                *reinterpret_cast<uint4 *>(dst + sw128_chunk(t, (q4 & 1) * 4 + q8)) = pack8<E>(v + 8 * q8);
+        }
+    }
+    fence_before_sync();
+    __syncthreads();
+
+    // ---- W = [T b ; T b g] K (rows 64-127 used) -> TMEM cols [64, 192)
+    if (ok && tid == 0) {
+        fence_after_sync();
+        const uint32_t si = smem_u32(sImg), sk = smem_u32(sKQ);
+        const uint32_t id = idesc_f16(128, 128, false, true, kbf);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint64_t bd = desc_sw128(sk + k * 2048, 16384, 1024);
+            mma_f16(tbase + 64, desc_sw128(si + k * 32, 16, 1024), bd, id, k > 0);
+            mma_f16(tbase + 64, desc_sw128(si + 16384 + k * 32, 16, 1024), bd, id, 1);
+        }
+        mma_commit(bar_mma);
+    }
+    ok = ok && mbar_wait(bar_mma, 0, kWaitNs);
+    fence_after_sync();
+    if (ok && warp >= 2) {
+        const int t = tid - 64;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            float v[32];
+            tmem_ld32(lane_base + 64 + 32 * q4, v);
+            uint8_t *dst = rec + REC_W + (q4 >> 1) * 8192;
+#pragma unroll
+            for (int q8 = 0; q8 < 4; ++q8)
+                *reinterpret_cast<uint4 *>(dst + sw128_chunk(t, (q4 & 1) * 4 + q8)) = pack8<E>(v + 8 * q8);
+        }
+    }
+    if (!ok) {
+        if (tid == 0) atomicOr(p.err, (uint32_t)GDN_DEVERR_TIMEOUT);
+        mbar_wait(bar_ld, 0, kWaitNs);  // copies in flight must land before the CTA exits
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, 256);
+}
+
+// ============================================================ phase B ====
+
+constexpr uint32_t ST_A1 = 0;        // [Q ; W] image, 2 K-blocks of 128 rows
+constexpr uint32_t ST_K = 32768;     // K image, 2 dk blocks of 64 rows
+constexpr uint32_t ST_P = 49152;     // P' image (rows 0-63 of the [P'; X] operand)
+constexpr uint32_t ST_U = 57344;     // U tile image (also the unused rows 64-127 of [P'; X])
+constexpr uint32_t ST_VEC = 65536;   // gamma, w, gamma_last
+constexpr uint32_t ST_BYTES = 66560;
+constexpr int NS = 2;
+constexpr uint32_t B_S = NS * ST_BYTES;        // S^T image (MN-major, 128 K-rows)
+constexpr uint32_t B_DW = B_S + 16384;         // diag(w) Delta image
+constexpr uint32_t B_DD = B_DW + 8192;         // Delta image
+constexpr uint32_t B_BAR = B_DD + 8192;
+constexpr uint32_t B_SMEM = B_BAR + 128 + 1024;
+constexpr uint32_t STAGE_TX = 16384 + 16384 + 16384 + 8192 + 8192 + 1024;
+
+template <typename E>
+__global__ void __launch_bounds__(128, 1)
+prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap mq,
+                     const __grid_constant__ CUtensorMap mk) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sS = sm + B_S, *sDw = sm + B_DW, *sDd = sm + B_DD;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + B_BAR);  // [NS]
+    uint64_t *bar1 = full + NS, *bar2 = full + NS + 1;
+    uint32_t *slot = reinterpret_cast<uint32_t *>(full + NS + 2);
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int vt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int Hv = p.Hv, Hk = p.Hk;
+    const int hk = h / (Hv / Hk);
+    const int i0 = vt * DVT;
+    long rtok0;
+    int len;
+    row_range(p.cu_seqlens, b, p.T, rtok0, len);
+    const int nc = n_chunks(len);
+    const uint8_t *rec0 = reinterpret_cast<const uint8_t *>(p.ws) +
+                          (size_t)chunk_base(p.cu_seqlens, p.B, p.T, b) * Hv * REC_BYTES +
+                          (size_t)h * REC_BYTES;
+    const size_t rec_stride = (size_t)Hv * REC_BYTES;
+
+    auto issue_stage = [&](int cc) {
+        const int s = cc % NS;
+        uint8_t *st = sm + s * ST_BYTES;
+        const uint8_t *rec = rec0 + (size_t)cc * rec_stride;
+        const int t0 = (int)(rtok0 + (long)cc * C);
+        mbar_arrive_expect_tx(&full[s], STAGE_TX);
+        tma_load_3d(st + ST_A1, &mq, 0, hk, t0, &full[s]);
+        tma_load_3d(st + ST_A1 + 16384, &mq, 64, hk, t0, &full[s]);
+        bulk_load(st + ST_A1 + 8192, rec + REC_W, 8192, &full[s]);
+        bulk_load(st + ST_A1 + 24576, rec + REC_W + 8192, 8192, &full[s]);
+        tma_load_3d(st + ST_K, &mk, 0, hk, t0, &full[s]);
+        tma_load_3d(st + ST_K + 8192, &mk, 64, hk, t0, &full[s]);
+        bulk_load(st + ST_P, rec + REC_P, 8192, &full[s]);
+        bulk_load(st + ST_U, rec + REC_U + vt * 8192, 8192, &full[s]);
+        bulk_load(st + ST_VEC, rec + REC_VEC, 1024, &full[s]);
+    };
+
+    if (tid == 0) {
+        prefetch_tensormap(&mq);
+        prefetch_tensormap(&mk);
+        for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
+        mbar_init(bar1, 1);
+        mbar_init(bar2, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        tmem_alloc(slot, 256);
+        tmem_relinquish();
+    }
+    if (tid == 0)
+        for (int cc = 0; cc < NS && cc < nc; ++cc) issue_stage(cc);
+
+    // state tile: thread j holds S[i0 + i][j], i < 64 (row j of S^T)
+    const int j = tid;
+    float S[DVT];
+    {
+        const float *s0 = initial_state_ptr(p.s0, p.s0_idx, p.n_s0, b, h, Hv, D, D, p.err);
+#pragma unroll
+        for (int i = 0; i < DVT; ++i) S[i] = s0 ? s0[(size_t)(i0 + i) * D + j] : 0.f;
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8)
+            *reinterpret_cast<uint4 *>(sS + sw128_chunk(j, q8)) = pack8<E>(S + 8 * q8);
+    }
+    fence_proxy_async();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tbase = *slot;
+    const uint32_t lane_base = tbase + ((uint32_t)(32 * warp) << 16);
+    const bool kbf = Elem<E>::kBf16;
+    const uint32_t id1 = idesc_f16(128, 64, false, true, kbf);
+    const uint32_t id2 = idesc_f16(128, 64, true, true, kbf);
+    const uint32_t id3 = idesc_f16(128, 64, false, true, kbf);
+    E *ob = reinterpret_cast<E *>(p.out);
+    bool ok = true;
+
+    for (int cc = 0; cc < nc && ok; ++cc) {
+        const int s = cc % NS;
+        uint8_t *st = sm + s * ST_BYTES;
+        const uint32_t d1 = (cc & 1) ? 192u : 0u;
+        const int n = min(C, len - cc * C);
+        ok = mbar_wait(&full[s], (cc / NS) & 1, kWaitNs);
+        if (!ok) break;
+        if (tid == 0) {
+            fence_after_sync();
+            const uint32_t sa = smem_u32(st + ST_A1), sb = smem_u32(sS);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                mma_f16(tbase + d1, desc_sw128(sa + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
+                        desc_sw128(sb + k * 2048, 8192, 1024), id1, k > 0);
+            mma_commit(bar1);
+        }
+        const float *vec = reinterpret_cast<const float *>(st + ST_VEC);
+        const float gC = vec[128];
+        const float gt = (warp < 2) ? vec[tid] : 0.f;
+        const float wt = (warp >= 2) ? vec[64 + tid - 64] : 0.f;
+        ok = mbar_wait(bar1, cc & 1, kWaitNs);
+        if (!ok) break;
+        fence_after_sync();
+        if (warp >= 2) {
+            // Delta = U - W S^T for token t = tid - 64
+            const int t = tid - 64;
+            const uint8_t *su = st + ST_U;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float ws[32];
+                tmem_ld32(lane_base + d1 + 32 * hh, ws);
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8) {
+                    float u[8], dd[8], dw[8];
+                    unpack8<E>(*reinterpret_cast<const uint4 *>(su + sw128_chunk(t, 4 * hh + q8)), u);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        dd[e] = u[e] - ws[8 * q8 + e];
+                        dw[e] = wt * dd[e];
+                    }
+                    *reinterpret_cast<uint4 *>(sDd + sw128_chunk(t, 4 * hh + q8)) = pack8<E>(dd);
+                    *reinterpret_cast<uint4 *>(sDw + sw128_chunk(t, 4 * hh + q8)) = pack8<E>(dw);
+                }
+            }
+        }
+        fence_proxy_async();
+        fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            fence_after_sync();
+            const uint32_t sk = smem_u32(st + ST_K), sp = smem_u32(st + ST_P);
+            const uint32_t sdw = smem_u32(sDw), sdd = smem_u32(sDd);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                mma_f16(tbase + 64, desc_sw128(sk + k * 2048, 8192, 1024),
+                        desc_sw128(sdw + k * 2048, 8192, 1024), id2, k > 0);
+                mma_f16(tbase + 128, desc_sw128(sp + k * 32, 16, 1024),
+                        desc_sw128(sdd + k * 2048, 8192, 1024), id3, k > 0);
+            }
+            mma_commit(bar2);
+        }
+        ok = mbar_wait(bar2, cc & 1, kWaitNs);
+        if (!ok) break;
+        fence_after_sync();
+        // S <- gamma_last S + K^T diag(w) Delta   (TMEM lane j = dk index)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            float v[32];
+            tmem_ld32(lane_base + 64 + 32 * hh, v);
+#pragma unroll
+            for (int ii = 0; ii < 32; ++ii) S[32 * hh + ii] = fmaf(gC, S[32 * hh + ii], v[ii]);
+        }
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8)
+            *reinterpret_cast<uint4 *>(sS + sw128_chunk(j, q8)) = pack8<E>(S + 8 * q8);
+        fence_proxy_async();
+        fence_before_sync();
+        __syncthreads();
+        if (tid == 0 && cc + NS < nc) issue_stage(cc + NS);
+        if (warp < 2) {
+            // O = gamma_t (Q S^T) + P' Delta for token t = tid
+            const int t = tid;
+            fence_after_sync();
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float qs[32], pd[32];
+                tmem_ld32(lane_base + d1 + 32 * hh, qs);
+                tmem_ld32(lane_base + 128 + 32 * hh, pd);
+                if (t < n) {
+                    E *dst = ob + ((rtok0 + (long)cc * C + t) * Hv + h) * (long)D + i0 + 32 * hh;
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8) {
+                        float o[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) o[e] = fmaf(gt, qs[8 * q8 + e], pd[8 * q8 + e]);
+                        *reinterpret_cast<uint4 *>(dst + 8 * q8) = pack8<E>(o);
+                    }
+                }
+            }
+            fence_before_sync();
+        }
+    }
+
+    if (ok && p.s_final != nullptr) {
+        float *sf = p.s_final + (((size_t)b * Hv + h) * D + i0) * D;
+#pragma unroll
+        for (int i = 0; i < DVT; ++i) sf[(size_t)i * D + j] = S[i];
+    }
+    if (!ok) {
+        if (tid == 0) atomicOr(p.err, (uint32_t)GDN_DEVERR_TIMEOUT);
+        // let every copy this CTA issued land before its shared memory is released
+        for (int s = 0; s < NS; ++s) mbar_wait(&full[s], 0, kWaitNs / 4);
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, 256);
+}
+
+// ============================================================== host =====
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// [total_T, H, 128] 16-bit tensor, box {64 features, 1 head, 64 tokens}, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *ptr, int H, long total_T, bool bf16) {
+    EncodeTiledFn enc = encode_fn();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)total_T};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+    cuuint32_t box[3] = {64, 1, 64};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+               const_cast<void *>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename E>
+cudaError_t launch_e(const PrefillParams &p, long total_T, long max_chunks, cudaStream_t stream) {
+    const bool bf = Elem<E>::kBf16;
+    CUtensorMap mq, mk, mv;
+    memset(&mq, 0, sizeof(mq));
+    memset(&mk, 0, sizeof(mk));
+    memset(&mv, 0, sizeof(mv));
+    // With no tokens at all no chunk exists and the maps are never used.
+    if (total_T > 0 && (!make_map(&mq, p.q, p.Hk, total_T, bf) || !make_map(&mk, p.k, p.Hk, total_T, bf) ||
+                        !make_map(&mv, p.v, p.Hv, total_T, bf)))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(prefill_intra_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)A_SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(prefill_carry_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)B_SMEM);
+    if (e != cudaSuccess) return e;
+    if (max_chunks > 0) {
+        dim3 ga((unsigned)max_chunks, p.Hv);
+        prefill_intra_kernel<E><<<ga, 128, A_SMEM, stream>>>(p, mq, mk, mv);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    dim3 gb(D / DVT, p.Hv, p.B);
+    prefill_carry_kernel<E><<<gb, 128, B_SMEM, stream>>>(p, mq, mk);
+    return cudaGetLastError();
+}
+
+long max_chunks_of(int B, int T, bool varlen) {
+    return varlen ? (long)T / C + B : (long)B * ((T + C - 1) / C);
+}
+
+}  // namespace
+
+bool prefill_tc_supported(int dk, int dv, int chunk, int dt_qkv) {
+    return dk == D && dv == D && chunk == C && (dt_qkv == GDN_BF16 || dt_qkv == GDN_F16);
+}
+
+size_t prefill_tc_workspace_bytes(int B, int T, int Hv, bool varlen) {
+    return (size_t)max_chunks_of(B, T, varlen) * (size_t)Hv * REC_BYTES;
+}
+
+cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t stream) {
+    const bool varlen = p.cu_seqlens != nullptr;
+    const long total_T = varlen ? (long)p.T : (long)p.B * p.T;
+    const long mc = max_chunks_of(p.B, p.T, varlen);
+    if (p.dt_qkv == GDN_BF16) return launch_e<__nv_bfloat16>(p, total_T, mc, stream);
+    return launch_e<__half>(p, total_T, mc, stream);
+}
+
+}  // namespace gdn

@@ -44,7 +44,7 @@ def lib() -> ctypes.CDLL:
             "`python -c 'import __graft_entry__ as g; g.build()'` first")
     L = ctypes.CDLL(path)
     vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
-    L.gdn_prefill_workspace_size.argtypes = [i, i, i, i, i, i, i, i]
+    L.gdn_prefill_workspace_size.argtypes = [i, i, i, i, i, i, i, i, i]
     L.gdn_prefill_workspace_size.restype = sz
     L.gdn_prefill_chunked.argtypes = [vp] * 8 + [i, vp, vp] + [i] * 8 + [f, i, i, vp, sz, vp]
     L.gdn_prefill_chunked.restype = i
@@ -95,9 +95,9 @@ def slot_width(Hk: int, Hv: int, dk: int, dv: int) -> int:
     return Hv + Hk * dk + Hv * dv
 
 
-def gdn_prefill_workspace_size(B, T, Hk, Hv, dk, dv, chunk, dtype_qkv) -> int:
+def gdn_prefill_workspace_size(B, T, Hk, Hv, dk, dv, chunk, dtype_qkv, varlen=False) -> int:
     return int(lib().gdn_prefill_workspace_size(B, T, Hk, Hv, dk, dv, chunk,
-                                                _DT.get(dtype_qkv, dtype_qkv)))
+                                                _DT.get(dtype_qkv, dtype_qkv), int(bool(varlen))))
 
 
 def _dims(q, v, B, T, cu_seqlens):
@@ -122,7 +122,8 @@ def gdn_prefill_chunked(q, k, v, alpha, beta, *, B: int, T: Optional[int] = None
     if final_state is None and want_final_state:
         final_state = torch.empty((B, Hv, dv, dk), dtype=torch.float32, device=v.device)
     n0 = initial_state.shape[0] if initial_state is not None else 0
-    need = gdn_prefill_workspace_size(B, T, Hk, Hv, dk, dv, chunk, q.dtype)
+    need = gdn_prefill_workspace_size(B, T, Hk, Hv, dk, dv, chunk, q.dtype,
+                                      varlen=cu_seqlens is not None)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=v.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0

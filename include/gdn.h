@@ -90,10 +90,12 @@ enum { GDN_F32 = 0, GDN_F16 = 1, GDN_BF16 = 2 };
 /*
  * gdn_prefill_workspace_size -- bytes of device workspace that
  * gdn_prefill_chunked needs for these sizes (0 if none).  T as in
- * gdn_prefill_chunked.  Returns (size_t)-1 for invalid sizes.
+ * gdn_prefill_chunked; varlen != 0 when cu_seqlens will be passed.  The
+ * tensor-core path (dk = dv = 128, chunk 64, 16-bit q/k/v) stores about 41 KB
+ * per (chunk, value head).  Returns (size_t)-1 for invalid sizes.
  */
 GDN_API size_t gdn_prefill_workspace_size(int B, int T, int Hk, int Hv, int dk, int dv,
-                                  int chunk, int dtype_qkv);
+                                          int chunk, int dtype_qkv, int varlen);
 
 /*
  * gdn_prefill_chunked -- chunked parallel prefill with explicit initial and

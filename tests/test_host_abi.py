@@ -58,7 +58,7 @@ def pre(L, **kw):
     a = dict(q=A, k=A + GiB, v=A + 2 * GiB, alpha=A + 3 * GiB, beta=A + 4 * GiB, cu=None,
              s0=A + 5 * GiB, idx=None, n0=1, sf=A + 6 * GiB, out=A + 7 * GiB, B=1, T=100,
              Hq=16, Hk=16, Hv=32, dk=128, dv=128, chunk=64, scale=1.0, dtq=2, dtg=0,
-             ws=None, wsb=0)
+             ws=A + 8 * GiB, wsb=1 << 30)
     a.update(kw)
     return L.gdn_prefill_chunked(a["q"], a["k"], a["v"], a["alpha"], a["beta"], a["cu"],
                                  a["s0"], a["idx"], a["n0"], a["sf"], a["out"], a["B"],
@@ -113,6 +113,9 @@ def test_recurrent_rejects(L, kw, code):
     (dict(out=A + 2 * GiB), ALIAS),          # out is v
     (dict(sf=A + 7 * GiB + 128), ALIAS),     # final state overlaps out
     (dict(dtg=3), INVALID),
+    (dict(ws=None, wsb=0), WS),              # tensor-core path needs its workspace
+    (dict(wsb=1024), WS),
+    (dict(ws=A + 7 * GiB + 1024), ALIAS),    # workspace overlaps out
 ])
 def test_prefill_rejects(L, kw, code):
     assert pre(L, **kw) == code
@@ -139,8 +142,10 @@ def test_empty_batch_is_a_no_op(L):
 
 
 def test_workspace_size_query(L):
-    assert L.gdn_prefill_workspace_size(1, 4100, 16, 32, 128, 128, 64, 2) != ctypes.c_size_t(-1).value
-    assert L.gdn_prefill_workspace_size(-1, 4100, 16, 32, 128, 128, 64, 2) == ctypes.c_size_t(-1).value
+    big = L.gdn_prefill_workspace_size(1, 4100, 16, 32, 128, 128, 64, 2, 0)
+    assert big == 65 * 32 * 41984  # tensor-core path: one record per (chunk, value head)
+    assert L.gdn_prefill_workspace_size(2, 100, 1, 2, 32, 32, 16, 0, 0) == 0  # CUDA-core path
+    assert L.gdn_prefill_workspace_size(-1, 4100, 16, 32, 128, 128, 64, 2, 0) == ctypes.c_size_t(-1).value
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
