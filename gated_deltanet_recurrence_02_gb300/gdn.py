@@ -186,3 +186,30 @@ def gdn_device_errors(stream=None) -> int:
     if st not in (GDN_OK,):
         raise GdnError(st, "gdn_device_errors")
     return int(flags.value)
+
+
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def gdn_prefill_chunked_noalloc(q, k, v, alpha, beta, *, B: int, T: Optional[int] = None,
+                                cu_seqlens=None, initial_state=None,
+                                initial_state_indices=None, final_state, out,
+                                chunk: int = 64, scale: float = 1.0, stream=None):
+    """Chunked prefill that allocates nothing: the library's fixed device
+    scratch replaces the workspace, and the caller passes `out` and
+    `final_state` (None allowed for final_state only if not wanted).  For
+    callers that cannot allocate device memory; see include/gdn.h for the size
+    limit and the rule that calls must not overlap on the GPU."""
+    L = lib()
+    fn = L.gdn_prefill_chunked_noalloc
+    if fn.restype is not ctypes.c_int or fn.argtypes is None:
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        fn.argtypes = [vp] * 8 + [i, vp, vp] + [i] * 8 + [f, i, i, vp]
+        fn.restype = ctypes.c_int
+    T, Hk, dk, Hv, dv = _dims(q, v, B, T, cu_seqlens)
+    n0 = initial_state.shape[0] if initial_state is not None else 0
+    st = fn(_p(q), _p(k), _p(v), _p(alpha), _p(beta), _p(cu_seqlens), _p(initial_state),
+            _p(initial_state_indices), n0, _p(final_state), _p(out), B, T, Hk, Hk, Hv, dk, dv,
+            chunk, scale, _DT[q.dtype], _DT[alpha.dtype], _stream(stream))
+    _check(st, "gdn_prefill_chunked_noalloc")
+    return out, final_state

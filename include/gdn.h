@@ -180,6 +180,41 @@ GDN_API int gdn_replay_state_updates(const float *state_in, float *state_out,
                              const int32_t *accepted_count, int B, int Hk,
                              int Hv, int dk, int dv, void *stream);
 
+/*
+ * gdn_prefill_chunked_noalloc -- gdn_prefill_chunked for callers that cannot
+ * allocate device memory: runtimes with their own memory planner that forbid
+ * hidden allocations, code running while a stream is being captured into a
+ * CUDA graph (where cudaMalloc is not allowed), or latency-critical paths that
+ * must never enter the allocator.  Same arguments and results as
+ * gdn_prefill_chunked, without the workspace: the library uses a fixed device
+ * buffer of GDN_NOALLOC_SCRATCH_BYTES compiled into it (every device that
+ * loads the library keeps it until the process exits).  The pages describe
+ * no such entry point; it exists only for these callers.
+ *
+ *  - Sizes: the call is accepted when gdn_prefill_workspace_size(...) for the
+ *    same arguments is <= GDN_NOALLOC_SCRATCH_BYTES (32 MiB: e.g. up to 799
+ *    (chunk, value head) records on the tensor-core path, 1536 tokens at
+ *    Hv = 32 in one row); larger problems return GDN_ERR_WORKSPACE before
+ *    anything is launched.  Shapes that need no workspace always fit.
+ *  - The first call on a device looks up the buffer's device address (a CUDA
+ *    runtime query, cached per device); make that first call before any
+ *    stream capture starts.
+ *  - All calls share the buffer and it keeps the last call's contents (the
+ *    prefill writes every scratch byte it reads, so nothing is cleared).
+ *    Calls whose GPU work overlaps (e.g. on unordered streams) race on it:
+ *    serialise them.
+ *  - No cudaMalloc, cudaFree or allocating library routine is called.
+ */
+#define GDN_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+GDN_API int gdn_prefill_chunked_noalloc(const void *q, const void *k, const void *v,
+                                        const void *alpha, const void *beta,
+                                        const int32_t *cu_seqlens, const float *initial_state,
+                                        const int32_t *initial_state_indices,
+                                        int num_initial_states, float *final_state, void *out,
+                                        int B, int T, int Hq, int Hk, int Hv, int dk, int dv,
+                                        int chunk, float scale, int dtype_qkv, int dtype_gate,
+                                        void *stream);
+
 /* Device-side error bits (gdn_device_errors). */
 enum {
     GDN_DEVERR_BAD_INDEX = 1, /* an initial_state_indices entry was out of range */
