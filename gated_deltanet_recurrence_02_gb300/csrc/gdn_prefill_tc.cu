@@ -14,21 +14,25 @@
 //   S_end = gamma_last S0 + Delta^T diag(w) K
 //
 // Phase A (prefill_intra_kernel, one CTA per (chunk, value head), all chunks in
-// parallel): [K;Q] K^T on the tensor cores, A and P' from it, T by forward
-// substitution in fp32, then U and W on the tensor cores with T split into a
+// parallel): [K;Q] K^T on the tensor cores, A and P' from it, T by a blocked
+// (16 x 16 tiles) unit-lower-triangular inverse in fp32, then U and W on the
+// tensor cores with T split into a
 // bf16 hi part and a bf16 lo part (so T keeps ~16 bits).  Writes W, P' and U as
 // ready-made shared-memory operand images plus gamma / w into the workspace.
 //
-// Phase B (prefill_carry_kernel, one CTA per (value head, 64-row dv tile,
+// Phase B (prefill_carry_kernel, one CTA per (value head, 32-row dv tile,
 // row), serial over chunks): per chunk two dependent tensor-core steps,
 //   D1 = [Q; W] S^T                       (M=128: Q S^T and W S^T at once)
 //   Delta = U - (W S^T)                   (threads, fp32)
 //   D2 = K^T diag(w) Delta,  D3 = P' Delta (tensor cores)
 //   S <- gamma_last S + D2,  O = gamma (Q S^T) + D3
 // The state tile lives in fp32 registers (thread j owns column j of S, i.e.
-// row j of S^T, for the tile's 64 rows) and is re-packed to bf16/fp16 in
+// row j of S^T, for the tile's 32 rows) and is re-packed to bf16/fp16 in
 // shared memory as the next chunk's MMA operand.  Chunk operands stream in
-// through a two-stage TMA / bulk-copy ring.
+// through a three-stage TMA / bulk-copy ring, with L2 prefetches further
+// ahead; the output MMA (P' Delta) is committed separately so the state
+// update never waits for it, and the next chunk's first MMA is issued as soon
+// as the state image is written.
 //
 // Ragged chunks: tokens t >= n get alpha = 1 and beta = 0, which makes their
 // rows of T the identity rows and their U, W, Delta rows zero, so whatever the
@@ -52,13 +56,14 @@ using namespace tc;
 
 constexpr int C = 64;    // chunk
 constexpr int D = 128;   // dk = dv
-constexpr int DVT = 64;  // state rows per phase-B CTA
+constexpr int DVT = 32;  // state rows per phase-B CTA
 constexpr uint64_t kWaitNs = 1000000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
 
 // Workspace record per (chunk, value head), bytes.
 constexpr uint32_t REC_W = 0;         // W image: 2 SW128 blocks (dk 0-63, 64-127) x 64 rows
 constexpr uint32_t REC_P = 16384;     // P' image: 1 SW128 block, 64 rows
-constexpr uint32_t REC_U = 24576;     // U images: 2 dv tiles x SW128 block of 64 rows
+constexpr uint32_t REC_U = 24576;     // U: 4 dv tiles of [64 t][32 i], 4 KB each
 constexpr uint32_t REC_VEC = 40960;   // gamma[64], w[64], gamma_last
 constexpr uint32_t REC_BYTES = 41984;
 
@@ -103,6 +108,10 @@ __device__ __forceinline__ void unpack8(uint4 u, float *v) {
 // Byte offset of the 16-byte chunk holding elements [8*q, 8*q+8) of row r.
 __device__ __forceinline__ uint32_t sw128_chunk(int r, int q) {
     return (uint32_t)(r * 128 + (((q ^ (r & 7)) & 7) << 4));
+}
+// Same for the 64-byte rows of a 32-column U tile (chunks swizzled by row % 4).
+__device__ __forceinline__ uint32_t u32_chunk(int r, int q) {
+    return (uint32_t)(r * 64 + (((q ^ (r & 3)) & 3) << 4));
 }
 
 // ---- chunk bookkeeping ------------------------------------------------------
@@ -155,12 +164,86 @@ struct TcMaps {
 
 constexpr uint32_t A_KQ = 0;          // [K;Q] image, 2 K-blocks of 128 rows (32 KB)
 constexpr uint32_t A_V = 32768;       // V image, 2 dv blocks of 64 rows (16 KB)
-constexpr uint32_t A_IMG = 49152;     // [T*beta ; T*beta*gamma] hi (16 KB) | lo (16 KB); At aliases it
+constexpr uint32_t A_IMG = 49152;     // [T*beta ; T*beta*gamma] hi (16 KB) | lo (16 KB)
+constexpr uint32_t A_AT = A_IMG;      //   aliased before the images exist: A^T fp32 [64][68]
+constexpr uint32_t A_X = A_IMG + 64 * 68 * 4;  //   and the blocked-inverse scratch, 3 x 16 x 16 fp32
 constexpr uint32_t A_T = 81920;       // T fp32 [64][68]
 constexpr uint32_t A_VEC = A_T + 64 * 68 * 4;  // g, beta, gamma, w: 4 x 64 floats
 constexpr uint32_t A_BAR = A_VEC + 1024;
 constexpr uint32_t A_SMEM = A_BAR + 64 + 1024;  // + alignment slack
-constexpr int AT_LD = 68;
+constexpr int LD = 68;                           // fp32 row stride of A^T and T
+
+// T = (I + A)^{-1} for the strictly lower 64 x 64 matrix A (A[r][c] = At[c*LD + r]),
+// blocked in 16 x 16 tiles: the four diagonal tiles D_J = (I + A_JJ)^{-1} by
+// forward substitution, then the off-diagonal tiles by increasing distance,
+// T_JI = -D_J (sum_{I <= K < J} A_JK T_KI).  Each thread of a level computes a
+// 2 x 4 piece of a tile (rows rr and rr + 8, columns c0 .. c0 + 3) so that one
+// float4 of T feeds eight FMAs.  All 128 threads; T written to sT.
+__device__ __forceinline__ void blocked_unit_lower_inverse(const float *At, float *sT, float *X, int tid) {
+    if (tid < 64) {
+        const int bb = tid >> 4, cl = tid & 15, o = 16 * bb;
+        float acc[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) acc[r] = 0.f;
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+            const float x = (t < cl) ? 0.f : ((t == cl) ? 1.f : -acc[t]);
+            sT[(o + t) * LD + o + cl] = x;
+#pragma unroll
+            for (int r = t + 1; r < 16; ++r) acc[r] = fmaf(At[(o + t) * LD + o + r], x, acc[r]);
+        }
+    } else {
+        // zero the tiles above the diagonal
+        for (int e = tid - 64; e < 6 * 64; e += 64) {
+            const int blk = e >> 6, r = (e >> 2) & 15, c4 = (e & 3) * 4;
+            const int I = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+            const int J = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+            *reinterpret_cast<float4 *>(sT + (16 * I + r) * LD + 16 * J + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    __syncthreads();
+    const int q = tid & 31, rr = q >> 2, c0 = (q & 3) * 4;
+    for (int d = 1; d < 4; ++d) {
+        const int nb = 4 - d;
+        const int blk = tid >> 5, I = blk, J = blk + d;
+        if (blk < nb) {
+            float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+            for (int K = I; K < J; ++K) {
+#pragma unroll 4
+                for (int m = 0; m < 16; ++m) {
+                    const float* ar = At + (16 * K + m) * LD + 16 * J + rr;
+                    const float x0 = ar[0], x1 = ar[8];
+                    const float4 t4 = *reinterpret_cast<const float4 *>(sT + (16 * K + m) * LD + 16 * I + c0);
+                    a0.x = fmaf(x0, t4.x, a0.x); a0.y = fmaf(x0, t4.y, a0.y);
+                    a0.z = fmaf(x0, t4.z, a0.z); a0.w = fmaf(x0, t4.w, a0.w);
+                    a1.x = fmaf(x1, t4.x, a1.x); a1.y = fmaf(x1, t4.y, a1.y);
+                    a1.z = fmaf(x1, t4.z, a1.z); a1.w = fmaf(x1, t4.w, a1.w);
+                }
+            }
+            *reinterpret_cast<float4 *>(X + blk * 256 + rr * 16 + c0) = a0;
+            *reinterpret_cast<float4 *>(X + blk * 256 + (rr + 8) * 16 + c0) = a1;
+        }
+        __syncthreads();
+        if (blk < nb) {
+            float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+#pragma unroll 4
+            for (int m = 0; m < 16; ++m) {
+                const float d0 = sT[(16 * J + rr) * LD + 16 * J + m];
+                const float d1 = sT[(16 * J + rr + 8) * LD + 16 * J + m];
+                const float4 x4 = *reinterpret_cast<const float4 *>(X + blk * 256 + m * 16 + c0);
+                a0.x = fmaf(d0, x4.x, a0.x); a0.y = fmaf(d0, x4.y, a0.y);
+                a0.z = fmaf(d0, x4.z, a0.z); a0.w = fmaf(d0, x4.w, a0.w);
+                a1.x = fmaf(d1, x4.x, a1.x); a1.y = fmaf(d1, x4.y, a1.y);
+                a1.z = fmaf(d1, x4.z, a1.z); a1.w = fmaf(d1, x4.w, a1.w);
+            }
+            *reinterpret_cast<float4 *>(sT + (16 * J + rr) * LD + 16 * I + c0) =
+                make_float4(-a0.x, -a0.y, -a0.z, -a0.w);
+            *reinterpret_cast<float4 *>(sT + (16 * J + rr + 8) * LD + 16 * I + c0) =
+                make_float4(-a1.x, -a1.y, -a1.z, -a1.w);
+        }
+        __syncthreads();
+    }
+}
 
 template <typename E>
 __global__ void __launch_bounds__(128, 2)
@@ -171,10 +254,11 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     uint8_t *sKQ = sm + A_KQ;
     uint8_t *sV = sm + A_V;
     uint8_t *sImg = sm + A_IMG;
-    float *At = reinterpret_cast<float *>(sm + A_IMG);
+    float *At = reinterpret_cast<float *>(sm + A_AT);
+    float *X = reinterpret_cast<float *>(sm + A_X);
     float *sT = reinterpret_cast<float *>(sm + A_T);
     float *vg = reinterpret_cast<float *>(sm + A_VEC);
-    float *vbeta = vg + 64, *vgam = vg + 128, *vw = vg + 192;
+    float *vbeta = vg + 64, *vgam = vg + 128;
     uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + A_BAR);
     uint64_t *bar_mma = bar_ld + 1;
     uint32_t *slot = reinterpret_cast<uint32_t *>(bar_ld + 2);
@@ -219,8 +303,29 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
         vg[tid] = (tid < n) ? logf(ld_gate(p.alpha, gi, p.dt_gate)) : 0.f;
         vbeta[tid] = (tid < n) ? ld_gate(p.beta, gi, p.dt_gate) : 0.f;
     }
+    fence_before_sync();
     __syncthreads();
-    if (warp == 0) {
+    fence_after_sync();
+    const uint32_t tbase = *slot;
+    const uint32_t lane_base = tbase + ((uint32_t)(32 * warp) << 16);
+    const bool kbf = Elem<E>::kBf16;
+    bool ok = true;
+    if (tid == 0) {
+        // [K; Q] K^T -> TMEM cols [0, 64): rows 0-63 K K^T, rows 64-127 Q K^T
+        ok = mbar_wait(bar_ld, 0, kWaitNs);
+        if (ok) {
+            fence_after_sync();
+            const uint64_t d0 = desc_sw128(smem_u32(sKQ), 16, 1024);
+            const uint32_t id = idesc_f16(128, 64, false, false, kbf);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint64_t d = desc_add(d0, (k >> 2) * 16384 + (k & 3) * 32);
+                mma_f16(tbase, d, d, id, k > 0);
+            }
+            mma_commit(bar_mma);
+        }
+    } else if (warp == 1) {
+        // cumulative log2-decay g2 (base-2 exponents), gamma, w while the MMA runs
         float x0 = vg[lane], x1 = vg[lane + 32];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -230,39 +335,20 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
         }
         x1 += __shfl_sync(0xffffffffu, x0, 31);
         const float glast = __shfl_sync(0xffffffffu, x1, 31);
-        vg[lane] = x0;
-        vg[lane + 32] = x1;
         const float g0 = expf(x0), g1 = expf(x1), w0 = expf(glast - x0), w1 = expf(glast - x1);
-        vgam[lane] = g0; vgam[lane + 32] = g1; vw[lane] = w0; vw[lane + 32] = w1;
+        vg[lane] = x0 * kLog2e;
+        vg[lane + 32] = x1 * kLog2e;
+        vgam[lane] = g0; vgam[lane + 32] = g1;
         float *rv = reinterpret_cast<float *>(rec + REC_VEC);
         rv[lane] = g0; rv[lane + 32] = g1; rv[64 + lane] = w0; rv[96 + lane] = w1;
         if (lane == 0) rv[128] = expf(glast);
     }
-    fence_before_sync();
     __syncthreads();
-    fence_after_sync();
-    const uint32_t tbase = *slot;
-    const uint32_t lane_base = tbase + ((uint32_t)(32 * warp) << 16);
-    const bool kbf = Elem<E>::kBf16;
-    bool ok = mbar_wait(bar_ld, 0, kWaitNs);
-
-    // ---- [K; Q] K^T -> TMEM cols [0, 64): rows 0-63 K K^T, rows 64-127 Q K^T
-    if (ok && tid == 0) {
-        fence_after_sync();
-        const uint32_t s = smem_u32(sKQ);
-        const uint32_t id = idesc_f16(128, 64, false, false, kbf);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-            mma_f16(tbase, desc_sw128(s + off, 16, 1024), desc_sw128(s + off, 16, 1024), id, k > 0);
-        }
-        mma_commit(bar_mma);
-    }
     ok = ok && mbar_wait(bar_mma, 0, kWaitNs);
     fence_after_sync();
     if (ok) {
         if (warp < 2) {
-            // A, stored transposed: At[i][t] = A[t][i]
+            // A, stored transposed: At[i][t] = A[t][i] = beta_t 2^{g2_t - g2_i} k_t.k_i
             const int t = tid;
             const float gt = vg[t], bt = vbeta[t];
 #pragma unroll
@@ -272,7 +358,7 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
 #pragma unroll
                 for (int ii = 0; ii < 32; ++ii) {
                     const int i = 32 * hh + ii;
-                    At[i * AT_LD + t] = (i < t) ? bt * expf(gt - vg[i]) * v[ii] : 0.f;
+                    At[i * LD + t] = (i < t) ? bt * exp2f(gt - vg[i]) * v[ii] : 0.f;
                 }
             }
         } else {
@@ -290,7 +376,7 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int i = 32 * hh + 8 * q8 + e;
-                        pv[e] = (i <= t) ? expf(gt - vg[i]) * v[8 * q8 + e] : 0.f;
+                        pv[e] = (i <= t) ? exp2f(gt - vg[i]) * v[8 * q8 + e] : 0.f;
                     }
                     *reinterpret_cast<uint4 *>(dst + sw128_chunk(t, 4 * hh + q8)) = pack8<E>(pv);
                 }
@@ -299,38 +385,23 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     }
     __syncthreads();
 
-    // ---- T = (I + A)^{-1}: thread c < 64 solves column c, right-looking ----
-    if (ok && warp < 2) {
-        const int col = tid;
-        float acc[64];
-#pragma unroll
-        for (int r = 0; r < 64; ++r) acc[r] = 0.f;
-#pragma unroll
-        for (int t = 0; t < 64; ++t) {
-            const float xt = (t < col) ? 0.f : ((t == col) ? 1.f : -acc[t]);
-            sT[t * AT_LD + col] = xt;
-#pragma unroll
-            for (int r4 = ((t + 1) >> 2) << 2; r4 < 64; r4 += 4) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(At + t * AT_LD + r4);
-                acc[r4 + 0] = fmaf(a4.x, xt, acc[r4 + 0]);
-                acc[r4 + 1] = fmaf(a4.y, xt, acc[r4 + 1]);
-                acc[r4 + 2] = fmaf(a4.z, xt, acc[r4 + 2]);
-                acc[r4 + 3] = fmaf(a4.w, xt, acc[r4 + 3]);
-            }
-        }
+    // ---- T = (I + A)^{-1}
+    if (ok) blocked_unit_lower_inverse(At, sT, X, tid);
+    else {
+        __syncthreads(); __syncthreads(); __syncthreads(); __syncthreads(); __syncthreads(); __syncthreads();
+        __syncthreads();
     }
-    __syncthreads();
 
     // ---- operand images [T diag(beta) ; T diag(beta gamma)], hi and lo parts
     if (ok) {
         const int t = tid & 63, which = tid >> 6, r = which * 64 + t;
-#pragma unroll
+#pragma unroll 2
         for (int q8 = 0; q8 < 8; ++q8) {
             float hi[8], lo[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int s = 8 * q8 + e;
-                const float val = sT[t * AT_LD + s] * (which ? vbeta[s] * vgam[s] : vbeta[s]);
+                const float val = sT[t * LD + s] * (which ? vbeta[s] * vgam[s] : vbeta[s]);
                 hi[e] = Elem<E>::round(val);
                 lo[e] = val - hi[e];
             }
@@ -345,28 +416,29 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     // ---- U = [T b ; T b g] V (rows 0-63 used) -> TMEM cols [64, 192)
     if (ok && tid == 0) {
         fence_after_sync();
-        const uint32_t si = smem_u32(sImg), sv = smem_u32(sV);
+        const uint64_t a0 = desc_sw128(smem_u32(sImg), 16, 1024), b0 = desc_sw128(smem_u32(sV), 8192, 1024);
         const uint32_t id = idesc_f16(128, 128, false, true, kbf);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const uint64_t bd = desc_sw128(sv + k * 2048, 8192, 1024);
-            mma_f16(tbase + 64, desc_sw128(si + k * 32, 16, 1024), bd, id, k > 0);
-            mma_f16(tbase + 64, desc_sw128(si + 16384 + k * 32, 16, 1024), bd, id, 1);
+            const uint64_t bd = desc_add(b0, k * 2048);
+            mma_f16(tbase + 64, desc_add(a0, k * 32), bd, id, k > 0);
+            mma_f16(tbase + 64, desc_add(a0, 16384 + k * 32), bd, id, 1);
         }
         mma_commit(bar_mma);
     }
     ok = ok && mbar_wait(bar_mma, 1, kWaitNs);
     fence_after_sync();
     if (ok && warp < 2) {
+        // U as four thread-read tiles of 32 dv columns: [64 t][32 i], 16-byte chunks swizzled by t
         const int t = tid;
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
             float v[32];
             tmem_ld32(lane_base + 64 + 32 * q4, v);
-            uint8_t *dst = rec + REC_U + (q4 >> 1) * 8192;
+            uint8_t *dst = rec + REC_U + q4 * 4096;
 #pragma unroll
             for (int q8 = 0; q8 < 4; ++q8)
-                *reinterpret_cast<uint4 *>(dst + sw128_chunk(t, (q4 & 1) * 4 + q8)) = pack8<E>(v + 8 * q8);
+                *reinterpret_cast<uint4 *>(dst + u32_chunk(t, q8)) = pack8<E>(v + 8 * q8);
         }
     }
     fence_before_sync();
@@ -375,13 +447,13 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     // ---- W = [T b ; T b g] K (rows 64-127 used) -> TMEM cols [64, 192)
     if (ok && tid == 0) {
         fence_after_sync();
-        const uint32_t si = smem_u32(sImg), sk = smem_u32(sKQ);
+        const uint64_t a0 = desc_sw128(smem_u32(sImg), 16, 1024), b0 = desc_sw128(smem_u32(sKQ), 16384, 1024);
         const uint32_t id = idesc_f16(128, 128, false, true, kbf);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const uint64_t bd = desc_sw128(sk + k * 2048, 16384, 1024);
-            mma_f16(tbase + 64, desc_sw128(si + k * 32, 16, 1024), bd, id, k > 0);
-            mma_f16(tbase + 64, desc_sw128(si + 16384 + k * 32, 16, 1024), bd, id, 1);
+            const uint64_t bd = desc_add(b0, k * 2048);
+            mma_f16(tbase + 64, desc_add(a0, k * 32), bd, id, k > 0);
+            mma_f16(tbase + 64, desc_add(a0, 16384 + k * 32), bd, id, 1);
         }
         mma_commit(bar_mma);
     }
@@ -412,17 +484,19 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
 
 constexpr uint32_t ST_A1 = 0;        // [Q ; W] image, 2 K-blocks of 128 rows
 constexpr uint32_t ST_K = 32768;     // K image, 2 dk blocks of 64 rows
-constexpr uint32_t ST_P = 49152;     // P' image (rows 0-63 of the [P'; X] operand)
-constexpr uint32_t ST_U = 57344;     // U tile image (also the unused rows 64-127 of [P'; X])
-constexpr uint32_t ST_VEC = 65536;   // gamma, w, gamma_last
-constexpr uint32_t ST_BYTES = 66560;
-constexpr int NS = 2;
-constexpr uint32_t B_S = NS * ST_BYTES;        // S^T image (MN-major, 128 K-rows)
-constexpr uint32_t B_DW = B_S + 16384;         // diag(w) Delta image
+constexpr uint32_t ST_P = 49152;     // P' image (rows 0-63 of the [P'; X] operand; X = what follows)
+constexpr uint32_t ST_U = 57344;     // U tile, [64 t][32 i]
+constexpr uint32_t ST_VEC = 61440;   // gamma, w, gamma_last
+constexpr uint32_t ST_BYTES = 62464;
+constexpr int NS = 3;
+constexpr uint32_t B_S = NS * ST_BYTES;        // S^T image (MN-major, 128 K-rows, 32 N used)
+constexpr uint32_t B_DW = B_S + 16384;         // diag(w) Delta image (64 K-rows)
 constexpr uint32_t B_DD = B_DW + 8192;         // Delta image
 constexpr uint32_t B_BAR = B_DD + 8192;
 constexpr uint32_t B_SMEM = B_BAR + 128 + 1024;
-constexpr uint32_t STAGE_TX = 16384 + 16384 + 16384 + 8192 + 8192 + 1024;
+constexpr uint32_t STAGE_TX = 16384 + 16384 + 16384 + 8192 + 4096 + 1024;
+constexpr int ISSUER = 64;                     // thread issuing the MMAs (warp 2)
+constexpr int COPIER = 32;                     // thread issuing stage copies (warp 1, off the chain)
 
 template <typename E>
 __global__ void __launch_bounds__(128, 1)
@@ -432,8 +506,8 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sS = sm + B_S, *sDw = sm + B_DW, *sDd = sm + B_DD;
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + B_BAR);  // [NS]
-    uint64_t *bar1 = full + NS, *bar2 = full + NS + 1;
-    uint32_t *slot = reinterpret_cast<uint32_t *>(full + NS + 2);
+    uint64_t *bar1 = full + NS, *bar2 = full + NS + 1, *bar3 = full + NS + 2;
+    uint32_t *slot = reinterpret_cast<uint32_t *>(full + NS + 3);
 
     const int tid = threadIdx.x, warp = tid >> 5;
     const int vt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -462,8 +536,19 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
         tma_load_3d(st + ST_K, &mk, 0, hk, t0, &full[s]);
         tma_load_3d(st + ST_K + 8192, &mk, 64, hk, t0, &full[s]);
         bulk_load(st + ST_P, rec + REC_P, 8192, &full[s]);
-        bulk_load(st + ST_U, rec + REC_U + vt * 8192, 8192, &full[s]);
+        bulk_load(st + ST_U, rec + REC_U + vt * 4096, 4096, &full[s]);
         bulk_load(st + ST_VEC, rec + REC_VEC, 1024, &full[s]);
+    };
+    auto prefetch_chunk = [&](int cc) {
+        const uint8_t *rec = rec0 + (size_t)cc * rec_stride;
+        const int t0 = (int)(rtok0 + (long)cc * C);
+        tma_prefetch_l2_3d(&mq, 0, hk, t0);
+        tma_prefetch_l2_3d(&mq, 64, hk, t0);
+        tma_prefetch_l2_3d(&mk, 0, hk, t0);
+        tma_prefetch_l2_3d(&mk, 64, hk, t0);
+        bulk_prefetch_l2(rec + REC_W, 16384 + 8192);
+        bulk_prefetch_l2(rec + REC_U + vt * 4096, 4096);
+        bulk_prefetch_l2(rec + REC_VEC, 1024);
     };
 
     if (tid == 0) {
@@ -472,6 +557,7 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
         for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
         mbar_init(bar1, 1);
         mbar_init(bar2, 1);
+        mbar_init(bar3, 1);
         fence_mbar_init();
     }
     __syncthreads();
@@ -479,10 +565,12 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
         tmem_alloc(slot, 256);
         tmem_relinquish();
     }
-    if (tid == 0)
+    if (tid == COPIER) {
         for (int cc = 0; cc < NS && cc < nc; ++cc) issue_stage(cc);
+        for (int cc = NS; cc < NS + 2 && cc < nc; ++cc) prefetch_chunk(cc);
+    }
 
-    // state tile: thread j holds S[i0 + i][j], i < 64 (row j of S^T)
+    // state tile: thread j holds S[i0 + i][j], i < 32 (row j of S^T)
     const int j = tid;
     float S[DVT];
     {
@@ -490,7 +578,7 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
 #pragma unroll
         for (int i = 0; i < DVT; ++i) S[i] = s0 ? s0[(size_t)(i0 + i) * D + j] : 0.f;
 #pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8)
+        for (int q8 = 0; q8 < DVT / 8; ++q8)
             *reinterpret_cast<uint4 *>(sS + sw128_chunk(j, q8)) = pack8<E>(S + 8 * q8);
     }
     fence_proxy_async();
@@ -500,109 +588,130 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     const uint32_t tbase = *slot;
     const uint32_t lane_base = tbase + ((uint32_t)(32 * warp) << 16);
     const bool kbf = Elem<E>::kBf16;
-    const uint32_t id1 = idesc_f16(128, 64, false, true, kbf);
-    const uint32_t id2 = idesc_f16(128, 64, true, true, kbf);
-    const uint32_t id3 = idesc_f16(128, 64, false, true, kbf);
+    const uint32_t id1 = idesc_f16(128, DVT, false, true, kbf);
+    const uint32_t id2 = idesc_f16(128, DVT, true, true, kbf);
+    const uint32_t id3 = idesc_f16(128, DVT, false, true, kbf);
     E *ob = reinterpret_cast<E *>(p.out);
     bool ok = true;
+    // loop-invariant operand descriptors
+    const uint64_t bS0 = desc_sw128(smem_u32(sS), 8192, 1024);
+    const uint64_t bDw0 = desc_sw128(smem_u32(sDw), 8192, 1024);
+    const uint64_t bDd0 = desc_sw128(smem_u32(sDd), 8192, 1024);
+
+    // D1 = [Q; W] S^T for chunk cc, double-buffered in TMEM columns [0,32) / [32,64)
+    auto issue_mma1 = [&](int cc) -> bool {
+        const int s = cc % NS;
+        if (!mbar_wait(&full[s], (cc / NS) & 1, kWaitNs)) return false;
+        fence_after_sync();
+        const uint64_t a0 = desc_sw128(smem_u32(sm + s * ST_BYTES + ST_A1), 16, 1024);
+        const uint32_t d1 = (cc & 1) ? 32u : 0u;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            mma_f16(tbase + d1, desc_add(a0, (k >> 2) * 16384 + (k & 3) * 32), desc_add(bS0, k * 2048), id1,
+                    k > 0);
+        mma_commit(bar1);
+        return true;
+    };
+    if (tid == ISSUER && nc > 0) issue_mma1(0);  // a timeout here surfaces as one on bar1
 
     for (int cc = 0; cc < nc && ok; ++cc) {
         const int s = cc % NS;
         uint8_t *st = sm + s * ST_BYTES;
-        const uint32_t d1 = (cc & 1) ? 192u : 0u;
+        const uint32_t d1 = (cc & 1) ? 32u : 0u;        // D1 = [Q; W] S^T (double-buffered)
+        const uint32_t d3 = (cc & 1) ? 128u : 96u;      // D3 = P' Delta   (double-buffered)
         const int n = min(C, len - cc * C);
         ok = mbar_wait(&full[s], (cc / NS) & 1, kWaitNs);
         if (!ok) break;
-        if (tid == 0) {
-            fence_after_sync();
-            const uint32_t sa = smem_u32(st + ST_A1), sb = smem_u32(sS);
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                mma_f16(tbase + d1, desc_sw128(sa + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
-                        desc_sw128(sb + k * 2048, 8192, 1024), id1, k > 0);
-            mma_commit(bar1);
-        }
+        // everything this chunk needs from the stage's vectors is read now:
+        // the stage is refilled right after the block barrier below
         const float *vec = reinterpret_cast<const float *>(st + ST_VEC);
         const float gC = vec[128];
         const float gt = (warp < 2) ? vec[tid] : 0.f;
-        const float wt = (warp >= 2) ? vec[64 + tid - 64] : 0.f;
-        ok = mbar_wait(bar1, cc & 1, kWaitNs);
-        if (!ok) break;
-        fence_after_sync();
         if (warp >= 2) {
             // Delta = U - W S^T for token t = tid - 64
             const int t = tid - 64;
+            const float wt = vec[64 + t];
+            ok = mbar_wait(bar1, cc & 1, kWaitNs);
+            if (!ok) break;
+            fence_after_sync();
+            float ws[32];
+            tmem_ld32(lane_base + d1, ws);
             const uint8_t *su = st + ST_U;
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float ws[32];
-                tmem_ld32(lane_base + d1 + 32 * hh, ws);
+            for (int q8 = 0; q8 < 4; ++q8) {
+                float u[8], dd[8], dw[8];
+                unpack8<E>(*reinterpret_cast<const uint4 *>(su + u32_chunk(t, q8)), u);
 #pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8) {
-                    float u[8], dd[8], dw[8];
-                    unpack8<E>(*reinterpret_cast<const uint4 *>(su + sw128_chunk(t, 4 * hh + q8)), u);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        dd[e] = u[e] - ws[8 * q8 + e];
-                        dw[e] = wt * dd[e];
-                    }
-                    *reinterpret_cast<uint4 *>(sDd + sw128_chunk(t, 4 * hh + q8)) = pack8<E>(dd);
-                    *reinterpret_cast<uint4 *>(sDw + sw128_chunk(t, 4 * hh + q8)) = pack8<E>(dw);
+                for (int e = 0; e < 8; ++e) {
+                    dd[e] = u[e] - ws[8 * q8 + e];
+                    dw[e] = wt * dd[e];
                 }
+                *reinterpret_cast<uint4 *>(sDd + sw128_chunk(t, q8)) = pack8<E>(dd);
+                *reinterpret_cast<uint4 *>(sDw + sw128_chunk(t, q8)) = pack8<E>(dw);
             }
-        }
-        fence_proxy_async();
-        fence_before_sync();
-        __syncthreads();
-        if (tid == 0) {
-            fence_after_sync();
-            const uint32_t sk = smem_u32(st + ST_K), sp = smem_u32(st + ST_P);
-            const uint32_t sdw = smem_u32(sDw), sdd = smem_u32(sDd);
+            fence_proxy_async();
+            fence_before_sync();
+            named_bar(1, 64);
+            if (tid == ISSUER) {
+                fence_after_sync();
+                const uint64_t k0 = desc_sw128(smem_u32(st + ST_K), 8192, 1024);
+                const uint64_t p0 = desc_sw128(smem_u32(st + ST_P), 16, 1024);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                mma_f16(tbase + 64, desc_sw128(sk + k * 2048, 8192, 1024),
-                        desc_sw128(sdw + k * 2048, 8192, 1024), id2, k > 0);
-                mma_f16(tbase + 128, desc_sw128(sp + k * 32, 16, 1024),
-                        desc_sw128(sdd + k * 2048, 8192, 1024), id3, k > 0);
+                for (int k = 0; k < 4; ++k)
+                    mma_f16(tbase + 64, desc_add(k0, k * 2048), desc_add(bDw0, k * 2048), id2, k > 0);
+                mma_commit(bar2);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_f16(tbase + d3, desc_add(p0, k * 32), desc_add(bDd0, k * 2048), id3, k > 0);
+                mma_commit(bar3);
             }
-            mma_commit(bar2);
         }
+        // S <- gamma_last S + K^T diag(w) Delta   (TMEM lane j = dk index)
         ok = mbar_wait(bar2, cc & 1, kWaitNs);
         if (!ok) break;
         fence_after_sync();
-        // S <- gamma_last S + K^T diag(w) Delta   (TMEM lane j = dk index)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
+        {
             float v[32];
-            tmem_ld32(lane_base + 64 + 32 * hh, v);
+            tmem_ld32(lane_base + 64, v);
 #pragma unroll
-            for (int ii = 0; ii < 32; ++ii) S[32 * hh + ii] = fmaf(gC, S[32 * hh + ii], v[ii]);
+            for (int i = 0; i < DVT; ++i) S[i] = fmaf(gC, S[i], v[i]);
         }
 #pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8)
+        for (int q8 = 0; q8 < DVT / 8; ++q8)
             *reinterpret_cast<uint4 *>(sS + sw128_chunk(j, q8)) = pack8<E>(S + 8 * q8);
         fence_proxy_async();
+        if (warp < 2) {
+            // the output MMA of this chunk must be done before the barrier: after
+            // it the stage is refilled and the next chunk's MMAs may start
+            ok = mbar_wait(bar3, cc & 1, kWaitNs);
+            if (!ok) break;
+        }
         fence_before_sync();
         __syncthreads();
-        if (tid == 0 && cc + NS < nc) issue_stage(cc + NS);
+        if (tid == ISSUER) {
+            fence_after_sync();
+            if (cc + 1 < nc) issue_mma1(cc + 1);
+        }
+        if (tid == COPIER) {
+            // the stage of this chunk is free: its MMAs completed (bar2, bar3)
+            if (cc + NS < nc) issue_stage(cc + NS);
+            if (cc + NS + 2 < nc) prefetch_chunk(cc + NS + 2);
+        }
         if (warp < 2) {
             // O = gamma_t (Q S^T) + P' Delta for token t = tid
             const int t = tid;
             fence_after_sync();
+            float qs[32], pd[32];
+            tmem_ld32(lane_base + d1, qs);
+            tmem_ld32(lane_base + d3, pd);
+            if (t < n) {
+                E *dst = ob + ((rtok0 + (long)cc * C + t) * Hv + h) * (long)D + i0;
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float qs[32], pd[32];
-                tmem_ld32(lane_base + d1 + 32 * hh, qs);
-                tmem_ld32(lane_base + 128 + 32 * hh, pd);
-                if (t < n) {
-                    E *dst = ob + ((rtok0 + (long)cc * C + t) * Hv + h) * (long)D + i0 + 32 * hh;
+                for (int q8 = 0; q8 < 4; ++q8) {
+                    float o[8];
 #pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8) {
-                        float o[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) o[e] = fmaf(gt, qs[8 * q8 + e], pd[8 * q8 + e]);
-                        *reinterpret_cast<uint4 *>(dst + 8 * q8) = pack8<E>(o);
-                    }
+                    for (int e = 0; e < 8; ++e) o[e] = fmaf(gt, qs[8 * q8 + e], pd[8 * q8 + e]);
+                    *reinterpret_cast<uint4 *>(dst + 8 * q8) = pack8<E>(o);
                 }
             }
             fence_before_sync();
@@ -615,9 +724,9 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
         for (int i = 0; i < DVT; ++i) sf[(size_t)i * D + j] = S[i];
     }
     if (!ok) {
-        if (tid == 0) atomicOr(p.err, (uint32_t)GDN_DEVERR_TIMEOUT);
+        atomicOr(p.err, (uint32_t)GDN_DEVERR_TIMEOUT);
         // let every copy this CTA issued land before its shared memory is released
-        for (int s = 0; s < NS; ++s) mbar_wait(&full[s], 0, kWaitNs / 4);
+        for (int s = 0; s < NS; ++s) mbar_wait(&full[s], 0, kWaitNs / 8);
     }
     fence_before_sync();
     __syncthreads();
