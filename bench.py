@@ -341,7 +341,7 @@ def run_ours(args, rank, world, local_rank):
                 "kernel": "recurrent_kernel<128,bf16> (decode, T=1)",
                 "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
                 "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
-                "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": DECODE_TRAFFIC_BYTES,
                 "algorithmic_bytes_per_launch": dec_bytes_call,
                 "avg_launch_us": round(launch_avg_s * 1e6, 2),
             },
@@ -374,7 +374,10 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
-PREFILL_LAUNCHES = 1  # kernels one gdn_prefill_chunked call launches on this workload
+PREFILL_LAUNCHES = 2  # kernels one gdn_prefill_chunked call launches on this workload (tensor-core path)
+# DRAM bytes (read + write) of one decode launch at B=256, from one ncu capture of
+# the current recurrent kernel (profiles/recurrent_decode_B256_traffic.md).
+DECODE_TRAFFIC_BYTES = 541_230_000 + 485_970_000
 
 
 def run_e2e(args, gdn, dev, stream, hq, hk_, hv, ha, hb, S0_host, counts, d):
