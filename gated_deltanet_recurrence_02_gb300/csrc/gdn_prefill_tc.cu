@@ -58,7 +58,6 @@ constexpr int C = 64;    // chunk
 constexpr int D = 128;   // dk = dv
 constexpr int DVT = 32;  // state rows per phase-B CTA
 constexpr uint64_t kWaitNs = 1000000000ull;
-constexpr float kLog2e = 1.4426950408889634f;
 
 // Workspace record per (chunk, value head), bytes.
 constexpr uint32_t REC_W = 0;         // W image: 2 SW128 blocks (dk 0-63, 64-127) x 64 rows
@@ -176,9 +175,10 @@ constexpr int LD = 68;                           // fp32 row stride of A^T and T
 // T = (I + A)^{-1} for the strictly lower 64 x 64 matrix A (A[r][c] = At[c*LD + r]),
 // blocked in 16 x 16 tiles: the four diagonal tiles D_J = (I + A_JJ)^{-1} by
 // forward substitution, then the off-diagonal tiles by increasing distance,
-// T_JI = -D_J (sum_{I <= K < J} A_JK T_KI).  Each thread of a level computes a
-// 2 x 4 piece of a tile (rows rr and rr + 8, columns c0 .. c0 + 3) so that one
-// float4 of T feeds eight FMAs.  All 128 threads; T written to sT.
+// T_JI = -D_J (sum_{I <= K < J} A_JK T_KI).  In the level stages each thread
+// computes a 1 x 4 piece of a tile (row r, columns c0 .. c0 + 3), fed by one
+// float4 of T per step.  256 threads; T written to sT.
+constexpr int kIntraThreads = 256;
 __device__ __forceinline__ void blocked_unit_lower_inverse(const float *At, float *sT, float *X, int tid) {
     if (tid < 64) {
         const int bb = tid >> 4, cl = tid & 15, o = 16 * bb;
@@ -194,7 +194,7 @@ __device__ __forceinline__ void blocked_unit_lower_inverse(const float *At, floa
         }
     } else {
         // zero the tiles above the diagonal
-        for (int e = tid - 64; e < 6 * 64; e += 64) {
+        for (int e = tid - 64; e < 6 * 64; e += kIntraThreads - 64) {
             const int blk = e >> 6, r = (e >> 2) & 15, c4 = (e & 3) * 4;
             const int I = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
             const int J = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
@@ -202,51 +202,41 @@ __device__ __forceinline__ void blocked_unit_lower_inverse(const float *At, floa
         }
     }
     __syncthreads();
-    const int q = tid & 31, rr = q >> 2, c0 = (q & 3) * 4;
+    const int q = tid & 63, r = q >> 2, c0 = (q & 3) * 4;
     for (int d = 1; d < 4; ++d) {
         const int nb = 4 - d;
-        const int blk = tid >> 5, I = blk, J = blk + d;
+        const int blk = tid >> 6, I = blk, J = blk + d;
         if (blk < nb) {
-            float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int K = I; K < J; ++K) {
-#pragma unroll 4
+#pragma unroll 8
                 for (int m = 0; m < 16; ++m) {
-                    const float* ar = At + (16 * K + m) * LD + 16 * J + rr;
-                    const float x0 = ar[0], x1 = ar[8];
+                    const float x = At[(16 * K + m) * LD + 16 * J + r];
                     const float4 t4 = *reinterpret_cast<const float4 *>(sT + (16 * K + m) * LD + 16 * I + c0);
-                    a0.x = fmaf(x0, t4.x, a0.x); a0.y = fmaf(x0, t4.y, a0.y);
-                    a0.z = fmaf(x0, t4.z, a0.z); a0.w = fmaf(x0, t4.w, a0.w);
-                    a1.x = fmaf(x1, t4.x, a1.x); a1.y = fmaf(x1, t4.y, a1.y);
-                    a1.z = fmaf(x1, t4.z, a1.z); a1.w = fmaf(x1, t4.w, a1.w);
+                    a.x = fmaf(x, t4.x, a.x); a.y = fmaf(x, t4.y, a.y);
+                    a.z = fmaf(x, t4.z, a.z); a.w = fmaf(x, t4.w, a.w);
                 }
             }
-            *reinterpret_cast<float4 *>(X + blk * 256 + rr * 16 + c0) = a0;
-            *reinterpret_cast<float4 *>(X + blk * 256 + (rr + 8) * 16 + c0) = a1;
+            *reinterpret_cast<float4 *>(X + blk * 256 + r * 16 + c0) = a;
         }
         __syncthreads();
         if (blk < nb) {
-            float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-#pragma unroll 4
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
             for (int m = 0; m < 16; ++m) {
-                const float d0 = sT[(16 * J + rr) * LD + 16 * J + m];
-                const float d1 = sT[(16 * J + rr + 8) * LD + 16 * J + m];
+                const float dd = sT[(16 * J + r) * LD + 16 * J + m];
                 const float4 x4 = *reinterpret_cast<const float4 *>(X + blk * 256 + m * 16 + c0);
-                a0.x = fmaf(d0, x4.x, a0.x); a0.y = fmaf(d0, x4.y, a0.y);
-                a0.z = fmaf(d0, x4.z, a0.z); a0.w = fmaf(d0, x4.w, a0.w);
-                a1.x = fmaf(d1, x4.x, a1.x); a1.y = fmaf(d1, x4.y, a1.y);
-                a1.z = fmaf(d1, x4.z, a1.z); a1.w = fmaf(d1, x4.w, a1.w);
+                a.x = fmaf(dd, x4.x, a.x); a.y = fmaf(dd, x4.y, a.y);
+                a.z = fmaf(dd, x4.z, a.z); a.w = fmaf(dd, x4.w, a.w);
             }
-            *reinterpret_cast<float4 *>(sT + (16 * J + rr) * LD + 16 * I + c0) =
-                make_float4(-a0.x, -a0.y, -a0.z, -a0.w);
-            *reinterpret_cast<float4 *>(sT + (16 * J + rr + 8) * LD + 16 * I + c0) =
-                make_float4(-a1.x, -a1.y, -a1.z, -a1.w);
+            *reinterpret_cast<float4 *>(sT + (16 * J + r) * LD + 16 * I + c0) = make_float4(-a.x, -a.y, -a.z, -a.w);
         }
         __syncthreads();
     }
 }
 
 template <typename E>
-__global__ void __launch_bounds__(128, 2)
+__global__ void __launch_bounds__(kIntraThreads, 2)
 prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap mq,
                      const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv) {
     extern __shared__ uint8_t smem_raw[];
@@ -307,7 +297,7 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     __syncthreads();
     fence_after_sync();
     const uint32_t tbase = *slot;
-    const uint32_t lane_base = tbase + ((uint32_t)(32 * warp) << 16);
+    const uint32_t lane_base = tbase + ((uint32_t)(32 * (warp & 3)) << 16);
     const bool kbf = Elem<E>::kBf16;
     bool ok = true;
     if (tid == 0) {
@@ -325,7 +315,7 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
             mma_commit(bar_mma);
         }
     } else if (warp == 1) {
-        // cumulative log2-decay g2 (base-2 exponents), gamma, w while the MMA runs
+        // cumulative log-decay g, gamma, w while the MMA runs
         float x0 = vg[lane], x1 = vg[lane + 32];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -336,8 +326,8 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
         x1 += __shfl_sync(0xffffffffu, x0, 31);
         const float glast = __shfl_sync(0xffffffffu, x1, 31);
         const float g0 = expf(x0), g1 = expf(x1), w0 = expf(glast - x0), w1 = expf(glast - x1);
-        vg[lane] = x0 * kLog2e;
-        vg[lane + 32] = x1 * kLog2e;
+        vg[lane] = x0;
+        vg[lane + 32] = x1;
         vgam[lane] = g0; vgam[lane + 32] = g1;
         float *rv = reinterpret_cast<float *>(rec + REC_VEC);
         rv[lane] = g0; rv[lane + 32] = g1; rv[64 + lane] = w0; rv[96 + lane] = w1;
@@ -347,39 +337,35 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     ok = ok && mbar_wait(bar_mma, 0, kWaitNs);
     fence_after_sync();
     if (ok) {
-        if (warp < 2) {
-            // A, stored transposed: At[i][t] = A[t][i] = beta_t 2^{g2_t - g2_i} k_t.k_i
-            const int t = tid;
+        // warp w reads TMEM lane quarter (w % 4); warps w and w + 4 split the 64 columns
+        const int quarter = warp & 3, half = warp >> 2;
+        if (quarter < 2) {
+            // A, stored transposed: At[i][t] = A[t][i] = beta_t e^{g_t - g_i} k_t.k_i  (i < t)
+            const int t = 32 * quarter + lane;
             const float gt = vg[t], bt = vbeta[t];
+            float v[32];
+            tmem_ld32(lane_base + 32 * half, v);
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float v[32];
-                tmem_ld32(lane_base + 32 * hh, v);
-#pragma unroll
-                for (int ii = 0; ii < 32; ++ii) {
-                    const int i = 32 * hh + ii;
-                    At[i * LD + t] = (i < t) ? bt * exp2f(gt - vg[i]) * v[ii] : 0.f;
-                }
+            for (int ii = 0; ii < 32; ++ii) {
+                const int i = 32 * half + ii;
+                At[i * LD + t] = (i < t) ? bt * __expf(gt - vg[i]) * v[ii] : 0.f;
             }
         } else {
-            // P' image straight to the workspace
-            const int t = tid - 64;
+            // P'[t][i] = e^{g_t - g_i} q_t.k_i (i <= t), image straight to the workspace
+            const int t = 32 * (quarter - 2) + lane;
             const float gt = vg[t];
             uint8_t *dst = rec + REC_P;
+            float v[32];
+            tmem_ld32(lane_base + 32 * half, v);
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float v[32];
-                tmem_ld32(lane_base + 32 * hh, v);
+            for (int q8 = 0; q8 < 4; ++q8) {
+                float pv[8];
 #pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8) {
-                    float pv[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int i = 32 * hh + 8 * q8 + e;
-                        pv[e] = (i <= t) ? exp2f(gt - vg[i]) * v[8 * q8 + e] : 0.f;
-                    }
-                    *reinterpret_cast<uint4 *>(dst + sw128_chunk(t, 4 * hh + q8)) = pack8<E>(pv);
+                for (int e = 0; e < 8; ++e) {
+                    const int i = 32 * half + 8 * q8 + e;
+                    pv[e] = (i <= t) ? __expf(gt - vg[i]) * v[8 * q8 + e] : 0.f;
                 }
+                *reinterpret_cast<uint4 *>(dst + sw128_chunk(t, 4 * half + q8)) = pack8<E>(pv);
             }
         }
     }
@@ -394,9 +380,10 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
 
     // ---- operand images [T diag(beta) ; T diag(beta gamma)], hi and lo parts
     if (ok) {
-        const int t = tid & 63, which = tid >> 6, r = which * 64 + t;
-#pragma unroll 2
-        for (int q8 = 0; q8 < 8; ++q8) {
+        const int t = tid & 63, which = (tid >> 6) & 1, part = tid >> 7, r = which * 64 + t;
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+            const int q8 = 4 * part + qq;
             float hi[8], lo[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
@@ -428,11 +415,12 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     }
     ok = ok && mbar_wait(bar_mma, 1, kWaitNs);
     fence_after_sync();
-    if (ok && warp < 2) {
+    if (ok && (warp & 3) < 2) {
         // U as four thread-read tiles of 32 dv columns: [64 t][32 i], 16-byte chunks swizzled by t
-        const int t = tid;
+        const int t = 32 * (warp & 3) + lane, half = warp >> 2;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int qq = 0; qq < 2; ++qq) {
+            const int q4 = 2 * half + qq;
             float v[32];
             tmem_ld32(lane_base + 64 + 32 * q4, v);
             uint8_t *dst = rec + REC_U + q4 * 4096;
@@ -459,10 +447,11 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     }
     ok = ok && mbar_wait(bar_mma, 0, kWaitNs);
     fence_after_sync();
-    if (ok && warp >= 2) {
-        const int t = tid - 64;
+    if (ok && (warp & 3) >= 2) {
+        const int t = 32 * ((warp & 3) - 2) + lane, half = warp >> 2;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int qq = 0; qq < 2; ++qq) {
+            const int q4 = 2 * half + qq;
             float v[32];
             tmem_ld32(lane_base + 64 + 32 * q4, v);
             uint8_t *dst = rec + REC_W + (q4 >> 1) * 8192;
@@ -786,7 +775,7 @@ cudaError_t launch_e(const PrefillParams &p, long total_T, long max_chunks, cuda
     if (e != cudaSuccess) return e;
     if (max_chunks > 0) {
         dim3 ga((unsigned)max_chunks, p.Hv);
-        prefill_intra_kernel<E><<<ga, 128, A_SMEM, stream>>>(p, mq, mk, mv);
+        prefill_intra_kernel<E><<<ga, kIntraThreads, A_SMEM, stream>>>(p, mq, mk, mv);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
