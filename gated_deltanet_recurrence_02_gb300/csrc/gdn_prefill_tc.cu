@@ -16,9 +16,12 @@
 // Phase A (prefill_intra_kernel, one CTA per (chunk, value head), all chunks in
 // parallel): [K;Q] K^T on the tensor cores, A and P' from it, T by a blocked
 // (16 x 16 tiles) unit-lower-triangular inverse in fp32, then U and W on the
-// tensor cores with T split into a
-// bf16 hi part and a bf16 lo part (so T keeps ~16 bits).  Writes W, P' and U as
-// ready-made shared-memory operand images plus gamma / w into the workspace.
+// tensor cores with T rounded to the 16-bit input type (its rounding is of
+// the same size as the rounding of U and W themselves).  V is loaded into
+// Q's shared-memory slot once [K;Q]K^T has consumed Q; 71 KB of shared
+// memory and 128 TMEM columns per CTA let three CTAs share an SM.  Writes W,
+// P' and U as ready-made shared-memory operand images plus gamma / w into
+// the workspace.
 //
 // Phase B (prefill_carry_kernel, one CTA per (value head, 32-row dv tile,
 // row), serial over chunks): per chunk two dependent tensor-core steps,
@@ -161,15 +164,17 @@ struct TcMaps {
 
 // ============================================================ phase A ====
 
-constexpr uint32_t A_KQ = 0;          // [K;Q] image, 2 K-blocks of 128 rows (32 KB)
-constexpr uint32_t A_V = 32768;       // V image, 2 dv blocks of 64 rows (16 KB)
-constexpr uint32_t A_IMG = 49152;     // [T*beta ; T*beta*gamma] hi (16 KB) | lo (16 KB)
-constexpr uint32_t A_AT = A_IMG;      //   aliased before the images exist: A^T fp32 [64][68]
+constexpr uint32_t A_KQ = 0;          // [K;Q] image, 2 K-blocks of 128 rows (32 KB); V replaces Q
+constexpr uint32_t A_V0 = 8192;       //   V dv 0-63 (rows of the first K-block's Q half)
+constexpr uint32_t A_V1 = 24576;      //   V dv 64-127 (second K-block's Q half)
+constexpr uint32_t A_IMG = 32768;     // [T*beta ; T*beta*gamma] bf16 image (16 KB) ...
+constexpr uint32_t A_AT = A_IMG;      //   ... aliasing, before it exists, A^T fp32 [64][68]
 constexpr uint32_t A_X = A_IMG + 64 * 68 * 4;  //   and the blocked-inverse scratch, 3 x 16 x 16 fp32
-constexpr uint32_t A_T = 81920;       // T fp32 [64][68]
-constexpr uint32_t A_VEC = A_T + 64 * 68 * 4;  // g, beta, gamma, w: 4 x 64 floats
+constexpr uint32_t A_T = A_X + 3 * 256 * 4;    // T fp32 [64][68]
+constexpr uint32_t A_VEC = A_T + 64 * 68 * 4;  // g, beta, gamma: 3 x 64 floats (1 KB reserved)
 constexpr uint32_t A_BAR = A_VEC + 1024;
 constexpr uint32_t A_SMEM = A_BAR + 64 + 1024;  // + alignment slack
+constexpr uint32_t A_TMEM_COLS = 128;
 constexpr int LD = 68;                           // fp32 row stride of A^T and T
 
 // T = (I + A)^{-1} for the strictly lower 64 x 64 matrix A (A[r][c] = At[c*LD + r]),
@@ -236,13 +241,12 @@ __device__ __forceinline__ void blocked_unit_lower_inverse(const float *At, floa
 }
 
 template <typename E>
-__global__ void __launch_bounds__(kIntraThreads, 2)
+__global__ void __launch_bounds__(kIntraThreads, 3)
 prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap mq,
                      const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sKQ = sm + A_KQ;
-    uint8_t *sV = sm + A_V;
     uint8_t *sImg = sm + A_IMG;
     float *At = reinterpret_cast<float *>(sm + A_AT);
     float *X = reinterpret_cast<float *>(sm + A_X);
@@ -251,7 +255,8 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     float *vbeta = vg + 64, *vgam = vg + 128;
     uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + A_BAR);
     uint64_t *bar_mma = bar_ld + 1;
-    uint32_t *slot = reinterpret_cast<uint32_t *>(bar_ld + 2);
+    uint64_t *bar_v = bar_ld + 2;
+    uint32_t *slot = reinterpret_cast<uint32_t *>(bar_ld + 3);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = blockIdx.y, Hv = p.Hv, Hk = p.Hk;
@@ -272,21 +277,20 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
         prefetch_tensormap(&mv);
         mbar_init(bar_ld, 1);
         mbar_init(bar_mma, 1);
+        mbar_init(bar_v, 1);
         fence_mbar_init();
     }
     __syncthreads();
     if (warp == 0) {
-        tmem_alloc(slot, 256);
+        tmem_alloc(slot, A_TMEM_COLS);
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_arrive_expect_tx(bar_ld, 32768 + 16384);
+        mbar_arrive_expect_tx(bar_ld, 32768);
         tma_load_3d(sKQ, &mk, 0, hk, (int)tok0, bar_ld);
         tma_load_3d(sKQ + 16384, &mk, 64, hk, (int)tok0, bar_ld);
         tma_load_3d(sKQ + 8192, &mq, 0, hk, (int)tok0, bar_ld);
         tma_load_3d(sKQ + 24576, &mq, 64, hk, (int)tok0, bar_ld);
-        tma_load_3d(sV, &mv, 0, h, (int)tok0, bar_ld);
-        tma_load_3d(sV + 8192, &mv, 64, h, (int)tok0, bar_ld);
     }
     if (tid < C) {
         const long gi = (tok0 + tid) * Hv + h;
@@ -336,6 +340,12 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     __syncthreads();
     ok = ok && mbar_wait(bar_mma, 0, kWaitNs);
     fence_after_sync();
+    if (ok && tid == 0) {
+        // Q has been consumed: V takes its place (the load overlaps A, P' and T)
+        mbar_arrive_expect_tx(bar_v, 16384);
+        tma_load_3d(sm + A_V0, &mv, 0, h, (int)tok0, bar_v);
+        tma_load_3d(sm + A_V1, &mv, 64, h, (int)tok0, bar_v);
+    }
     if (ok) {
         // warp w reads TMEM lane quarter (w % 4); warps w and w + 4 split the 64 columns
         const int quarter = warp & 3, half = warp >> 2;
@@ -378,40 +388,36 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
         __syncthreads();
     }
 
-    // ---- operand images [T diag(beta) ; T diag(beta gamma)], hi and lo parts
+    // ---- operand image [T diag(beta) ; T diag(beta gamma)] in the 16-bit input type
     if (ok) {
         const int t = tid & 63, which = (tid >> 6) & 1, part = tid >> 7, r = which * 64 + t;
 #pragma unroll
         for (int qq = 0; qq < 4; ++qq) {
             const int q8 = 4 * part + qq;
-            float hi[8], lo[8];
+            float val[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int s = 8 * q8 + e;
-                const float val = sT[t * LD + s] * (which ? vbeta[s] * vgam[s] : vbeta[s]);
-                hi[e] = Elem<E>::round(val);
-                lo[e] = val - hi[e];
+                val[e] = sT[t * LD + s] * (which ? vbeta[s] * vgam[s] : vbeta[s]);
             }
-            *reinterpret_cast<uint4 *>(sImg + sw128_chunk(r, q8)) = pack8<E>(hi);
-            *reinterpret_cast<uint4 *>(sImg + 16384 + sw128_chunk(r, q8)) = pack8<E>(lo);
+            *reinterpret_cast<uint4 *>(sImg + sw128_chunk(r, q8)) = pack8<E>(val);
         }
     }
     fence_proxy_async();
     fence_before_sync();
     __syncthreads();
 
-    // ---- U = [T b ; T b g] V (rows 0-63 used) -> TMEM cols [64, 192)
+    // ---- U = [T b ; T b g] V (rows 0-63 used) -> TMEM cols [0, 128)
     if (ok && tid == 0) {
         fence_after_sync();
-        const uint64_t a0 = desc_sw128(smem_u32(sImg), 16, 1024), b0 = desc_sw128(smem_u32(sV), 8192, 1024);
-        const uint32_t id = idesc_f16(128, 128, false, true, kbf);
+        ok = mbar_wait(bar_v, 0, kWaitNs);
+        if (ok) {
+            const uint64_t a0 = desc_sw128(smem_u32(sImg), 16, 1024), b0 = desc_sw128(smem_u32(sm + A_V0), 16384, 1024);
+            const uint32_t id = idesc_f16(128, 128, false, true, kbf);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint64_t bd = desc_add(b0, k * 2048);
-            mma_f16(tbase + 64, desc_add(a0, k * 32), bd, id, k > 0);
-            mma_f16(tbase + 64, desc_add(a0, 16384 + k * 32), bd, id, 1);
+            for (int k = 0; k < 4; ++k) mma_f16(tbase, desc_add(a0, k * 32), desc_add(b0, k * 2048), id, k > 0);
+            mma_commit(bar_mma);
         }
-        mma_commit(bar_mma);
     }
     ok = ok && mbar_wait(bar_mma, 1, kWaitNs);
     fence_after_sync();
@@ -422,7 +428,7 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
         for (int qq = 0; qq < 2; ++qq) {
             const int q4 = 2 * half + qq;
             float v[32];
-            tmem_ld32(lane_base + 64 + 32 * q4, v);
+            tmem_ld32(lane_base + 32 * q4, v);
             uint8_t *dst = rec + REC_U + q4 * 4096;
 #pragma unroll
             for (int q8 = 0; q8 < 4; ++q8)
@@ -432,17 +438,13 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     fence_before_sync();
     __syncthreads();
 
-    // ---- W = [T b ; T b g] K (rows 64-127 used) -> TMEM cols [64, 192)
+    // ---- W = [T b ; T b g] K (rows 64-127 used) -> TMEM cols [0, 128)
     if (ok && tid == 0) {
         fence_after_sync();
         const uint64_t a0 = desc_sw128(smem_u32(sImg), 16, 1024), b0 = desc_sw128(smem_u32(sKQ), 16384, 1024);
         const uint32_t id = idesc_f16(128, 128, false, true, kbf);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint64_t bd = desc_add(b0, k * 2048);
-            mma_f16(tbase + 64, desc_add(a0, k * 32), bd, id, k > 0);
-            mma_f16(tbase + 64, desc_add(a0, 16384 + k * 32), bd, id, 1);
-        }
+        for (int k = 0; k < 4; ++k) mma_f16(tbase, desc_add(a0, k * 32), desc_add(b0, k * 2048), id, k > 0);
         mma_commit(bar_mma);
     }
     ok = ok && mbar_wait(bar_mma, 0, kWaitNs);
@@ -453,7 +455,7 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
         for (int qq = 0; qq < 2; ++qq) {
             const int q4 = 2 * half + qq;
             float v[32];
-            tmem_ld32(lane_base + 64 + 32 * q4, v);
+            tmem_ld32(lane_base + 32 * q4, v);
             uint8_t *dst = rec + REC_W + (q4 >> 1) * 8192;
 #pragma unroll
             for (int q8 = 0; q8 < 4; ++q8)
@@ -462,11 +464,13 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     }
     if (!ok) {
         if (tid == 0) atomicOr(p.err, (uint32_t)GDN_DEVERR_TIMEOUT);
-        mbar_wait(bar_ld, 0, kWaitNs);  // copies in flight must land before the CTA exits
+        // copies in flight must land before the CTA exits
+        mbar_wait(bar_ld, 0, kWaitNs);
+        mbar_wait(bar_v, 0, kWaitNs / 4);
     }
     fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, 256);
+    if (warp == 0) tmem_dealloc(tbase, A_TMEM_COLS);
 }
 
 // ============================================================ phase B ====
