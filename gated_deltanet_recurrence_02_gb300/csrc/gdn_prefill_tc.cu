@@ -488,11 +488,16 @@ constexpr uint32_t B_DD = B_DW + 8192;         // Delta image
 constexpr uint32_t B_BAR = B_DD + 8192;
 constexpr uint32_t B_SMEM = B_BAR + 128 + 1024;
 constexpr uint32_t STAGE_TX = 16384 + 16384 + 16384 + 8192 + 4096 + 1024;
-constexpr int ISSUER = 64;                     // thread issuing the MMAs (warp 2)
-constexpr int COPIER = 32;                     // thread issuing stage copies (warp 1, off the chain)
+// 8 compute warps: warp w reads TMEM lane quarter w % 4, warps w and w + 4
+// split the tile's 32 columns.  Warp 8 issues every MMA and copy.
+constexpr int kCarryComputeWarps = 8;
+constexpr int kCarryThreads = (kCarryComputeWarps + 1) * 32;
+constexpr int kIssuerWarp = kCarryComputeWarps;
+constexpr uint32_t kBarDelta = 1;  // named barrier: Delta images written (all warps)
+constexpr uint32_t kBarState = 2;  // named barrier: S image written (all warps)
 
 template <typename E>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kCarryThreads, 1)
 prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap mq,
                      const __grid_constant__ CUtensorMap mk) {
     extern __shared__ uint8_t smem_raw[];
@@ -502,7 +507,8 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     uint64_t *bar1 = full + NS, *bar2 = full + NS + 1, *bar3 = full + NS + 2;
     uint32_t *slot = reinterpret_cast<uint32_t *>(full + NS + 3);
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3, half = (warp >> 2) & 1;
     const int vt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int Hv = p.Hv, Hk = p.Hk;
     const int hk = h / (Hv / Hk);
@@ -515,34 +521,6 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
                           (size_t)chunk_base(p.cu_seqlens, p.B, p.T, b) * Hv * REC_BYTES +
                           (size_t)h * REC_BYTES;
     const size_t rec_stride = (size_t)Hv * REC_BYTES;
-
-    auto issue_stage = [&](int cc) {
-        const int s = cc % NS;
-        uint8_t *st = sm + s * ST_BYTES;
-        const uint8_t *rec = rec0 + (size_t)cc * rec_stride;
-        const int t0 = (int)(rtok0 + (long)cc * C);
-        mbar_arrive_expect_tx(&full[s], STAGE_TX);
-        tma_load_3d(st + ST_A1, &mq, 0, hk, t0, &full[s]);
-        tma_load_3d(st + ST_A1 + 16384, &mq, 64, hk, t0, &full[s]);
-        bulk_load(st + ST_A1 + 8192, rec + REC_W, 8192, &full[s]);
-        bulk_load(st + ST_A1 + 24576, rec + REC_W + 8192, 8192, &full[s]);
-        tma_load_3d(st + ST_K, &mk, 0, hk, t0, &full[s]);
-        tma_load_3d(st + ST_K + 8192, &mk, 64, hk, t0, &full[s]);
-        bulk_load(st + ST_P, rec + REC_P, 8192, &full[s]);
-        bulk_load(st + ST_U, rec + REC_U + vt * 4096, 4096, &full[s]);
-        bulk_load(st + ST_VEC, rec + REC_VEC, 1024, &full[s]);
-    };
-    auto prefetch_chunk = [&](int cc) {
-        const uint8_t *rec = rec0 + (size_t)cc * rec_stride;
-        const int t0 = (int)(rtok0 + (long)cc * C);
-        tma_prefetch_l2_3d(&mq, 0, hk, t0);
-        tma_prefetch_l2_3d(&mq, 64, hk, t0);
-        tma_prefetch_l2_3d(&mk, 0, hk, t0);
-        tma_prefetch_l2_3d(&mk, 64, hk, t0);
-        bulk_prefetch_l2(rec + REC_W, 16384 + 8192);
-        bulk_prefetch_l2(rec + REC_U + vt * 4096, 4096);
-        bulk_prefetch_l2(rec + REC_VEC, 1024);
-    };
 
     if (tid == 0) {
         prefetch_tensormap(&mq);
@@ -558,97 +536,84 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
         tmem_alloc(slot, 256);
         tmem_relinquish();
     }
-    if (tid == COPIER) {
-        for (int cc = 0; cc < NS && cc < nc; ++cc) issue_stage(cc);
-        for (int cc = NS; cc < NS + 2 && cc < nc; ++cc) prefetch_chunk(cc);
-    }
-
-    // state tile: thread j holds S[i0 + i][j], i < 32 (row j of S^T)
-    const int j = tid;
-    float S[DVT];
-    {
-        const float *s0 = initial_state_ptr(p.s0, p.s0_idx, p.n_s0, b, h, Hv, D, D, p.err);
-#pragma unroll
-        for (int i = 0; i < DVT; ++i) S[i] = s0 ? s0[(size_t)(i0 + i) * D + j] : 0.f;
-#pragma unroll
-        for (int q8 = 0; q8 < DVT / 8; ++q8)
-            *reinterpret_cast<uint4 *>(sS + sw128_chunk(j, q8)) = pack8<E>(S + 8 * q8);
-    }
-    fence_proxy_async();
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    const uint32_t tbase = *slot;
-    const uint32_t lane_base = tbase + ((uint32_t)(32 * warp) << 16);
     const bool kbf = Elem<E>::kBf16;
-    const uint32_t id1 = idesc_f16(128, DVT, false, true, kbf);
-    const uint32_t id2 = idesc_f16(128, DVT, true, true, kbf);
-    const uint32_t id3 = idesc_f16(128, DVT, false, true, kbf);
-    E *ob = reinterpret_cast<E *>(p.out);
+    // TMEM columns: D1 = [Q; W] S^T at 0 / 32 (double-buffered), D2 = K^T w Delta
+    // at 64, D3 = P' Delta at 96 / 128 (double-buffered)
     bool ok = true;
-    // loop-invariant operand descriptors
-    const uint64_t bS0 = desc_sw128(smem_u32(sS), 8192, 1024);
-    const uint64_t bDw0 = desc_sw128(smem_u32(sDw), 8192, 1024);
-    const uint64_t bDd0 = desc_sw128(smem_u32(sDd), 8192, 1024);
 
-    // D1 = [Q; W] S^T for chunk cc, double-buffered in TMEM columns [0,32) / [32,64)
-    auto issue_mma1 = [&](int cc) -> bool {
-        const int s = cc % NS;
-        if (!mbar_wait(&full[s], (cc / NS) & 1, kWaitNs)) return false;
+    if (warp == kIssuerWarp) {
+        // ======================= issuer warp ============================
+        auto issue_stage = [&](int cc) {
+            const int s = cc % NS;
+            uint8_t *st = sm + s * ST_BYTES;
+            const uint8_t *rec = rec0 + (size_t)cc * rec_stride;
+            const int t0 = (int)(rtok0 + (long)cc * C);
+            mbar_arrive_expect_tx(&full[s], STAGE_TX);
+            tma_load_3d(st + ST_A1, &mq, 0, hk, t0, &full[s]);
+            tma_load_3d(st + ST_A1 + 16384, &mq, 64, hk, t0, &full[s]);
+            bulk_load(st + ST_A1 + 8192, rec + REC_W, 8192, &full[s]);
+            bulk_load(st + ST_A1 + 24576, rec + REC_W + 8192, 8192, &full[s]);
+            tma_load_3d(st + ST_K, &mk, 0, hk, t0, &full[s]);
+            tma_load_3d(st + ST_K + 8192, &mk, 64, hk, t0, &full[s]);
+            bulk_load(st + ST_P, rec + REC_P, 8192, &full[s]);
+            bulk_load(st + ST_U, rec + REC_U + vt * 4096, 4096, &full[s]);
+            bulk_load(st + ST_VEC, rec + REC_VEC, 1024, &full[s]);
+        };
+        auto prefetch_chunk = [&](int cc) {
+            const uint8_t *rec = rec0 + (size_t)cc * rec_stride;
+            const int t0 = (int)(rtok0 + (long)cc * C);
+            tma_prefetch_l2_3d(&mq, 0, hk, t0);
+            tma_prefetch_l2_3d(&mq, 64, hk, t0);
+            tma_prefetch_l2_3d(&mk, 0, hk, t0);
+            tma_prefetch_l2_3d(&mk, 64, hk, t0);
+            bulk_prefetch_l2(rec + REC_W, 16384 + 8192);
+            bulk_prefetch_l2(rec + REC_U + vt * 4096, 4096);
+            bulk_prefetch_l2(rec + REC_VEC, 1024);
+        };
+        if (lane == 0) {
+            for (int cc = 0; cc < NS && cc < nc; ++cc) issue_stage(cc);
+            for (int cc = NS; cc < NS + 2 && cc < nc; ++cc) prefetch_chunk(cc);
+        }
+        fence_before_sync();
+        named_bar(kBarState, kCarryThreads);  // initial S image written
         fence_after_sync();
-        const uint64_t a0 = desc_sw128(smem_u32(sm + s * ST_BYTES + ST_A1), 16, 1024);
-        const uint32_t d1 = (cc & 1) ? 32u : 0u;
+        const uint32_t tbase = *slot;
+        const uint32_t id1 = idesc_f16(128, DVT, false, true, kbf);
+        const uint32_t id2 = idesc_f16(128, DVT, true, true, kbf);
+        const uint32_t id3 = idesc_f16(128, DVT, false, true, kbf);
+        const uint64_t bS0 = desc_sw128(smem_u32(sS), 8192, 1024);
+        const uint64_t bDw0 = desc_sw128(smem_u32(sDw), 8192, 1024);
+        const uint64_t bDd0 = desc_sw128(smem_u32(sDd), 8192, 1024);
+        for (int cc = 0; cc < nc; ++cc) {
+            const int s = cc % NS;
+            uint8_t *st = sm + s * ST_BYTES;
+            if (lane == 0) {
+                ok = mbar_wait(&full[s], (cc / NS) & 1, kWaitNs);
+                if (ok) {
+                    // D1 = [Q; W] S^T
+                    const uint64_t a0 = desc_sw128(smem_u32(st + ST_A1), 16, 1024);
+                    const uint32_t d1 = (cc & 1) ? 32u : 0u;
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-            mma_f16(tbase + d1, desc_add(a0, (k >> 2) * 16384 + (k & 3) * 32), desc_add(bS0, k * 2048), id1,
-                    k > 0);
-        mma_commit(bar1);
-        return true;
-    };
-    if (tid == ISSUER && nc > 0) issue_mma1(0);  // a timeout here surfaces as one on bar1
-
-    for (int cc = 0; cc < nc && ok; ++cc) {
-        const int s = cc % NS;
-        uint8_t *st = sm + s * ST_BYTES;
-        const uint32_t d1 = (cc & 1) ? 32u : 0u;        // D1 = [Q; W] S^T (double-buffered)
-        const uint32_t d3 = (cc & 1) ? 128u : 96u;      // D3 = P' Delta   (double-buffered)
-        const int n = min(C, len - cc * C);
-        ok = mbar_wait(&full[s], (cc / NS) & 1, kWaitNs);
-        if (!ok) break;
-        // everything this chunk needs from the stage's vectors is read now:
-        // the stage is refilled right after the block barrier below
-        const float *vec = reinterpret_cast<const float *>(st + ST_VEC);
-        const float gC = vec[128];
-        const float gt = (warp < 2) ? vec[tid] : 0.f;
-        if (warp >= 2) {
-            // Delta = U - W S^T for token t = tid - 64
-            const int t = tid - 64;
-            const float wt = vec[64 + t];
-            ok = mbar_wait(bar1, cc & 1, kWaitNs);
-            if (!ok) break;
-            fence_after_sync();
-            float ws[32];
-            tmem_ld32(lane_base + d1, ws);
-            const uint8_t *su = st + ST_U;
-#pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8) {
-                float u[8], dd[8], dw[8];
-                unpack8<E>(*reinterpret_cast<const uint4 *>(su + u32_chunk(t, q8)), u);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    dd[e] = u[e] - ws[8 * q8 + e];
-                    dw[e] = wt * dd[e];
+                    for (int k = 0; k < 8; ++k)
+                        mma_f16(tbase + d1, desc_add(a0, (k >> 2) * 16384 + (k & 3) * 32), desc_add(bS0, k * 2048),
+                                id1, k > 0);
+                    mma_commit(bar1);
                 }
-                *reinterpret_cast<uint4 *>(sDd + sw128_chunk(t, q8)) = pack8<E>(dd);
-                *reinterpret_cast<uint4 *>(sDw + sw128_chunk(t, q8)) = pack8<E>(dw);
+                // the previous chunk's stage is free once its output MMA is done
+                if (ok && cc >= 1) {
+                    ok = mbar_wait(bar3, (cc - 1) & 1, kWaitNs);
+                    if (ok && cc - 1 + NS < nc) issue_stage(cc - 1 + NS);
+                    if (ok && cc - 1 + NS + 2 < nc) prefetch_chunk(cc - 1 + NS + 2);
+                }
             }
-            fence_proxy_async();
+            ok = __shfl_sync(0xffffffffu, ok, 0);
             fence_before_sync();
-            named_bar(1, 64);
-            if (tid == ISSUER) {
-                fence_after_sync();
+            named_bar(kBarDelta, kCarryThreads);  // Delta images written
+            fence_after_sync();
+            if (lane == 0 && ok) {
                 const uint64_t k0 = desc_sw128(smem_u32(st + ST_K), 8192, 1024);
                 const uint64_t p0 = desc_sw128(smem_u32(st + ST_P), 16, 1024);
+                const uint32_t d3 = (cc & 1) ? 128u : 96u;
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     mma_f16(tbase + 64, desc_add(k0, k * 2048), desc_add(bDw0, k * 2048), id2, k > 0);
@@ -658,72 +623,124 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
                     mma_f16(tbase + d3, desc_add(p0, k * 32), desc_add(bDd0, k * 2048), id3, k > 0);
                 mma_commit(bar3);
             }
+            fence_before_sync();
+            named_bar(kBarState, kCarryThreads);  // S image written
+            fence_after_sync();
         }
-        // S <- gamma_last S + K^T diag(w) Delta   (TMEM lane j = dk index)
-        ok = mbar_wait(bar2, cc & 1, kWaitNs);
-        if (!ok) break;
-        fence_after_sync();
-        {
-            float v[32];
-            tmem_ld32(lane_base + 64, v);
-#pragma unroll
-            for (int i = 0; i < DVT; ++i) S[i] = fmaf(gC, S[i], v[i]);
+        if (lane == 0 && nc > 0) {
+            // drain: the last output MMA and any copy still in flight
+            mbar_wait(bar3, (nc - 1) & 1, kWaitNs);
         }
+    } else {
+        // ======================= compute warps ==========================
+        // state tile: thread (quarter, lane) owns dk row j = 32 * quarter + lane of
+        // S^T for the 16 columns [16 * half, 16 * half + 16) of the tile
+        const int j = 32 * quarter + lane;
+        const int c0 = 16 * half;
+        float S[16];
+        const float *s0 = initial_state_ptr(p.s0, p.s0_idx, p.n_s0, b, h, Hv, D, D, p.err);
 #pragma unroll
-        for (int q8 = 0; q8 < DVT / 8; ++q8)
-            *reinterpret_cast<uint4 *>(sS + sw128_chunk(j, q8)) = pack8<E>(S + 8 * q8);
+        for (int i = 0; i < 16; ++i) S[i] = s0 ? s0[(size_t)(i0 + c0 + i) * D + j] : 0.f;
+#pragma unroll
+        for (int q8 = 0; q8 < 2; ++q8)
+            *reinterpret_cast<uint4 *>(sS + sw128_chunk(j, 2 * half + q8)) = pack8<E>(S + 8 * q8);
         fence_proxy_async();
-        if (warp < 2) {
-            // the output MMA of this chunk must be done before the barrier: after
-            // it the stage is refilled and the next chunk's MMAs may start
-            ok = mbar_wait(bar3, cc & 1, kWaitNs);
-            if (!ok) break;
-        }
         fence_before_sync();
-        __syncthreads();
-        if (tid == ISSUER) {
-            fence_after_sync();
-            if (cc + 1 < nc) issue_mma1(cc + 1);
-        }
-        if (tid == COPIER) {
-            // the stage of this chunk is free: its MMAs completed (bar2, bar3)
-            if (cc + NS < nc) issue_stage(cc + NS);
-            if (cc + NS + 2 < nc) prefetch_chunk(cc + NS + 2);
-        }
-        if (warp < 2) {
-            // O = gamma_t (Q S^T) + P' Delta for token t = tid
-            const int t = tid;
-            fence_after_sync();
-            float qs[32], pd[32];
-            tmem_ld32(lane_base + d1, qs);
-            tmem_ld32(lane_base + d3, pd);
-            if (t < n) {
-                E *dst = ob + ((rtok0 + (long)cc * C + t) * Hv + h) * (long)D + i0;
+        named_bar(kBarState, kCarryThreads);
+        fence_after_sync();
+        const uint32_t tbase = *slot;
+        const uint32_t lane_base = tbase + ((uint32_t)(32 * quarter) << 16);
+        E *ob = reinterpret_cast<E *>(p.out);
+
+        for (int cc = 0; cc < nc; ++cc) {
+            const int s = cc % NS;
+            uint8_t *st = sm + s * ST_BYTES;
+            const uint32_t d1 = (cc & 1) ? 32u : 0u;
+            const uint32_t d3 = (cc & 1) ? 128u : 96u;
+            const int n = min(C, len - cc * C);
+            if (ok) ok = mbar_wait(&full[s], (cc / NS) & 1, kWaitNs);
+            const float *vec = reinterpret_cast<const float *>(st + ST_VEC);
+            const float gC = ok ? vec[128] : 0.f;
+            if (quarter >= 2) {
+                // Delta = U - W S^T for token t, 16 of the 32 columns
+                const int t = 32 * (quarter - 2) + lane;
+                const float wt = ok ? vec[64 + t] : 0.f;
+                if (ok) ok = mbar_wait(bar1, cc & 1, kWaitNs);
+                if (ok) {
+                    fence_after_sync();
+                    float ws[16];
+                    tmem_ld16(lane_base + d1 + c0, ws);
+                    const uint8_t *su = st + ST_U;
 #pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8) {
-                    float o[8];
+                    for (int q8 = 0; q8 < 2; ++q8) {
+                        float u[8], dd[8], dw[8];
+                        unpack8<E>(*reinterpret_cast<const uint4 *>(su + u32_chunk(t, 2 * half + q8)), u);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) o[e] = fmaf(gt, qs[8 * q8 + e], pd[8 * q8 + e]);
-                    *reinterpret_cast<uint4 *>(dst + 8 * q8) = pack8<E>(o);
+                        for (int e = 0; e < 8; ++e) {
+                            dd[e] = u[e] - ws[8 * q8 + e];
+                            dw[e] = wt * dd[e];
+                        }
+                        *reinterpret_cast<uint4 *>(sDd + sw128_chunk(t, 2 * half + q8)) = pack8<E>(dd);
+                        *reinterpret_cast<uint4 *>(sDw + sw128_chunk(t, 2 * half + q8)) = pack8<E>(dw);
+                    }
+                    fence_proxy_async();
                 }
             }
+            const float gt = (quarter < 2 && ok) ? vec[32 * quarter + lane] : 0.f;
             fence_before_sync();
+            named_bar(kBarDelta, kCarryThreads);
+            fence_after_sync();
+            // S <- gamma_last S + K^T diag(w) Delta   (TMEM lane j = dk index)
+            if (ok) ok = mbar_wait(bar2, cc & 1, kWaitNs);
+            if (ok) {
+                fence_after_sync();
+                float v[16];
+                tmem_ld16(lane_base + 64 + c0, v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) S[i] = fmaf(gC, S[i], v[i]);
+#pragma unroll
+                for (int q8 = 0; q8 < 2; ++q8)
+                    *reinterpret_cast<uint4 *>(sS + sw128_chunk(j, 2 * half + q8)) = pack8<E>(S + 8 * q8);
+                fence_proxy_async();
+            }
+            fence_before_sync();
+            named_bar(kBarState, kCarryThreads);
+            fence_after_sync();
+            if (quarter < 2 && ok) {
+                // O = gamma_t (Q S^T) + P' Delta for token t, 16 columns
+                const int t = 32 * quarter + lane;
+                ok = mbar_wait(bar3, cc & 1, kWaitNs);
+                if (ok) {
+                    fence_after_sync();
+                    float qs[16], pd[16];
+                    tmem_ld16(lane_base + d1 + c0, qs);
+                    tmem_ld16(lane_base + d3 + c0, pd);
+                    if (t < n) {
+                        E *dst = ob + ((rtok0 + (long)cc * C + t) * Hv + h) * (long)D + i0 + c0;
+#pragma unroll
+                        for (int q8 = 0; q8 < 2; ++q8) {
+                            float o[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) o[e] = fmaf(gt, qs[8 * q8 + e], pd[8 * q8 + e]);
+                            *reinterpret_cast<uint4 *>(dst + 8 * q8) = pack8<E>(o);
+                        }
+                    }
+                }
+            }
+        }
+        if (ok && p.s_final != nullptr) {
+            float *sf = p.s_final + (((size_t)b * Hv + h) * D + i0 + c0) * D;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sf[(size_t)i * D + j] = S[i];
         }
     }
-
-    if (ok && p.s_final != nullptr) {
-        float *sf = p.s_final + (((size_t)b * Hv + h) * D + i0) * D;
-#pragma unroll
-        for (int i = 0; i < DVT; ++i) sf[(size_t)i * D + j] = S[i];
-    }
-    if (!ok) {
-        atomicOr(p.err, (uint32_t)GDN_DEVERR_TIMEOUT);
-        // let every copy this CTA issued land before its shared memory is released
-        for (int s = 0; s < NS; ++s) mbar_wait(&full[s], 0, kWaitNs / 8);
-    }
+    if (!ok && tid == 0) atomicOr(p.err, (uint32_t)GDN_DEVERR_TIMEOUT);
     fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, 256);
+    if (!ok && tid == 0)
+        for (int s = 0; s < NS; ++s) mbar_wait(&full[s], 0, kWaitNs / 8);  // copies must land first
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(*slot, 256);
 }
 
 // ============================================================== host =====
@@ -784,7 +801,7 @@ cudaError_t launch_e(const PrefillParams &p, long total_T, long max_chunks, cuda
         if (e != cudaSuccess) return e;
     }
     dim3 gb(D / DVT, p.Hv, p.B);
-    prefill_carry_kernel<E><<<gb, 128, B_SMEM, stream>>>(p, mq, mk);
+    prefill_carry_kernel<E><<<gb, kCarryThreads, B_SMEM, stream>>>(p, mq, mk);
     return cudaGetLastError();
 }
 
