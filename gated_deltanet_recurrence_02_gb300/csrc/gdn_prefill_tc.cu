@@ -489,10 +489,14 @@ constexpr uint32_t B_BAR = B_DD + 8192;
 constexpr uint32_t B_SMEM = B_BAR + 128 + 1024;
 constexpr uint32_t STAGE_TX = 16384 + 16384 + 16384 + 8192 + 4096 + 1024;
 // 8 compute warps: warp w reads TMEM lane quarter w % 4, warps w and w + 4
-// split the tile's 32 columns.  Warp 8 issues every MMA and copy.
+// split the tile's 32 columns.  Warp 8 issues every MMA; warp 9 refills the
+// stage ring, each stage once the output MMA of its chunk has retired (that
+// MMA's commit arrives on the stage's `empty` barrier).
 constexpr int kCarryComputeWarps = 8;
-constexpr int kCarryThreads = (kCarryComputeWarps + 1) * 32;
-constexpr int kIssuerWarp = kCarryComputeWarps;
+constexpr int kIssuerWarp = kCarryComputeWarps;          // issues every MMA
+constexpr int kCopierWarp = kCarryComputeWarps + 1;      // issues every copy; no named barriers
+constexpr int kCarryThreads = (kCarryComputeWarps + 2) * 32;
+constexpr int kBarThreads = (kCarryComputeWarps + 1) * 32;  // compute warps + issuer
 constexpr uint32_t kBarDelta = 1;  // named barrier: Delta images written (all warps)
 constexpr uint32_t kBarState = 2;  // named barrier: S image written (all warps)
 
@@ -504,8 +508,9 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sS = sm + B_S, *sDw = sm + B_DW, *sDd = sm + B_DD;
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + B_BAR);  // [NS]
-    uint64_t *bar1 = full + NS, *bar2 = full + NS + 1, *bar3 = full + NS + 2;
-    uint32_t *slot = reinterpret_cast<uint32_t *>(full + NS + 3);
+    uint64_t *empty = full + NS;                                  // [NS]
+    uint64_t *bar1 = full + 2 * NS, *bar2 = bar1 + 1, *bar3 = bar1 + 2;
+    uint32_t *slot = reinterpret_cast<uint32_t *>(bar1 + 3);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = (warp >> 2) & 1;
@@ -525,7 +530,10 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     if (tid == 0) {
         prefetch_tensormap(&mq);
         prefetch_tensormap(&mk);
-        for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
         mbar_init(bar1, 1);
         mbar_init(bar2, 1);
         mbar_init(bar3, 1);
@@ -541,8 +549,8 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     // at 64, D3 = P' Delta at 96 / 128 (double-buffered)
     bool ok = true;
 
-    if (warp == kIssuerWarp) {
-        // ======================= issuer warp ============================
+    if (warp == kCopierWarp) {
+        // ======================= copier warp ============================
         auto issue_stage = [&](int cc) {
             const int s = cc % NS;
             uint8_t *st = sm + s * ST_BYTES;
@@ -573,9 +581,20 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
         if (lane == 0) {
             for (int cc = 0; cc < NS && cc < nc; ++cc) issue_stage(cc);
             for (int cc = NS; cc < NS + 2 && cc < nc; ++cc) prefetch_chunk(cc);
+            for (int cc = NS; cc < nc; ++cc) {
+                // chunk cc reuses the stage of chunk cc - NS
+                if (!mbar_wait(&empty[cc % NS], (cc / NS - 1) & 1, kWaitNs)) {
+                    ok = false;
+                    break;
+                }
+                issue_stage(cc);
+                if (cc + 2 < nc) prefetch_chunk(cc + 2);
+            }
         }
+    } else if (warp == kIssuerWarp) {
+        // ======================= issuer warp ============================
         fence_before_sync();
-        named_bar(kBarState, kCarryThreads);  // initial S image written
+        named_bar(kBarState, kBarThreads);  // initial S image written
         fence_after_sync();
         const uint32_t tbase = *slot;
         const uint32_t id1 = idesc_f16(128, DVT, false, true, kbf);
@@ -599,16 +618,10 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
                                 id1, k > 0);
                     mma_commit(bar1);
                 }
-                // the previous chunk's stage is free once its output MMA is done
-                if (ok && cc >= 1) {
-                    ok = mbar_wait(bar3, (cc - 1) & 1, kWaitNs);
-                    if (ok && cc - 1 + NS < nc) issue_stage(cc - 1 + NS);
-                    if (ok && cc - 1 + NS + 2 < nc) prefetch_chunk(cc - 1 + NS + 2);
-                }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             fence_before_sync();
-            named_bar(kBarDelta, kCarryThreads);  // Delta images written
+            named_bar(kBarDelta, kBarThreads);  // Delta images written
             fence_after_sync();
             if (lane == 0 && ok) {
                 const uint64_t k0 = desc_sw128(smem_u32(st + ST_K), 8192, 1024);
@@ -622,9 +635,10 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
                 for (int k = 0; k < 4; ++k)
                     mma_f16(tbase + d3, desc_add(p0, k * 32), desc_add(bDd0, k * 2048), id3, k > 0);
                 mma_commit(bar3);
+                mma_commit(&empty[s]);  // every MMA reading this chunk's stage has retired
             }
             fence_before_sync();
-            named_bar(kBarState, kCarryThreads);  // S image written
+            named_bar(kBarState, kBarThreads);  // S image written
             fence_after_sync();
         }
         if (lane == 0 && nc > 0) {
@@ -646,7 +660,7 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
             *reinterpret_cast<uint4 *>(sS + sw128_chunk(j, 2 * half + q8)) = pack8<E>(S + 8 * q8);
         fence_proxy_async();
         fence_before_sync();
-        named_bar(kBarState, kCarryThreads);
+        named_bar(kBarState, kBarThreads);
         fence_after_sync();
         const uint32_t tbase = *slot;
         const uint32_t lane_base = tbase + ((uint32_t)(32 * quarter) << 16);
@@ -688,7 +702,7 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
             }
             const float gt = (quarter < 2 && ok) ? vec[32 * quarter + lane] : 0.f;
             fence_before_sync();
-            named_bar(kBarDelta, kCarryThreads);
+            named_bar(kBarDelta, kBarThreads);
             fence_after_sync();
             // S <- gamma_last S + K^T diag(w) Delta   (TMEM lane j = dk index)
             if (ok) ok = mbar_wait(bar2, cc & 1, kWaitNs);
@@ -704,7 +718,7 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
                 fence_proxy_async();
             }
             fence_before_sync();
-            named_bar(kBarState, kCarryThreads);
+            named_bar(kBarState, kBarThreads);
             fence_after_sync();
             if (quarter < 2 && ok) {
                 // O = gamma_t (Q S^T) + P' Delta for token t, 16 columns
