@@ -210,6 +210,36 @@ def replay(state_in, state_update, accepted_count, *, B, Hk, Hv, dk, dv,
     return S
 
 
+def replay_verify(q, k, v, alpha, beta, *, B, Hk, Hv, dk, dv, T=None,
+                  cu_seqlens=None, state_in=None, prev_state_update=None,
+                  prev_capacity=0, accepted_count=None, scale=1.0, capacity=0,
+                  capture_count=None, active=True, state_update=None,
+                  units=None, threads=None):
+    """One speculative-decoding step: replay the accepted prefix of the
+    previous capture, then run the draft tokens with capture ("[WebGPU EP]
+    adds state update capacity support for GatedDeltaNet", onnxruntime PR
+    32767, "DFlash2 Prerequisite": replay after partial acceptance, state and
+    output matching the non-speculative run).  Written as what it is, the
+    replay of ``replay`` followed by the recurrence of ``recurrent``.
+
+    Returns (o, committed_state, draft_final_state, state_update)."""
+    if state_in is None:
+        S = np.zeros((B, Hv, dv, dk))
+    else:
+        S = f64(state_in).copy()
+    if prev_capacity > 0:
+        S = replay(S, prev_state_update, accepted_count, B=B, Hk=Hk, Hv=Hv,
+                   dk=dk, dv=dv, capacity=prev_capacity, units=units,
+                   threads=threads)
+    o, S_final, su = recurrent(q, k, v, alpha, beta, B=B, Hk=Hk, Hv=Hv, dk=dk,
+                               dv=dv, T=T, cu_seqlens=cu_seqlens,
+                               initial_state=S, scale=scale, capacity=capacity,
+                               capture_count=capture_count, active=active,
+                               state_update=state_update, units=units,
+                               threads=threads)
+    return o, S, S_final, su
+
+
 def _gather_states(initial_state, indices, B, Hv, dv, dk):
     if initial_state is None:
         return np.zeros((B, Hv, dv, dk))

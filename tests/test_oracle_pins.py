@@ -228,3 +228,47 @@ def test_capture_clamp_prefix_and_inactive(oracle_mod):
                                        state_update=sentinel.copy(), **dims)
     assert np.all(su0 == 0.0)
     assert np.array_equal(o2, o) and np.array_equal(S2, S)
+
+
+# --- speculative loop (replay + verify) -----------------------------------
+
+@pytest.mark.parametrize("accepted", [[0, 0], [2, 4], [4, 4], [4, 1]])
+def test_speculative_loop_matches_non_speculative_run(oracle_mod, accepted):
+    """"DFlash2 Prerequisite" (onnxruntime PR 32767): with full, partial and
+    zero acceptance, verify-with-capture then replay-and-verify must give the
+    output and state of running the accepted tokens and the next drafts
+    straight through the recurrence.  Two rows with different acceptance;
+    ragged second drafts (one row has none)."""
+    rng = np.random.default_rng(60)
+    B, Hk, Hv, dk, dv, T1 = 2, 1, 2, 5, 4, 4
+    lens2 = [3, 0]
+    q, k, v, a, b, _ = _rand_case(rng, B * T1 + sum(lens2), Hk, Hv, dk, dv)
+    S0 = 0.3 * rng.standard_normal((B, Hv, dv, dk))
+    dims = dict(B=B, Hk=Hk, Hv=Hv, dk=dk, dv=dv)
+    X = slice(0, B * T1)
+    Y = slice(B * T1, None)
+    # verify pass 1: T1 drafts per row, all captured
+    _, _, su1 = oracle_mod.recurrent(q[X], k[X], v[X], a[X], b[X], T=T1,
+                                     initial_state=S0, capacity=T1,
+                                     capture_count=[T1] * B, **dims)
+    cu2 = np.concatenate([[0], np.cumsum(lens2)])
+    o2, S_commit, S_draft, su2 = oracle_mod.replay_verify(
+        q[Y], k[Y], v[Y], a[Y], b[Y], cu_seqlens=cu2, state_in=S0,
+        prev_state_update=su1, prev_capacity=T1, accepted_count=accepted,
+        capacity=4, capture_count=[4, 4], **dims)
+    for r in range(B):
+        m = accepted[r]
+        # non-speculative: accepted tokens then the new drafts, one row
+        toks = list(range(r * T1, r * T1 + m)) + [B * T1 + cu2[r] + i for i in range(lens2[r])]
+        one = dict(B=1, Hk=Hk, Hv=Hv, dk=dk, dv=dv)
+        _, S_m, _ = oracle_mod.recurrent(q[toks[:m]], k[toks[:m]], v[toks[:m]],
+                                         a[toks[:m]], b[toks[:m]], T=m,
+                                         initial_state=S0[r:r + 1], **one)
+        o_ns, S_ns, _ = oracle_mod.recurrent(q[toks], k[toks], v[toks], a[toks],
+                                             b[toks], T=len(toks),
+                                             initial_state=S0[r:r + 1], **one)
+        assert _rel(S_commit[r], S_m[0]) < 1e-13
+        assert _rel(S_draft[r], S_ns[0]) < 1e-13
+        if lens2[r]:
+            got = o2[cu2[r]:cu2[r + 1]]
+            assert _rel(got, o_ns[m:]) < 1e-13
