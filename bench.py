@@ -8,11 +8,17 @@ One step is one pass of the whole path over one batch of synthetic input:
                          heads, bf16 q/k/v/alpha/beta, the fp32 state updated
                          in place in HBM, capacity 4, capture_count ~ U{0..4};
   3. replay              the decode state, capacity 4, accepted ~ U{0..4},
-                         written to a separate output state.
+                         written to a separate output state;
+  4. speculative step    B=256: one fused replay + verify launch -- replay of
+                         the accepted prefix (U{0..4}) of a 4-slot capture,
+                         then 4 draft tokens per row with capture, the
+                         committed state in place.
 The headline `value` is the decode phase's state throughput (algorithmic
 bytes moved per second: state read + write, token vectors, outputs and
-captured factors).  Prefill tokens/s and replay GB/s ride along in
-"prefill" / "replay".  Inputs are resident in HBM before the timed region;
+captured factors).  Prefill tokens/s, replay GB/s and the speculative
+step's GB/s ride along in "prefill" / "replay" / "replay_verify"; the last
+also reports the same step done unfused (replay, then verify) for
+comparison, timed outside the step.  Inputs are resident in HBM before the timed region;
 the decode state (512 MiB) is larger than L2, and the L2 is flushed (a
 256 MiB write) before every prefill, outside the phase timers.
 
@@ -42,6 +48,7 @@ METRIC = "GDN prefill tokens/s & decode state GB/s on 1 GB300, % of roofline"
 DEC = dict(B=256, steps=64, Hk=16, Hv=32, dk=128, dv=128, cap=4, seed=1004)
 PRE = dict(T=4100, Hk=16, Hv=32, dk=128, dv=128, chunk=64, seed=1002)
 REP_SEED = 2004
+VER = dict(B=256, T=4, cap=4, seed=1005)  # speculative step: 4 drafts, capacity 4
 CPU_SAMPLE_ROWS = 128  # oracle sample: 128 rows x 32 heads x 64 tokens
 
 
@@ -154,6 +161,21 @@ def replay_bytes(accepted, d=DEC) -> int:
     return 2 * B * Hv * dv * dk * 4 + sum(min(max(int(a), 0), d["cap"]) for a in accepted) * slot + B * 4
 
 
+def verify_bytes(accepted, B, d=DEC, v=VER) -> int:
+    """Algorithmic bytes of ONE fused replay + verify call, state in place:
+    the state read for every row and written for rows that replay (m_b >= 1;
+    rows with m_b = 0 are left in place), the replayed slots read, the draft
+    tokens' bf16 q, k, v, alpha, beta read and o written, every draft
+    captured (fp32 slots written), int32 counts read."""
+    Hk, Hv, dk, dv, T, cap = d["Hk"], d["Hv"], d["dk"], d["dv"], v["T"], v["cap"]
+    st = Hv * dv * dk * 4
+    slot = (Hv + Hk * dk + Hv * dv) * 4
+    m = [min(max(int(a), 0), cap) for a in accepted]
+    state = B * st + sum(1 for x in m if x > 0) * st
+    tokens = B * T * ((2 * Hk * dk + 2 * Hv * dv + 2 * Hv) * 2)
+    return state + sum(m) * slot + B * min(cap, T) * slot + 2 * B * 4 + tokens
+
+
 def prefill_bytes_flops(p=PRE):
     """Minimum HBM bytes and the chunked form's flops of one prefill call."""
     T, Hk, Hv, dk, dv, C = p["T"], p["Hk"], p["Hv"], p["dk"], p["dv"], p["chunk"]
@@ -178,14 +200,15 @@ def load_peaks():
 def run_ours(args, rank, world, local_rank):
     import torch
     from gated_deltanet_recurrence_02_gb300 import gdn
-    from gated_deltanet_recurrence_02_gb300.inputs import capture_counts, make_inputs
+    from gated_deltanet_recurrence_02_gb300.inputs import accepted_counts, capture_counts, make_inputs
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     gdn.lib()
     stream = torch.cuda.current_stream()
     d = dict(DEC, B=args.decode_rows)
-    do_pre, do_dec, do_rep = (args.only in ("all", ph) for ph in ("prefill", "decode", "replay"))
+    do_pre, do_dec, do_rep, do_ver = (args.only in ("all", ph)
+                                      for ph in ("prefill", "decode", "replay", "verify"))
     B, S_, Hk, Hv, dk, dv, cap = d["B"], d["steps"], d["Hk"], d["Hv"], d["dk"], d["dv"], d["cap"]
 
     # ---- decode inputs (step-major on the device) ----
@@ -217,6 +240,34 @@ def run_ours(args, rank, world, local_rank):
     acc_d = accepted.to(dev)
     S_rep = torch.empty_like(S)
 
+    # ---- speculative step inputs: a 4-draft capture to replay (made here,
+    # outside the timed region), accepted ~ U{0..4}, 4 new drafts per row
+    vt, vcap = VER["T"], VER["cap"]
+    xv1 = make_inputs(VER["seed"] + 100 * rank, lengths=[vt] * B, Hk=Hk, Hv=Hv, dk=dk, dv=dv,
+                      dtype_qkv="bf16", dtype_gate="bf16")
+    xv2 = make_inputs(VER["seed"] + 1 + 100 * rank, lengths=[vt] * B, Hk=Hk, Hv=Hv, dk=dk,
+                      dv=dv, dtype_qkv="bf16", dtype_gate="bf16", zero_state=True)
+    gv1 = {n: getattr(xv1, n).to(dev) for n in ("q", "k", "v", "alpha", "beta")}
+    gv = {n: getattr(xv2, n).to(dev) for n in ("q", "k", "v", "alpha", "beta")}
+    S_ver = xv1.initial_state.to(dev)
+    v_full = torch.full((B,), vcap, dtype=torch.int32, device=dev)
+    su_prev = torch.empty((B, vcap, slot), dtype=torch.float32, device=dev)
+    gdn.gdn_recurrent_capture(gv1["q"], gv1["k"], gv1["v"], gv1["alpha"], gv1["beta"], B=B, T=vt,
+                              initial_state=S_ver, state_update_capacity=vcap,
+                              capture_count=v_full, state_update=su_prev, want_final_state=False)
+    v_acc = accepted_counts(VER["seed"] + 2 + 100 * rank, B, vcap)
+    v_acc_d = v_acc.to(dev)
+    v_out = torch.empty_like(gv["v"])
+    su_new = torch.empty_like(su_prev)
+    del xv1, gv1
+
+    def verify():
+        gdn.gdn_replay_verify(gv["q"], gv["k"], gv["v"], gv["alpha"], gv["beta"], B=B, T=vt,
+                              state_in=S_ver, state_out=S_ver, prev_state_update=su_prev,
+                              prev_capacity=vcap, accepted_count=v_acc_d, out=v_out,
+                              state_update_capacity=vcap, capture_count=v_full,
+                              state_update=su_new)
+
     # ---- prefill inputs ----
     p = PRE
     xp = make_inputs(p["seed"] + 100 * rank, lengths=[p["T"]], Hk=p["Hk"], Hv=p["Hv"],
@@ -244,7 +295,7 @@ def run_ours(args, rank, world, local_rank):
                                      state_out=S_rep)
 
     E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    n_ev = S_ + 4
+    n_ev = S_ + 5
     ev = [[E() for _ in range(n_ev)] for _ in range(args.steps)]
 
     def step(evs=None):
@@ -260,6 +311,9 @@ def run_ours(args, rank, world, local_rank):
         if do_rep:
             replay()
         if evs: evs[2 + S_].record(stream)
+        if do_ver:
+            verify()
+        if evs: evs[3 + S_].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -282,12 +336,15 @@ def run_ours(args, rank, world, local_rank):
                      for s in range(args.steps) for t in range(S_)]
     dec_ms = [ev[s][1].elapsed_time(ev[s][1 + S_]) for s in range(args.steps)]
     rep_ms = [ev[s][1 + S_].elapsed_time(ev[s][2 + S_]) for s in range(args.steps)]
+    ver_ms = [ev[s][2 + S_].elapsed_time(ev[s][3 + S_]) for s in range(args.steps)]
     assert torch.isfinite(out).all() and torch.isfinite(S).all() and torch.isfinite(p_out.float()).all()
+    assert torch.isfinite(S_ver).all() and torch.isfinite(v_out.float()).all()
 
     if args.only != "all":
         # profiling mode: one phase only, no JSON contract line
         return {"only": args.only, "decode_rows": B, "prefill_ms": statistics.mean(pre_ms),
-                "decode_ms": statistics.mean(dec_ms), "replay_ms": statistics.mean(rep_ms)}
+                "decode_ms": statistics.mean(dec_ms), "replay_ms": statistics.mean(rep_ms),
+                "verify_ms": statistics.mean(ver_ms)}
     dec_bytes_call = decode_bytes(counts.tolist(), d)
     dec_total_bytes = dec_bytes_call * S_ * args.steps
     dec_time = reduce_scalar(sum(dec_ms) / 1e3, "max", dev)
@@ -303,7 +360,10 @@ def run_ours(args, rank, world, local_rank):
     pre_tokens = reduce_scalar(p["T"] * args.steps, "sum", dev)
     rep_bytes_call = replay_bytes(accepted.tolist())
     rep_avg_s = statistics.mean(rep_ms) / 1e3
-    ms_per_step = (sum(pre_ms) + sum(dec_ms) + sum(rep_ms)) / args.steps
+    ver_bytes_call = verify_bytes(v_acc.tolist(), B, d)
+    ver_avg_s = statistics.mean(ver_ms) / 1e3
+    unfused = run_verify_unfused(gdn, stream, gv, su_prev, v_acc_d, v_full, S_ver, d)
+    ms_per_step = (sum(pre_ms) + sum(dec_ms) + sum(rep_ms) + sum(ver_ms)) / args.steps
     ms_per_step = reduce_scalar(ms_per_step, "max", dev)
 
     # ---- end to end through the public API with host buffers (decode) ----
@@ -338,7 +398,7 @@ def run_ours(args, rank, world, local_rank):
                 "parallelism": f"replicas x{world} (rows independent)",
             },
             "roofline": {
-                "kernel": "recurrent_kernel<128,bf16> (decode, T=1)",
+                "kernel": "recurrent_kernel<128, bf16, 1, 0, 4> (decode, T=1)",
                 "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
                 "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
                 "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": DECODE_TRAFFIC_BYTES,
@@ -366,18 +426,62 @@ def run_ours(args, rank, world, local_rank):
                 "frac": round(rep_bytes_call / rep_avg_s / 1e9 / hbm_peak, 4),
                 "algorithmic_bytes_per_launch": rep_bytes_call,
             },
+            "replay_verify": {
+                "workload": "verify_B256_T4: B=256, replay of accepted~U{0..4} of 4 captured "
+                            "slots, then 4 bf16 draft tokens per row with capture (capacity 4), "
+                            "state in place; one fused launch",
+                "value": round(ver_bytes_call / ver_avg_s / 1e9, 1), "unit": "GB/s",
+                "frac": round(ver_bytes_call / ver_avg_s / 1e9 / hbm_peak, 4),
+                "avg_launch_us": round(ver_avg_s * 1e6, 2),
+                "draft_tokens_per_s": round(B * VER["T"] / ver_avg_s, 1),
+                "algorithmic_bytes_per_launch": ver_bytes_call,
+                "traffic": VERIFY_TRAFFIC_BYTES,
+                "unfused_us": unfused,
+                "speedup_vs_unfused": round(unfused["total"] / (ver_avg_s * 1e6), 3),
+            },
             "e2e": e2e,
-            "gpu_launches": args.steps * (PREFILL_LAUNCHES + S_ + 1),
+            "gpu_launches": args.steps * (PREFILL_LAUNCHES + S_ + 2),
             "clocks": clocks,
             "wall_s_timed_region": round(t_wall, 4),
         }
     return line
 
 
+def run_verify_unfused(gdn, stream, gv, su_prev, acc_d, full, S_src, d, n=20, warm=3):
+    """The speculative step done as two calls -- replay in place, then the
+    drafts through gdn_recurrent_capture (no final state) -- on a copy of the
+    state, outside the step's timed region: per-call means in microseconds."""
+    import torch
+    B, vt, vcap, Hk = d["B"], VER["T"], VER["cap"], d["Hk"]
+    S = S_src.clone()
+    out = torch.empty_like(gv["v"])
+    su = torch.empty_like(su_prev)
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    ev = [[E(), E(), E()] for _ in range(n)]
+    for i in range(warm + n):
+        e = ev[i - warm] if i >= warm else None
+        if e: e[0].record(stream)
+        gdn.gdn_replay_state_updates(S, su_prev, acc_d, state_update_capacity=vcap, Hk=Hk,
+                                     state_out=S)
+        if e: e[1].record(stream)
+        gdn.gdn_recurrent_capture(gv["q"], gv["k"], gv["v"], gv["alpha"], gv["beta"], B=B, T=vt,
+                                  initial_state=S, want_final_state=False, out=out,
+                                  state_update_capacity=vcap, capture_count=full,
+                                  state_update=su)
+        if e: e[2].record(stream)
+    torch.cuda.synchronize()
+    rep = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) * 1e3
+    ver = statistics.mean(e[1].elapsed_time(e[2]) for e in ev) * 1e3
+    del S
+    return {"replay": round(rep, 2), "verify": round(ver, 2), "total": round(rep + ver, 2)}
+
+
 PREFILL_LAUNCHES = 2  # kernels one gdn_prefill_chunked call launches on this workload (tensor-core path)
-# DRAM bytes (read + write) of one decode launch at B=256, from one ncu capture of
-# the current recurrent kernel (profiles/recurrent_decode_B256_traffic.md).
-DECODE_TRAFFIC_BYTES = 541_230_000 + 485_970_000
+# DRAM bytes (read + write) of one launch, from one ncu capture of the current
+# kernels: decode at B=256 (profiles/recurrent_decode_B256_traffic.md) and the
+# fused replay + verify step (profiles/replay_verify_B256_T4.md).
+DECODE_TRAFFIC_BYTES = 541_225_984 + 483_706_880
+VERIFY_TRAFFIC_BYTES = 567_217_408 + 391_318_528
 
 
 def run_e2e(args, gdn, dev, stream, hq, hk_, hv, ha, hb, S0_host, counts, d):
@@ -557,7 +661,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "replay"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "replay", "verify"], default="all",
                     help="profiling aid: run one phase only (prints timings, not the contract line)")
     ap.add_argument("--decode-rows", type=int, default=DEC["B"],
                     help="profiling aid: rows of the decode / replay phases (default 256)")

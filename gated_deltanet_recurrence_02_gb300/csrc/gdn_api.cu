@@ -190,6 +190,75 @@ int gdn_recurrent_capture(const void *q, const void *k, const void *v, const voi
     p.scale = scale; p.dt_qkv = dtype_qkv; p.dt_gate = dtype_gate;
     p.capacity = cap; p.capture_count = capture_count; p.active = state_update_active;
     p.su = cap > 0 ? state_update : nullptr;
+    p.rp_su = nullptr; p.rp_capacity = 0; p.rp_accepted = nullptr; p.s_commit = nullptr;
+    if (error_word(&p.err) != cudaSuccess) return GDN_ERR_CUDA;
+    return launch_recurrent(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int gdn_replay_verify(const void *q, const void *k, const void *v, const void *alpha,
+                      const void *beta, const int32_t *cu_seqlens, const float *state_in,
+                      float *state_out, const float *prev_state_update, int prev_capacity,
+                      const int32_t *accepted_count, float *draft_final_state, void *out, int B,
+                      int T, int Hq, int Hk, int Hv, int dk, int dv, float scale, int dtype_qkv,
+                      int dtype_gate, int state_update_capacity, const int32_t *capture_count,
+                      const int32_t *state_update_active, float *state_update, void *stream) {
+    Shapes sh;
+    int st = check_common(q, k, v, alpha, beta, cu_seqlens, state_in, nullptr, B, draft_final_state,
+                          out, B, T, Hq, Hk, Hv, dk, dv, dtype_qkv, dtype_gate, &sh);
+    if (st != GDN_OK) return st;
+    const int cap = state_update_capacity;
+    if (cap < 0 || prev_capacity < 0) return GDN_ERR_INVALID_ARG;
+    if (cap > 0 && (capture_count == nullptr || state_update == nullptr)) return GDN_ERR_INVALID_ARG;
+    if (prev_capacity > 0 && (prev_state_update == nullptr || accepted_count == nullptr))
+        return GDN_ERR_INVALID_ARG;
+    if (B > 0 && state_out == nullptr) return GDN_ERR_INVALID_ARG;
+    if ((state_out && !aligned(state_out, 16)) || (state_update && !aligned(state_update, 16)) ||
+        (prev_state_update && !aligned(prev_state_update, 16)))
+        return GDN_ERR_ALIGN;
+    if ((capture_count && !aligned(capture_count, 4)) ||
+        (state_update_active && !aligned(state_update_active, 4)) ||
+        (accepted_count && !aligned(accepted_count, 4)))
+        return GDN_ERR_ALIGN;
+    const size_t slot_bytes = GDN_STATE_UPDATE_SLOT(Hk, Hv, dk, dv) * sizeof(float);
+    size_t su_bytes = 0, prev_bytes = 0;
+    if (cap > 0 && !mul_ok((size_t)B * cap, slot_bytes, &su_bytes)) return GDN_ERR_INVALID_ARG;
+    if (prev_capacity > 0 && !mul_ok((size_t)B * prev_capacity, slot_bytes, &prev_bytes))
+        return GDN_ERR_INVALID_ARG;
+    const size_t sbytes = (size_t)B * Hv * dv * dk * sizeof(float);
+    Span spans[] = {
+        {q, sh.qk_bytes, false},                        // 0
+        {k, sh.qk_bytes, false},                        // 1
+        {v, sh.v_bytes, false},                         // 2
+        {alpha, sh.gate_bytes, false},                  // 3
+        {beta, sh.gate_bytes, false},                   // 4
+        {cu_seqlens, cu_seqlens ? (size_t)(B + 1) * 4 : 0, false},
+        {state_in, state_in ? sbytes : 0, false},       // 6
+        {prev_state_update, prev_bytes, false},
+        {accepted_count, prev_capacity > 0 ? (size_t)B * 4 : 0, false},
+        {capture_count, cap > 0 ? (size_t)B * 4 : 0, false},
+        {state_update_active, state_update_active ? 4u : 0u, false},
+        {state_out, sbytes, true},                      // 11
+        {draft_final_state, sh.sf_bytes, true},
+        {out, sh.v_bytes, true},
+        {state_update, su_bytes, true},
+    };
+    st = check_alias(spans, (int)(sizeof(spans) / sizeof(spans[0])), 6, 11);
+    if (st != GDN_OK) return st;
+    if (B == 0) return GDN_OK;
+
+    RecurrentParams p;
+    p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.beta = beta;
+    p.cu_seqlens = cu_seqlens;
+    p.s0 = state_in; p.s0_idx = nullptr; p.n_s0 = B;
+    p.s_final = draft_final_state; p.out = out;
+    p.B = B; p.T = T; p.Hk = Hk; p.Hv = Hv; p.dk = dk; p.dv = dv;
+    p.scale = scale; p.dt_qkv = dtype_qkv; p.dt_gate = dtype_gate;
+    p.capacity = cap; p.capture_count = capture_count; p.active = state_update_active;
+    p.su = cap > 0 ? state_update : nullptr;
+    p.rp_su = prev_capacity > 0 ? prev_state_update : nullptr;
+    p.rp_capacity = prev_capacity;
+    p.rp_accepted = prev_capacity > 0 ? accepted_count : nullptr;
+    p.s_commit = state_out;
     if (error_word(&p.err) != cudaSuccess) return GDN_ERR_CUDA;
     return launch_recurrent(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

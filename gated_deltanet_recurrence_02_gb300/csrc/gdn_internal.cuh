@@ -31,6 +31,14 @@ struct RecurrentParams {
     const int32_t *capture_count;
     const int32_t *active;
     float *su;
+    // Fused replay + verify: before the tokens, replay the first
+    // clamp(rp_accepted[b], 0, rp_capacity) slots of rp_su onto the state and
+    // write the result to s_commit.  rp_capacity == 0 and s_commit == nullptr
+    // for the plain recurrent path.
+    const float *rp_su;
+    int rp_capacity;
+    const int32_t *rp_accepted;
+    float *s_commit;
     uint32_t *err;
 };
 

@@ -53,6 +53,9 @@ def lib() -> ctypes.CDLL:
     L.gdn_recurrent_capture.restype = i
     L.gdn_replay_state_updates.argtypes = [vp, vp, vp, i, vp, i, i, i, i, i, vp]
     L.gdn_replay_state_updates.restype = i
+    L.gdn_replay_verify.argtypes = ([vp] * 9 + [i] + [vp] * 3 + [i] * 7 + [f, i, i, i]
+                                    + [vp] * 4)
+    L.gdn_replay_verify.restype = i
     L.gdn_device_errors.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     L.gdn_device_errors.restype = i
     L.gdn_status_string.argtypes = [i]
@@ -177,6 +180,39 @@ def gdn_replay_state_updates(state_in, state_update, accepted_count, *,
         _p(accepted_count), B, int(Hk), Hv, dk, dv, _stream(stream))
     _check(st, "gdn_replay_state_updates")
     return state_out
+
+
+def gdn_replay_verify(q, k, v, alpha, beta, *, B: int, T: Optional[int] = None,
+                      cu_seqlens=None, state_in=None, state_out=None,
+                      prev_state_update=None, prev_capacity: int = 0,
+                      accepted_count=None, draft_final_state=None, out=None,
+                      scale: float = 1.0, state_update_capacity: int = 0,
+                      capture_count=None, state_update_active=None,
+                      state_update=None, want_draft_final_state: bool = False,
+                      stream=None):
+    """One speculative step: replay the accepted prefix of prev_state_update
+    onto state_in, write it to state_out (state_in itself allowed), then run
+    the draft tokens with capture.  Returns (out, state_out, state_update,
+    draft_final_state)."""
+    T, Hk, dk, Hv, dv = _dims(q, v, B, T, cu_seqlens)
+    if out is None:
+        out = torch.empty_like(v)
+    if state_out is None:
+        state_out = torch.empty((B, Hv, dv, dk), dtype=torch.float32, device=v.device)
+    if draft_final_state is None and want_draft_final_state:
+        draft_final_state = torch.empty((B, Hv, dv, dk), dtype=torch.float32, device=v.device)
+    cap = int(state_update_capacity)
+    if cap > 0 and state_update is None:
+        state_update = torch.empty((B, cap, slot_width(Hk, Hv, dk, dv)),
+                                   dtype=torch.float32, device=v.device)
+    st = lib().gdn_replay_verify(
+        _p(q), _p(k), _p(v), _p(alpha), _p(beta), _p(cu_seqlens), _p(state_in),
+        _p(state_out), _p(prev_state_update), int(prev_capacity), _p(accepted_count),
+        _p(draft_final_state), _p(out), B, T, Hk, Hk, Hv, dk, dv, scale,
+        _DT[q.dtype], _DT[alpha.dtype], cap, _p(capture_count),
+        _p(state_update_active), _p(state_update), _stream(stream))
+    _check(st, "gdn_replay_verify")
+    return out, state_out, state_update, draft_final_state
 
 
 def gdn_device_errors(stream=None) -> int:

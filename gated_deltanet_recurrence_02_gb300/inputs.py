@@ -103,7 +103,13 @@ def ragged_lengths(seed: int, B: int, lo: int, hi: int) -> list:
     return [int(x) for x in rng.integers(lo, hi + 1, size=B)]
 
 
-# The five workloads, by what they are.  Seeds are fixed per workload.
+def accepted_counts(seed: int, B: int, capacity: int) -> torch.Tensor:
+    """Draft tokens accepted per row ~ U{0..capacity}, int32."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return torch.from_numpy(rng.integers(0, capacity + 1, size=B).astype(np.int32))
+
+
+# The workloads, by what they are.  Seeds are fixed per workload.
 WORKLOADS = {
     "tiny_f32": dict(seed=1000, lengths=[64, 64], Hk=1, Hv=2, dk=32, dv=32,
                      dtype_qkv="f32", dtype_gate="f32", chunk=16,
@@ -121,4 +127,10 @@ WORKLOADS = {
     "decode_B256": dict(seed=1004, B=256, steps=64, Hk=16, Hv=32, dk=128,
                         dv=128, dtype_qkv="bf16", dtype_gate="bf16",
                         capacity=4),
+    # speculative decoding: each step replays the accepted prefix of the
+    # previous step's 4 captured drafts (accepted ~ U{0..4}) and verifies 4
+    # new draft tokens per row, all captured
+    "verify_B256_T4": dict(seed=1005, B=256, steps=16, T=4, Hk=16, Hv=32,
+                           dk=128, dv=128, dtype_qkv="bf16", dtype_gate="bf16",
+                           capacity=4),
 }

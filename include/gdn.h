@@ -181,6 +181,51 @@ GDN_API int gdn_replay_state_updates(const float *state_in, float *state_out,
                              int Hv, int dk, int dv, void *stream);
 
 /*
+ * gdn_replay_verify -- one speculative-decoding step in one launch: replay
+ * the accepted prefix of the previous verify pass, then verify the next
+ * draft tokens [P3-DF: the DFlash2 loop is capture during verification,
+ * replay of the accepted prefix, and a state that must match the
+ * non-speculative run].  It equals gdn_replay_state_updates followed by
+ * gdn_recurrent_capture, but reads each state once and writes it once instead
+ * of reading it twice and writing it once.  Per (row b, value head h):
+ *     S  = state_in[b]                        (zeros when state_in is NULL)
+ *     for t < m_b: S <- decay_t * S + outer(delta_t, key_t)
+ *                  factors from slot t of prev_state_update, row b;
+ *                  m_b = clamp(accepted_count[b], 0, prev_capacity)
+ *     state_out[b] = S                        (the committed state)
+ *     then the row's T_b draft tokens run from S exactly as in
+ *     gdn_recurrent_capture: out, capture into state_update, and the state
+ *     after the last draft token in draft_final_state (if not NULL).
+ *
+ *  q ... beta, cu_seqlens   the draft tokens, as in gdn_recurrent_capture;
+ *                         rows with T_b = 0 only replay.
+ *  state_in               NULL or fp32 [B, Hv, dv, dk] (no index gather).
+ *  state_out              fp32 [B, Hv, dv, dk], required; may be exactly
+ *                         state_in (in place: rows with m_b = 0 are then not
+ *                         rewritten).
+ *  prev_state_update      fp32 [B, prev_capacity, slot], the previous call's
+ *                         capture (input); NULL allowed when prev_capacity == 0
+ *                         (nothing is replayed).  It must not overlap
+ *                         state_update: alternate two capture buffers.
+ *  accepted_count         int32 [B], device; required when prev_capacity > 0.
+ *                         Precondition: m_b <= the n_b the capture used.
+ *  draft_final_state      NULL or fp32 [B, Hv, dv, dk] (output).
+ *  state_update_capacity, capture_count, state_update_active, state_update
+ *                         the new capture, as in gdn_recurrent_capture.
+ */
+GDN_API int gdn_replay_verify(const void *q, const void *k, const void *v,
+                              const void *alpha, const void *beta,
+                              const int32_t *cu_seqlens, const float *state_in,
+                              float *state_out, const float *prev_state_update,
+                              int prev_capacity, const int32_t *accepted_count,
+                              float *draft_final_state, void *out, int B, int T, int Hq,
+                              int Hk, int Hv, int dk, int dv, float scale, int dtype_qkv,
+                              int dtype_gate, int state_update_capacity,
+                              const int32_t *capture_count,
+                              const int32_t *state_update_active, float *state_update,
+                              void *stream);
+
+/*
  * gdn_prefill_chunked_noalloc -- gdn_prefill_chunked for callers that cannot
  * allocate device memory: runtimes with their own memory planner that forbid
  * hidden allocations, code running while a stream is being captured into a

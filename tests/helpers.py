@@ -51,3 +51,24 @@ def to_dev(x, dev="cuda"):
     g["cu_seqlens"] = x.cu_seqlens.to(dev)
     g["initial_state"] = x.initial_state.to(dev) if x.initial_state is not None else None
     return g
+
+
+def check_capture(su_gpu: Guarded, su_ref, counts, x, cap):
+    """Captured slots [0, n_b) against the oracle (decay and key bit for bit,
+    delta to TOL_CAPTURE); slots past n_b still hold the sentinel; guard
+    bands intact.  Returns the n_b."""
+    n = [max(0, min(int(c), cap, L)) for c, L in zip(counts, x.lengths)]
+    Hv, Hk, dk = x.Hv, x.Hk, x.dk
+    su = su_gpu.t
+    for b, nb in enumerate(n):
+        if nb > 0:
+            g = su[b, :nb].cpu().double().numpy()
+            r = su_ref[b, :nb]
+            # decay and key: exact widenings of the inputs
+            assert np.array_equal(g[:, :Hv + Hk * dk], r[:, :Hv + Hk * dk]), b
+            assert rel(su[b, :nb, Hv + Hk * dk:], r[:, Hv + Hk * dk:]) < TOL_CAPTURE, b
+        if nb < cap:
+            assert bool(torch.all(su_gpu.untouched((b, slice(nb, cap)))).item()), \
+                f"row {b}: uncaptured slots were written"
+    assert su_gpu.guards_intact()
+    return n

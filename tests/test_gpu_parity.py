@@ -15,7 +15,7 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import TOL, TOL_CAPTURE, Guarded, rel, to_dev
+from helpers import TOL, TOL_CAPTURE, Guarded, check_capture as _check_capture, rel, to_dev
 
 pytestmark = pytest.mark.gpu
 THREADS = min(32, os.cpu_count() or 4)
@@ -53,24 +53,6 @@ def _prefix_state(oracle_mod, x, b, n):
                                    initial_state=None if x.initial_state is None
                                    else x.initial_state[b:b + 1])
     return S[0]
-
-
-def _check_capture(su_gpu: Guarded, su_ref, counts, x, cap):
-    n = [max(0, min(int(c), cap, L)) for c, L in zip(counts, x.lengths)]
-    Hv, Hk, dk = x.Hv, x.Hk, x.dk
-    su = su_gpu.t
-    for b, nb in enumerate(n):
-        if nb > 0:
-            g = su[b, :nb].cpu().double().numpy()
-            r = su_ref[b, :nb]
-            # decay and key: exact widenings of the inputs
-            assert np.array_equal(g[:, :Hv + Hk * dk], r[:, :Hv + Hk * dk]), b
-            assert rel(su[b, :nb, Hv + Hk * dk:], r[:, Hv + Hk * dk:]) < TOL_CAPTURE, b
-        if nb < cap:
-            assert bool(torch.all(su_gpu.untouched((b, slice(nb, cap)))).item()), \
-                f"row {b}: uncaptured slots were written"
-    assert su_gpu.guards_intact()
-    return n
 
 
 # ---------------------------------------------------------------- tiny fp32

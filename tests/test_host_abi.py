@@ -75,6 +75,19 @@ def rep(L, **kw):
                                       a["Hk"], a["Hv"], a["dk"], a["dv"], None)
 
 
+def rv(L, **kw):
+    a = dict(q=A, k=A + GiB, v=A + 2 * GiB, alpha=A + 3 * GiB, beta=A + 4 * GiB, cu=None,
+             si=A + 5 * GiB, so=A + 5 * GiB, psu=A + 6 * GiB, pcap=4, acc=A + 7 * GiB,
+             sf=None, out=A + 8 * GiB, B=2, T=4, Hq=2, Hk=2, Hv=6, dk=128, dv=128,
+             scale=1.0, dtq=2, dtg=2, cap=4, cc=A + 9 * GiB, act=None, su=A + 10 * GiB)
+    a.update(kw)
+    return L.gdn_replay_verify(a["q"], a["k"], a["v"], a["alpha"], a["beta"], a["cu"],
+                               a["si"], a["so"], a["psu"], a["pcap"], a["acc"], a["sf"],
+                               a["out"], a["B"], a["T"], a["Hq"], a["Hk"], a["Hv"], a["dk"],
+                               a["dv"], a["scale"], a["dtq"], a["dtg"], a["cap"], a["cc"],
+                               a["act"], a["su"], None)
+
+
 INVALID, UNSUP, ALIAS, ALIGN, WS = 1, 2, 3, 4, 7
 
 
@@ -134,11 +147,38 @@ def test_replay_rejects(L, kw, code):
     assert rep(L, **kw) == code
 
 
+@pytest.mark.parametrize("kw,code", [
+    (dict(pcap=-1), INVALID),
+    (dict(acc=None), INVALID),               # replay needs the acceptance counts
+    (dict(psu=None), INVALID),               # ... and the previous capture
+    (dict(so=None), INVALID),                # the committed state is required
+    (dict(cc=None), INVALID),
+    (dict(Hv=5), INVALID),
+    (dict(dk=80), UNSUP),
+    (dict(psu=A + 6 * GiB + 4), ALIGN),
+    (dict(acc=A + 7 * GiB + 2), ALIGN),
+    (dict(so=A + 5 * GiB + 512), ALIAS),     # partial overlap with state_in
+    (dict(su=A + 6 * GiB + 1024), ALIAS),    # new capture over the previous one
+    (dict(sf=A + 5 * GiB), ALIAS),           # draft final state over the committed state
+    (dict(so=A + 8 * GiB), ALIAS),           # committed state over out
+    (dict(out=A + 2 * GiB), ALIAS),          # out is v
+])
+def test_replay_verify_rejects(L, kw, code):
+    assert rv(L, **kw) == code
+
+
+def test_replay_verify_accepts_plain_verify_and_no_replay_buffers(L):
+    # prev_capacity == 0: nothing to replay, the factor pointers may be NULL;
+    # B = 0 returns before any CUDA call.
+    assert rv(L, pcap=0, psu=None, acc=None, B=0, T=0) == 0
+
+
 def test_empty_batch_is_a_no_op(L):
     # B = 0 passes validation and returns before any CUDA call.
     assert rec(L, B=0, T=0) == 0
     assert pre(L, B=0, T=0) == 0
     assert rep(L, B=0) == 0
+    assert rv(L, B=0, T=0) == 0
 
 
 def test_workspace_size_query(L):
