@@ -210,6 +210,33 @@ def replay(state_in, state_update, accepted_count, *, B, Hk, Hv, dk, dv,
     return S
 
 
+def prefix_checkpoints(q, k, v, alpha, beta, *, B, Hk, Hv, dk, dv, every, capacity,
+                       T=None, cu_seqlens=None, initial_state=None,
+                       initial_state_indices=None, scale=1.0, heads=None, threads=None):
+    """State of row b after (j + 1) * every tokens, for
+    j < min(capacity, floor(T_b / every)): snapshots of growing prefixes of
+    each row ("Enable the native Kev example on the WebGPU backend",
+    executorch issue 23099: an immutable prefix snapshot reused later), kept
+    at every boundary.  Each is the recurrence (``recurrent``) run over that
+    prefix, continued segment by segment from the previous snapshot.
+    ``heads``: optional value heads to compute (others NaN).  Returns
+    [B, capacity, Hv, dv, dk] with NaN in slots that are not defined."""
+    rows = _row_bounds(cu_seqlens, B, T)
+    S = _gather_states(initial_state, initial_state_indices, B, Hv, dv, dk)
+    out = np.full((B, capacity, Hv, dv, dk), np.nan)
+    hs = range(Hv) if heads is None else heads
+    for b, (tok0, tb) in enumerate(rows):
+        Sb = S[b:b + 1]
+        for j in range(min(capacity, tb // every)):
+            seg = slice(tok0 + j * every, tok0 + (j + 1) * every)
+            _, Sb, _ = recurrent(q[seg], k[seg], v[seg], alpha[seg], beta[seg], B=1,
+                                 Hk=Hk, Hv=Hv, dk=dk, dv=dv, T=every, initial_state=Sb,
+                                 scale=scale, units=[(0, h) for h in hs],
+                                 threads=threads)
+            out[b, j, list(hs)] = Sb[0, list(hs)]
+    return out
+
+
 def replay_verify(q, k, v, alpha, beta, *, B, Hk, Hv, dk, dv, T=None,
                   cu_seqlens=None, state_in=None, prev_state_update=None,
                   prev_capacity=0, accepted_count=None, scale=1.0, capacity=0,

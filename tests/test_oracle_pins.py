@@ -272,3 +272,39 @@ def test_speculative_loop_matches_non_speculative_run(oracle_mod, accepted):
         if lens2[r]:
             got = o2[cu2[r]:cu2[r + 1]]
             assert _rel(got, o_ns[m:]) < 1e-13
+
+
+# --- chunk-boundary checkpoints -------------------------------------------
+
+def test_prefix_checkpoints_match_the_chunked_form_and_resume(oracle_mod):
+    """Checkpoint j is the state after (j + 1) * L tokens: it equals the
+    independent chunked (UT/WY) formulation run over that prefix, resuming
+    the recurrence from any checkpoint over the rest of the row gives the
+    row's final state, and slots past floor(T_b / L) (or the capacity) stay
+    undefined."""
+    rng = np.random.default_rng(70)
+    lengths = [37, 12, 50]
+    Hk, Hv, dk, dv, L, cap = 1, 2, 4, 3, 8, 5
+    T = sum(lengths)
+    q, k, v, a, b, _ = _rand_case(rng, T, Hk, Hv, dk, dv)
+    S0 = 0.3 * rng.standard_normal((3, Hv, dv, dk))
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    dims = dict(B=3, Hk=Hk, Hv=Hv, dk=dk, dv=dv)
+    ck = oracle_mod.prefix_checkpoints(q, k, v, a, b, every=L, capacity=cap,
+                                       cu_seqlens=cu, initial_state=S0, **dims)
+    _, S_fin, _ = oracle_mod.recurrent(q, k, v, a, b, cu_seqlens=cu, initial_state=S0, **dims)
+    one = dict(B=1, Hk=Hk, Hv=Hv, dk=dk, dv=dv)
+    for r, tb in enumerate(lengths):
+        n = min(cap, tb // L)
+        assert np.all(np.isnan(ck[r, n:]))
+        for j in range(n):
+            t1 = cu[r] + (j + 1) * L
+            _, Sc = oracle_mod.chunked(q[cu[r]:t1], k[cu[r]:t1], v[cu[r]:t1], a[cu[r]:t1],
+                                       b[cu[r]:t1], T=t1 - cu[r], chunk=5,
+                                       initial_state=S0[r:r + 1], **one)
+            assert _rel(ck[r, j], Sc[0]) < 1e-12, (r, j)
+            rest = slice(t1, cu[r + 1])
+            _, S_res, _ = oracle_mod.recurrent(q[rest], k[rest], v[rest], a[rest], b[rest],
+                                               T=cu[r + 1] - t1, initial_state=ck[r, j][None],
+                                               **one)
+            assert _rel(S_res[0], S_fin[r]) < 1e-12, (r, j)
