@@ -363,6 +363,7 @@ def run_ours(args, rank, world, local_rank):
     ver_bytes_call = verify_bytes(v_acc.tolist(), B, d)
     ver_avg_s = statistics.mean(ver_ms) / 1e3
     unfused = run_verify_unfused(gdn, stream, gv, su_prev, v_acc_d, v_full, S_ver, d)
+    ckpt = run_prefill_checkpoints(gdn, stream, gp, p_out, p_fs, ws, flush)
     ms_per_step = (sum(pre_ms) + sum(dec_ms) + sum(rep_ms) + sum(ver_ms)) / args.steps
     ms_per_step = reduce_scalar(ms_per_step, "max", dev)
 
@@ -419,6 +420,15 @@ def run_ours(args, rank, world, local_rank):
                     "algorithmic_flops_per_launch": pf, "traffic": None,
                 },
                 "e2e": e2e_pre,
+                "checkpoints": {
+                    "workload": "prefill_T4100 with the fp32 state written after every "
+                                "64-token chunk (64 checkpoints, gdn_prefill_chunked_checkpoints)",
+                    "avg_launch_us": ckpt["us"],
+                    "value": round(p["T"] / (ckpt["us"] * 1e-6), 1), "unit": "tokens/s",
+                    "checkpoint_bytes_per_launch": ckpt["bytes"],
+                    "frac": round((pb + ckpt["bytes"]) / (ckpt["us"] * 1e-6) / 1e9 / hbm_peak, 4),
+                    "overhead_vs_plain": round(ckpt["us"] / (pre_avg_s * 1e6) - 1.0, 4),
+                },
             },
             "replay": {
                 "value": round(rep_bytes_call / rep_avg_s / 1e9, 1), "unit": "GB/s",
@@ -474,6 +484,31 @@ def run_verify_unfused(gdn, stream, gv, su_prev, acc_d, full, S_src, d, n=20, wa
     ver = statistics.mean(e[1].elapsed_time(e[2]) for e in ev) * 1e3
     del S
     return {"replay": round(rep, 2), "verify": round(ver, 2), "total": round(rep + ver, 2)}
+
+
+def run_prefill_checkpoints(gdn, stream, gp, out, fs, ws, flush, n=10, warm=3):
+    """The prefill with a checkpoint after every chunk, timed outside the step
+    (L2 flushed before each launch): mean microseconds and checkpoint bytes."""
+    import torch
+    p = PRE
+    cap = p["T"] // p["chunk"]
+    ck = torch.empty((1, cap, p["Hv"], p["dv"], p["dk"]), dtype=torch.float32,
+                     device=gp["q"].device)
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    ev = [[E(), E()] for _ in range(n)]
+    for i in range(warm + n):
+        flush.fill_(2)
+        e = ev[i - warm] if i >= warm else None
+        if e: e[0].record(stream)
+        gdn.gdn_prefill_chunked_checkpoints(
+            gp["q"], gp["k"], gp["v"], gp["alpha"], gp["beta"], B=1, T=p["T"],
+            initial_state=gp["initial_state"], final_state=fs, out=out, checkpoints=ck,
+            checkpoint_capacity=cap, checkpoint_interval=1, chunk=p["chunk"], workspace=ws)
+        if e: e[1].record(stream)
+    torch.cuda.synchronize()
+    assert torch.isfinite(ck).all()
+    us = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) * 1e3
+    return {"us": round(us, 2), "bytes": ck.numel() * 4}
 
 
 PREFILL_LAUNCHES = 2  # kernels one gdn_prefill_chunked call launches on this workload (tensor-core path)

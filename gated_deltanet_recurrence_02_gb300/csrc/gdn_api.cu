@@ -313,6 +313,22 @@ int gdn_prefill_chunked(const void *q, const void *k, const void *v, const void 
                         float *final_state, void *out, int B, int T, int Hq, int Hk, int Hv,
                         int dk, int dv, int chunk, float scale, int dtype_qkv, int dtype_gate,
                         void *workspace, size_t workspace_bytes, void *stream) {
+    return gdn_prefill_chunked_checkpoints(q, k, v, alpha, beta, cu_seqlens, initial_state,
+                                           initial_state_indices, num_initial_states, final_state,
+                                           out, B, T, Hq, Hk, Hv, dk, dv, chunk, scale, dtype_qkv,
+                                           dtype_gate, nullptr, 0, 1, workspace, workspace_bytes,
+                                           stream);
+}
+
+int gdn_prefill_chunked_checkpoints(const void *q, const void *k, const void *v,
+                                    const void *alpha, const void *beta,
+                                    const int32_t *cu_seqlens, const float *initial_state,
+                                    const int32_t *initial_state_indices, int num_initial_states,
+                                    float *final_state, void *out, int B, int T, int Hq, int Hk,
+                                    int Hv, int dk, int dv, int chunk, float scale, int dtype_qkv,
+                                    int dtype_gate, float *checkpoints, int checkpoint_capacity,
+                                    int checkpoint_interval, void *workspace,
+                                    size_t workspace_bytes, void *stream) {
     Shapes sh;
     int st = check_common(q, k, v, alpha, beta, cu_seqlens, initial_state, initial_state_indices,
                           num_initial_states, final_state, out, B, T, Hq, Hk, Hv, dk, dv,
@@ -327,6 +343,13 @@ int gdn_prefill_chunked(const void *q, const void *k, const void *v, const void 
         gdn_prefill_workspace_size(B, T, Hk, Hv, dk, dv, chunk, dtype_qkv, cu_seqlens != nullptr);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return GDN_ERR_WORKSPACE;
     if (workspace && !aligned(workspace, 16)) return GDN_ERR_ALIGN;
+    if (checkpoint_capacity < 0 || checkpoint_interval < 1) return GDN_ERR_INVALID_ARG;
+    if (checkpoint_capacity > 0 && checkpoints == nullptr) return GDN_ERR_INVALID_ARG;
+    if (checkpoints && !aligned(checkpoints, 16)) return GDN_ERR_ALIGN;
+    size_t ck_bytes = 0;
+    if (checkpoint_capacity > 0 &&
+        !mul_ok((size_t)B * checkpoint_capacity, (size_t)Hv * dv * dk * sizeof(float), &ck_bytes))
+        return GDN_ERR_INVALID_ARG;
     const size_t sf_in_place = (final_state == initial_state) ? sh.sf_bytes : 0;
     Span spans[] = {
         {q, sh.qk_bytes, false},
@@ -340,6 +363,7 @@ int gdn_prefill_chunked(const void *q, const void *k, const void *v, const void 
         {final_state, sh.sf_bytes, true},                                  // 8
         {out, sh.v_bytes, true},
         {workspace, need, true},
+        {checkpoints, ck_bytes, true},
     };
     st = check_alias(spans, (int)(sizeof(spans) / sizeof(spans[0])), 6, 8);
     if (st != GDN_OK) return st;
@@ -353,6 +377,8 @@ int gdn_prefill_chunked(const void *q, const void *k, const void *v, const void 
     p.B = B; p.T = T; p.Hk = Hk; p.Hv = Hv; p.dk = dk; p.dv = dv; p.chunk = chunk;
     p.scale = scale; p.dt_qkv = dtype_qkv; p.dt_gate = dtype_gate;
     p.ws = workspace; p.ws_bytes = workspace_bytes;
+    p.ckpt = checkpoint_capacity > 0 ? checkpoints : nullptr;
+    p.ckpt_cap = checkpoint_capacity; p.ckpt_every = checkpoint_interval;
     if (error_word(&p.err) != cudaSuccess) return GDN_ERR_CUDA;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     const cudaError_t e = use_tc ? launch_prefill_tc(p, s) : launch_prefill_simt(p, s);

@@ -65,8 +65,23 @@ struct PrefillParams {
     int dt_qkv, dt_gate;
     void *ws;
     size_t ws_bytes;
+    // Chunk-boundary checkpoints (nullptr: none): slot j of row b receives the
+    // state after (j + 1) * ckpt_every chunks, for j < ckpt_cap, when that
+    // boundary lies inside the row.  Layout [B, ckpt_cap, Hv, dv, dk].
+    float *ckpt;
+    int ckpt_cap, ckpt_every;
     uint32_t *err;
 };
+
+// Checkpoint slot written at the end of chunk cc (0-based) of a row of len
+// tokens, or -1.
+__host__ __device__ __forceinline__ int ckpt_slot(const PrefillParams &p, int cc, int len) {
+    if (p.ckpt == nullptr) return -1;
+    const int done = cc + 1;
+    if (done % p.ckpt_every != 0 || (long)done * p.chunk > len) return -1;
+    const int j = done / p.ckpt_every - 1;
+    return j < p.ckpt_cap ? j : -1;
+}
 
 // Launchers: enqueue on `stream`, return cudaGetLastError().
 cudaError_t launch_recurrent(const RecurrentParams &p, cudaStream_t stream);

@@ -15,6 +15,8 @@
 //   Delta   = (I + A)^{-1} R                               forward substitution
 //   O       = diag(gamma) Q S0^T + P Delta
 //   S_end   = gamma_n S0 + Delta^T diag(e^{g_n - g}) K
+// S_end of a chunk that ends on a requested boundary is also written out as a
+// checkpoint (the state after that many tokens of the row).
 // (the UT/WY form; Delta equals U - W S0^T with U = T diag(beta) V and
 // W = T diag(beta gamma) K).  A ragged last chunk is padded with identity
 // tokens (k = q = v = 0, alpha = 1, beta = 0), which leave S unchanged and
@@ -239,6 +241,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(const Prefill
             }
         }
         __syncthreads();
+        // ---- 6. chunk-boundary checkpoint ------------------------------------
+        const int ck = ckpt_slot(p, c0 / C, Tb);
+        if (ck >= 0) {
+            float *dst = p.ckpt + ((((long)b * p.ckpt_cap + ck) * Hv + h) * dv + row0) * DK;
+            for (int e = tid; e < kDVT * DK / 4; e += kThreads) {
+                const int i = e / (DK / 4), j = (e % (DK / 4)) * 4;
+                __stcs(reinterpret_cast<float4 *>(dst + (long)i * DK + j),
+                       *reinterpret_cast<const float4 *>(Ss + i * KS + j));
+            }
+        }
     }
 
     if (p.s_final != nullptr) {

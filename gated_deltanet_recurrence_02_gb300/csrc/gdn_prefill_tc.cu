@@ -35,7 +35,8 @@
 // through a three-stage TMA / bulk-copy ring, with L2 prefetches further
 // ahead; the output MMA (P' Delta) is committed separately so the state
 // update never waits for it, and the next chunk's first MMA is issued as soon
-// as the state image is written.
+// as the state image is written.  At a requested chunk boundary the fp32
+// state in the registers is also streamed out as a checkpoint.
 //
 // Ragged chunks: tokens t >= n get alpha = 1 and beta = 0, which makes their
 // rows of T the identity rows and their U, W, Delta rows zero, so whatever the
@@ -716,6 +717,13 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
                 for (int q8 = 0; q8 < 2; ++q8)
                     *reinterpret_cast<uint4 *>(sS + sw128_chunk(j, 2 * half + q8)) = pack8<E>(S + 8 * q8);
                 fence_proxy_async();
+                // chunk-boundary checkpoint: the fp32 state after this chunk
+                const int ck = ckpt_slot(p, cc, len);
+                if (ck >= 0) {
+                    float *dst = p.ckpt + ((((size_t)b * p.ckpt_cap + ck) * Hv + h) * D + i0 + c0) * D;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) __stcs(dst + (size_t)i * D + j, S[i]);
+                }
             }
             fence_before_sync();
             named_bar(kBarState, kBarThreads);

@@ -48,6 +48,9 @@ def lib() -> ctypes.CDLL:
     L.gdn_prefill_workspace_size.restype = sz
     L.gdn_prefill_chunked.argtypes = [vp] * 8 + [i, vp, vp] + [i] * 8 + [f, i, i, vp, sz, vp]
     L.gdn_prefill_chunked.restype = i
+    L.gdn_prefill_chunked_checkpoints.argtypes = ([vp] * 8 + [i, vp, vp] + [i] * 8 + [f, i, i]
+                                                  + [vp, i, i, vp, sz, vp])
+    L.gdn_prefill_chunked_checkpoints.restype = i
     L.gdn_recurrent_capture.argtypes = ([vp] * 8 + [i, vp, vp] + [i] * 7 + [f, i, i]
                                         + [i, vp, vp, vp, vp])
     L.gdn_recurrent_capture.restype = i
@@ -137,6 +140,37 @@ def gdn_prefill_chunked(q, k, v, alpha, beta, *, B: int, T: Optional[int] = None
         ws_bytes, _stream(stream))
     _check(st, "gdn_prefill_chunked")
     return out, final_state
+
+
+def gdn_prefill_chunked_checkpoints(q, k, v, alpha, beta, *, B: int, checkpoint_capacity: int,
+                                    checkpoint_interval: int = 1, T: Optional[int] = None,
+                                    cu_seqlens=None, initial_state=None,
+                                    initial_state_indices=None, final_state=None, out=None,
+                                    checkpoints=None, chunk: int = 64, scale: float = 1.0,
+                                    workspace=None, want_final_state: bool = True, stream=None):
+    """Chunked prefill that also writes the state every checkpoint_interval
+    chunks.  Returns (out, final_state, checkpoints [B, capacity, Hv, dv, dk])."""
+    T, Hk, dk, Hv, dv = _dims(q, v, B, T, cu_seqlens)
+    if out is None:
+        out = torch.empty_like(v)
+    if final_state is None and want_final_state:
+        final_state = torch.empty((B, Hv, dv, dk), dtype=torch.float32, device=v.device)
+    cap = int(checkpoint_capacity)
+    if checkpoints is None and cap > 0:
+        checkpoints = torch.empty((B, cap, Hv, dv, dk), dtype=torch.float32, device=v.device)
+    n0 = initial_state.shape[0] if initial_state is not None else 0
+    need = gdn_prefill_workspace_size(B, T, Hk, Hv, dk, dv, chunk, q.dtype,
+                                      varlen=cu_seqlens is not None)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=v.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().gdn_prefill_chunked_checkpoints(
+        _p(q), _p(k), _p(v), _p(alpha), _p(beta), _p(cu_seqlens), _p(initial_state),
+        _p(initial_state_indices), n0, _p(final_state), _p(out), B, T, Hk, Hk, Hv,
+        dk, dv, chunk, scale, _DT[q.dtype], _DT[alpha.dtype], _p(checkpoints), cap,
+        int(checkpoint_interval), _p(workspace), ws_bytes, _stream(stream))
+    _check(st, "gdn_prefill_chunked_checkpoints")
+    return out, final_state, checkpoints
 
 
 def gdn_recurrent_capture(q, k, v, alpha, beta, *, B: int, T: Optional[int] = None,

@@ -133,6 +133,37 @@ GDN_API int gdn_prefill_chunked(const void *q, const void *k, const void *v,
                         void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * gdn_prefill_chunked_checkpoints -- gdn_prefill_chunked that also writes the
+ * state at chunk boundaries, so that a prefix can later be resumed from any
+ * of them (prefix-snapshot reuse at an offset [P1]: a snapshot is a state
+ * after a prefix; here one is kept every L tokens).  Arguments shared with
+ * gdn_prefill_chunked mean the same; gdn_prefill_chunked is this call with no
+ * checkpoints.
+ *
+ *  checkpoint_interval    >= 1 chunks: boundaries every L = interval * chunk
+ *                         tokens of each row.
+ *  checkpoint_capacity    >= 0 slots per row (0: none, checkpoints may be NULL).
+ *  checkpoints            fp32 [B, checkpoint_capacity, Hv, dv, dk] (output).
+ *                         Slot j of row b holds the state after (j + 1) * L
+ *                         tokens of the row, for
+ *                         j < min(capacity, floor(T_b / L)); later slots are
+ *                         not written (their contents are unspecified).  The
+ *                         state past the last full boundary is final_state.
+ */
+GDN_API int gdn_prefill_chunked_checkpoints(const void *q, const void *k, const void *v,
+                                            const void *alpha, const void *beta,
+                                            const int32_t *cu_seqlens,
+                                            const float *initial_state,
+                                            const int32_t *initial_state_indices,
+                                            int num_initial_states, float *final_state,
+                                            void *out, int B, int T, int Hq, int Hk, int Hv,
+                                            int dk, int dv, int chunk, float scale,
+                                            int dtype_qkv, int dtype_gate, float *checkpoints,
+                                            int checkpoint_capacity, int checkpoint_interval,
+                                            void *workspace, size_t workspace_bytes,
+                                            void *stream);
+
+/*
  * gdn_recurrent_capture -- per-token recurrent (decode / verify) path with
  * compact state-update capture [P3].  Arguments shared with
  * gdn_prefill_chunked mean the same (alpha = 0 is allowed here).

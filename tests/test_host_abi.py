@@ -75,6 +75,19 @@ def rep(L, **kw):
                                       a["Hk"], a["Hv"], a["dk"], a["dv"], None)
 
 
+def prc(L, **kw):
+    a = dict(q=A, k=A + GiB, v=A + 2 * GiB, alpha=A + 3 * GiB, beta=A + 4 * GiB, cu=None,
+             s0=A + 5 * GiB, idx=None, n0=1, sf=A + 6 * GiB, out=A + 7 * GiB, B=1, T=100,
+             Hq=16, Hk=16, Hv=32, dk=128, dv=128, chunk=64, scale=1.0, dtq=2, dtg=0,
+             ck=A + 9 * GiB, cap=2, every=1, ws=A + 8 * GiB, wsb=1 << 30)
+    a.update(kw)
+    return L.gdn_prefill_chunked_checkpoints(
+        a["q"], a["k"], a["v"], a["alpha"], a["beta"], a["cu"], a["s0"], a["idx"], a["n0"],
+        a["sf"], a["out"], a["B"], a["T"], a["Hq"], a["Hk"], a["Hv"], a["dk"], a["dv"],
+        a["chunk"], a["scale"], a["dtq"], a["dtg"], a["ck"], a["cap"], a["every"], a["ws"],
+        a["wsb"], None)
+
+
 def rv(L, **kw):
     a = dict(q=A, k=A + GiB, v=A + 2 * GiB, alpha=A + 3 * GiB, beta=A + 4 * GiB, cu=None,
              si=A + 5 * GiB, so=A + 5 * GiB, psu=A + 6 * GiB, pcap=4, acc=A + 7 * GiB,
@@ -165,6 +178,24 @@ def test_replay_rejects(L, kw, code):
 ])
 def test_replay_verify_rejects(L, kw, code):
     assert rv(L, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(cap=-1), INVALID),
+    (dict(every=0), INVALID),
+    (dict(ck=None), INVALID),                # capacity > 0 needs the buffer
+    (dict(ck=A + 9 * GiB + 8), ALIGN),
+    (dict(ck=A + 7 * GiB + 4096), ALIAS),    # checkpoints over out
+    (dict(ck=A + 8 * GiB), ALIAS),           # checkpoints over the workspace
+    (dict(chunk=40), UNSUP),
+])
+def test_prefill_checkpoints_rejects(L, kw, code):
+    assert prc(L, **kw) == code
+
+
+def test_prefill_checkpoints_empty_and_without_slots(L):
+    assert prc(L, B=0, T=0) == 0
+    assert prc(L, B=0, T=0, ck=None, cap=0) == 0
 
 
 def test_replay_verify_accepts_plain_verify_and_no_replay_buffers(L):
