@@ -74,3 +74,19 @@ def test_bench_decode_bytes_match_the_recipe():
     assert got == state + vecs + 200 * slot
     b, f = bench.prefill_bytes_flops()
     assert f == 4100 * 32 * (6 * 128 * 128 + 10 * 64 * 128)
+
+
+def test_bench_verify_bytes_match_the_recipe():
+    """Algorithmic bytes of one fused replay + verify call at B=256, state in
+    place: the state read for every row and written for rows that replay,
+    replayed slots read, 4 draft tokens' bf16 inputs and outputs, 4 captured
+    slots written per row, int32 counts."""
+    sys.path.insert(0, ROOT)
+    import bench
+    accepted = [0] * 56 + [1] * 50 + [2] * 50 + [3] * 50 + [4] * 50
+    got = bench.verify_bytes(accepted, 256)
+    st = 32 * 128 * 128 * 4
+    slot = (32 + 16 * 128 + 32 * 128) * 4
+    tokens = 256 * 4 * (2 * 16 * 128 + 2 * 32 * 128 + 2 * 32) * 2
+    replayed = 50 * (1 + 2 + 3 + 4)
+    assert got == 256 * st + 200 * st + replayed * slot + 256 * 4 * slot + 2 * 256 * 4 + tokens
