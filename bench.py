@@ -363,7 +363,8 @@ def run_ours(args, rank, world, local_rank):
     ver_bytes_call = verify_bytes(v_acc.tolist(), B, d)
     ver_avg_s = statistics.mean(ver_ms) / 1e3
     unfused = run_verify_unfused(gdn, stream, gv, su_prev, v_acc_d, v_full, S_ver, d)
-    ckpt = run_prefill_checkpoints(gdn, stream, gp, p_out, p_fs, ws, flush)
+    ckpt = run_prefill_variant(gdn, stream, gp, p_out, p_fs, ws, flush, "checkpoints")
+    pcap = run_prefill_variant(gdn, stream, gp, p_out, p_fs, ws, flush, "capture")
     ms_per_step = (sum(pre_ms) + sum(dec_ms) + sum(rep_ms) + sum(ver_ms)) / args.steps
     ms_per_step = reduce_scalar(ms_per_step, "max", dev)
 
@@ -429,6 +430,14 @@ def run_ours(args, rank, world, local_rank):
                     "frac": round((pb + ckpt["bytes"]) / (ckpt["us"] * 1e-6) / 1e9 / hbm_peak, 4),
                     "overhead_vs_plain": round(ckpt["us"] / (pre_avg_s * 1e6) - 1.0, 4),
                 },
+                "capture": {
+                    "workload": "prefill_T4100 with the compact capture of its first 64 tokens "
+                                "(capacity 64, gdn_prefill_chunked_capture)",
+                    "avg_launch_us": pcap["us"],
+                    "value": round(p["T"] / (pcap["us"] * 1e-6), 1), "unit": "tokens/s",
+                    "capture_bytes_per_launch": pcap["bytes"],
+                    "overhead_vs_plain": round(pcap["us"] / (pre_avg_s * 1e6) - 1.0, 4),
+                },
             },
             "replay": {
                 "value": round(rep_bytes_call / rep_avg_s / 1e9, 1), "unit": "GB/s",
@@ -486,29 +495,45 @@ def run_verify_unfused(gdn, stream, gv, su_prev, acc_d, full, S_src, d, n=20, wa
     return {"replay": round(rep, 2), "verify": round(ver, 2), "total": round(rep + ver, 2)}
 
 
-def run_prefill_checkpoints(gdn, stream, gp, out, fs, ws, flush, n=10, warm=3):
-    """The prefill with a checkpoint after every chunk, timed outside the step
-    (L2 flushed before each launch): mean microseconds and checkpoint bytes."""
+def run_prefill_variant(gdn, stream, gp, out, fs, ws, flush, kind, n=10, warm=3):
+    """The prefill with an extra output, timed outside the step (L2 flushed
+    before each launch): kind "checkpoints" writes the state after every chunk,
+    kind "capture" captures the first 64 tokens (capacity 64).  Returns the
+    mean microseconds and the extra bytes written per launch."""
     import torch
     p = PRE
-    cap = p["T"] // p["chunk"]
-    ck = torch.empty((1, cap, p["Hv"], p["dv"], p["dk"]), dtype=torch.float32,
-                     device=gp["q"].device)
+    dev = gp["q"].device
+    if kind == "checkpoints":
+        cap = p["T"] // p["chunk"]
+        buf = torch.empty((1, cap, p["Hv"], p["dv"], p["dk"]), dtype=torch.float32, device=dev)
+        extra = buf.numel() * 4
+    else:
+        cap = 64
+        slot = p["Hv"] + p["Hk"] * p["dk"] + p["Hv"] * p["dv"]
+        buf = torch.empty((1, cap, slot), dtype=torch.float32, device=dev)
+        count = torch.full((1,), cap, dtype=torch.int32, device=dev)
+        extra = buf.numel() * 4
     E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     ev = [[E(), E()] for _ in range(n)]
+    common = dict(B=1, T=p["T"], initial_state=gp["initial_state"], final_state=fs, out=out,
+                  chunk=p["chunk"], workspace=ws)
     for i in range(warm + n):
         flush.fill_(2)
         e = ev[i - warm] if i >= warm else None
         if e: e[0].record(stream)
-        gdn.gdn_prefill_chunked_checkpoints(
-            gp["q"], gp["k"], gp["v"], gp["alpha"], gp["beta"], B=1, T=p["T"],
-            initial_state=gp["initial_state"], final_state=fs, out=out, checkpoints=ck,
-            checkpoint_capacity=cap, checkpoint_interval=1, chunk=p["chunk"], workspace=ws)
+        if kind == "checkpoints":
+            gdn.gdn_prefill_chunked_checkpoints(gp["q"], gp["k"], gp["v"], gp["alpha"], gp["beta"],
+                                                checkpoints=buf, checkpoint_capacity=cap,
+                                                checkpoint_interval=1, **common)
+        else:
+            gdn.gdn_prefill_chunked_capture(gp["q"], gp["k"], gp["v"], gp["alpha"], gp["beta"],
+                                            state_update_capacity=cap, capture_count=count,
+                                            state_update=buf, **common)
         if e: e[1].record(stream)
     torch.cuda.synchronize()
-    assert torch.isfinite(ck).all()
+    assert torch.isfinite(buf).all()
     us = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) * 1e3
-    return {"us": round(us, 2), "bytes": ck.numel() * 4}
+    return {"us": round(us, 2), "bytes": extra}
 
 
 PREFILL_LAUNCHES = 2  # kernels one gdn_prefill_chunked call launches on this workload (tensor-core path)

@@ -307,28 +307,20 @@ size_t gdn_prefill_workspace_size(int B, int T, int Hk, int Hv, int dk, int dv, 
     return 0;
 }
 
-int gdn_prefill_chunked(const void *q, const void *k, const void *v, const void *alpha,
-                        const void *beta, const int32_t *cu_seqlens, const float *initial_state,
-                        const int32_t *initial_state_indices, int num_initial_states,
-                        float *final_state, void *out, int B, int T, int Hq, int Hk, int Hv,
-                        int dk, int dv, int chunk, float scale, int dtype_qkv, int dtype_gate,
-                        void *workspace, size_t workspace_bytes, void *stream) {
-    return gdn_prefill_chunked_checkpoints(q, k, v, alpha, beta, cu_seqlens, initial_state,
-                                           initial_state_indices, num_initial_states, final_state,
-                                           out, B, T, Hq, Hk, Hv, dk, dv, chunk, scale, dtype_qkv,
-                                           dtype_gate, nullptr, 0, 1, workspace, workspace_bytes,
-                                           stream);
-}
+}  // extern "C"
 
-int gdn_prefill_chunked_checkpoints(const void *q, const void *k, const void *v,
-                                    const void *alpha, const void *beta,
-                                    const int32_t *cu_seqlens, const float *initial_state,
-                                    const int32_t *initial_state_indices, int num_initial_states,
-                                    float *final_state, void *out, int B, int T, int Hq, int Hk,
-                                    int Hv, int dk, int dv, int chunk, float scale, int dtype_qkv,
-                                    int dtype_gate, float *checkpoints, int checkpoint_capacity,
-                                    int checkpoint_interval, void *workspace,
-                                    size_t workspace_bytes, void *stream) {
+namespace {
+
+// Every prefill entry point: validation, overlap checks, then one of the two
+// prefill kernels.  Checkpoints and capture are optional extras.
+int prefill_call(const void *q, const void *k, const void *v, const void *alpha, const void *beta,
+                 const int32_t *cu_seqlens, const float *initial_state,
+                 const int32_t *initial_state_indices, int num_initial_states, float *final_state,
+                 void *out, int B, int T, int Hq, int Hk, int Hv, int dk, int dv, int chunk,
+                 float scale, int dtype_qkv, int dtype_gate, float *checkpoints,
+                 int checkpoint_capacity, int checkpoint_interval, int capacity,
+                 const int32_t *capture_count, const int32_t *state_update_active,
+                 float *state_update, void *workspace, size_t workspace_bytes, void *stream) {
     Shapes sh;
     int st = check_common(q, k, v, alpha, beta, cu_seqlens, initial_state, initial_state_indices,
                           num_initial_states, final_state, out, B, T, Hq, Hk, Hv, dk, dv,
@@ -350,6 +342,16 @@ int gdn_prefill_chunked_checkpoints(const void *q, const void *k, const void *v,
     if (checkpoint_capacity > 0 &&
         !mul_ok((size_t)B * checkpoint_capacity, (size_t)Hv * dv * dk * sizeof(float), &ck_bytes))
         return GDN_ERR_INVALID_ARG;
+    if (capacity < 0) return GDN_ERR_INVALID_ARG;
+    if (capacity > 0 && (capture_count == nullptr || state_update == nullptr)) return GDN_ERR_INVALID_ARG;
+    if (state_update && !aligned(state_update, 16)) return GDN_ERR_ALIGN;
+    if ((capture_count && !aligned(capture_count, 4)) ||
+        (state_update_active && !aligned(state_update_active, 4)))
+        return GDN_ERR_ALIGN;
+    size_t su_bytes = 0;
+    if (capacity > 0 &&
+        !mul_ok((size_t)B * capacity, GDN_STATE_UPDATE_SLOT(Hk, Hv, dk, dv) * sizeof(float), &su_bytes))
+        return GDN_ERR_INVALID_ARG;
     const size_t sf_in_place = (final_state == initial_state) ? sh.sf_bytes : 0;
     Span spans[] = {
         {q, sh.qk_bytes, false},
@@ -360,12 +362,15 @@ int gdn_prefill_chunked_checkpoints(const void *q, const void *k, const void *v,
         {cu_seqlens, cu_seqlens ? (size_t)(B + 1) * 4 : 0, false},
         {initial_state, sf_in_place ? sf_in_place : sh.s0_bytes, false},  // 6
         {initial_state_indices, initial_state_indices ? (size_t)B * 4 : 0, false},
-        {final_state, sh.sf_bytes, true},                                  // 8
+        {capture_count, capacity > 0 ? (size_t)B * 4 : 0, false},
+        {state_update_active, (capacity > 0 && state_update_active) ? 4u : 0u, false},
+        {final_state, sh.sf_bytes, true},                                  // 10
         {out, sh.v_bytes, true},
         {workspace, need, true},
         {checkpoints, ck_bytes, true},
+        {state_update, su_bytes, true},
     };
-    st = check_alias(spans, (int)(sizeof(spans) / sizeof(spans[0])), 6, 8);
+    st = check_alias(spans, (int)(sizeof(spans) / sizeof(spans[0])), 6, 10);
     if (st != GDN_OK) return st;
     if (B == 0) return GDN_OK;
 
@@ -379,10 +384,62 @@ int gdn_prefill_chunked_checkpoints(const void *q, const void *k, const void *v,
     p.ws = workspace; p.ws_bytes = workspace_bytes;
     p.ckpt = checkpoint_capacity > 0 ? checkpoints : nullptr;
     p.ckpt_cap = checkpoint_capacity; p.ckpt_every = checkpoint_interval;
+    p.capacity = capacity;
+    p.capture_count = capacity > 0 ? capture_count : nullptr;
+    p.active = capacity > 0 ? state_update_active : nullptr;
+    p.su = capacity > 0 ? state_update : nullptr;
     if (error_word(&p.err) != cudaSuccess) return GDN_ERR_CUDA;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     const cudaError_t e = use_tc ? launch_prefill_tc(p, s) : launch_prefill_simt(p, s);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_prefill_chunked(const void *q, const void *k, const void *v, const void *alpha,
+                        const void *beta, const int32_t *cu_seqlens, const float *initial_state,
+                        const int32_t *initial_state_indices, int num_initial_states,
+                        float *final_state, void *out, int B, int T, int Hq, int Hk, int Hv,
+                        int dk, int dv, int chunk, float scale, int dtype_qkv, int dtype_gate,
+                        void *workspace, size_t workspace_bytes, void *stream) {
+    return prefill_call(q, k, v, alpha, beta, cu_seqlens, initial_state, initial_state_indices,
+                        num_initial_states, final_state, out, B, T, Hq, Hk, Hv, dk, dv, chunk,
+                        scale, dtype_qkv, dtype_gate, nullptr, 0, 1, 0, nullptr, nullptr, nullptr,
+                        workspace, workspace_bytes, stream);
+}
+
+int gdn_prefill_chunked_checkpoints(const void *q, const void *k, const void *v,
+                                    const void *alpha, const void *beta,
+                                    const int32_t *cu_seqlens, const float *initial_state,
+                                    const int32_t *initial_state_indices, int num_initial_states,
+                                    float *final_state, void *out, int B, int T, int Hq, int Hk,
+                                    int Hv, int dk, int dv, int chunk, float scale, int dtype_qkv,
+                                    int dtype_gate, float *checkpoints, int checkpoint_capacity,
+                                    int checkpoint_interval, void *workspace,
+                                    size_t workspace_bytes, void *stream) {
+    return prefill_call(q, k, v, alpha, beta, cu_seqlens, initial_state, initial_state_indices,
+                        num_initial_states, final_state, out, B, T, Hq, Hk, Hv, dk, dv, chunk,
+                        scale, dtype_qkv, dtype_gate, checkpoints, checkpoint_capacity,
+                        checkpoint_interval, 0, nullptr, nullptr, nullptr, workspace,
+                        workspace_bytes, stream);
+}
+
+int gdn_prefill_chunked_capture(const void *q, const void *k, const void *v, const void *alpha,
+                                const void *beta, const int32_t *cu_seqlens,
+                                const float *initial_state, const int32_t *initial_state_indices,
+                                int num_initial_states, float *final_state, void *out, int B, int T,
+                                int Hq, int Hk, int Hv, int dk, int dv, int chunk, float scale,
+                                int dtype_qkv, int dtype_gate, int state_update_capacity,
+                                const int32_t *capture_count, const int32_t *state_update_active,
+                                float *state_update, void *workspace, size_t workspace_bytes,
+                                void *stream) {
+    return prefill_call(q, k, v, alpha, beta, cu_seqlens, initial_state, initial_state_indices,
+                        num_initial_states, final_state, out, B, T, Hq, Hk, Hv, dk, dv, chunk,
+                        scale, dtype_qkv, dtype_gate, nullptr, 0, 1, state_update_capacity,
+                        capture_count, state_update_active, state_update, workspace,
+                        workspace_bytes, stream);
 }
 
 int gdn_device_errors(void *stream, uint32_t *flags) {

@@ -70,8 +70,35 @@ struct PrefillParams {
     // boundary lies inside the row.  Layout [B, ckpt_cap, Hv, dv, dk].
     float *ckpt;
     int ckpt_cap, ckpt_every;
+    // Compact capture as on the recurrent path (capacity 0: none): tokens
+    // t < n_b of row b write decay, shared key and delta into slot t; while
+    // inactive the whole [B, capacity, slot] buffer is zeroed instead.
+    int capacity;
+    const int32_t *capture_count;
+    const int32_t *active;
+    float *su;
     uint32_t *err;
 };
+
+// Captured tokens of row b (row length len): n_b = clamp(count, 0, min(capacity, len)),
+// 0 when capture is off or inactive.
+__device__ __forceinline__ int prefill_ncap(const PrefillParams &p, int b, int len) {
+    if (p.capacity <= 0 || (p.active != nullptr && *p.active == 0)) return 0;
+    const int c = p.capture_count[b];
+    const int lim = p.capacity < len ? p.capacity : len;
+    return c < 0 ? 0 : (c > lim ? lim : c);
+}
+
+// Inactive capture: CTA `cta` of `ncta` zeroes its share of the whole buffer.
+__device__ __forceinline__ void prefill_capture_clear(const PrefillParams &p, long slot, long cta, long ncta,
+                                                      int tid, int nthreads) {
+    if (p.capacity <= 0 || p.active == nullptr || *p.active != 0) return;
+    const long total = (long)p.B * p.capacity * slot;
+    const long per = (total + ncta - 1) / ncta;
+    const long e0 = cta * per;
+    const long e1 = (e0 + per < total) ? e0 + per : total;
+    for (long e = e0 + tid; e < e1; e += nthreads) p.su[e] = 0.0f;
+}
 
 // Checkpoint slot written at the end of chunk cc (0-based) of a row of len
 // tokens, or -1.

@@ -16,7 +16,10 @@
 //   O       = diag(gamma) Q S0^T + P Delta
 //   S_end   = gamma_n S0 + Delta^T diag(e^{g_n - g}) K
 // S_end of a chunk that ends on a requested boundary is also written out as a
-// checkpoint (the state after that many tokens of the row).
+// checkpoint (the state after that many tokens of the row).  With capture on,
+// the rows of Delta are the tokens' deltas (the delta rule's delta, formed
+// with the decayed state), so the first n_b tokens' decay, key and delta go to
+// the capture buffer exactly as on the recurrent path.
 // (the UT/WY form; Delta equals U - W S0^T with U = T diag(beta) V and
 // W = T diag(beta gamma) K).  A ragged last chunk is padded with identity
 // tokens (k = q = v = 0, alpha = 1, beta = 0), which leave S unchanged and
@@ -69,6 +72,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(const Prefill
     const TQ *vb = reinterpret_cast<const TQ *>(p.v);
     TQ *ob = reinterpret_cast<TQ *>(p.out);
     const float scale = p.scale;
+
+    const long slot = (long)Hv + (long)Hk * DK + (long)Hv * dv;
+    prefill_capture_clear(p, slot, ((long)b * gridDim.y + h) * gridDim.x + tile,
+                          (long)gridDim.x * gridDim.y * gridDim.z, tid, kThreads);
+    const int ncap = prefill_ncap(p, b, Tb);
 
     const float *s0 = initial_state_ptr(p.s0, p.s0_idx, p.n_s0, b, h, Hv, dv, DK, p.err);
     for (int e = tid; e < kDVT * DK / 4; e += kThreads) {
@@ -201,6 +209,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(const Prefill
             }
         }
         __syncthreads();
+
+        // ---- 4b. capture: delta of the tile's rows, decay and shared key -----
+        if (c0 < ncap) {
+            const int nc = (ncap - c0 < n) ? (ncap - c0) : n;
+            float *su0 = p.su + ((long)b * p.capacity + c0) * slot;
+            for (int e = tid; e < nc * kDVT; e += kThreads) {
+                const int t = e / kDVT, i = e % kDVT;
+                su0[t * slot + Hv + (long)Hk * DK + (long)h * dv + row0 + i] = Vs[t * DS + i];
+            }
+            if (tile == 0) {
+                for (int t = tid; t < nc; t += kThreads)
+                    su0[t * slot + h] = ld_gate(p.alpha, (tok0 + c0 + t) * Hv + h, p.dt_gate);
+                if (h % (Hv / Hk) == 0)
+                    for (int e = tid; e < nc * DK; e += kThreads) {
+                        const int t = e / DK, j = e % DK;
+                        su0[t * slot + Hv + (long)hk * DK + j] = Ks[t * KS + j];
+                    }
+            }
+        }
 
         // ---- 5a. outputs O = Os + P Delta -----------------------------------
         for (int e = tid; e < C * kDVT; e += kThreads) {

@@ -36,7 +36,10 @@
 // ahead; the output MMA (P' Delta) is committed separately so the state
 // update never waits for it, and the next chunk's first MMA is issued as soon
 // as the state image is written.  At a requested chunk boundary the fp32
-// state in the registers is also streamed out as a checkpoint.
+// state in the registers is also streamed out as a checkpoint.  Capture: the
+// rows of Delta are the tokens' deltas, so the carry phase writes the first
+// n_b tokens' deltas and phase A their decay and shared key (and clears the
+// whole buffer while capture is inactive).
 //
 // Ragged chunks: tokens t >= n get alpha = 1 and beta = 0, which makes their
 // rows of T the identity rows and their U, W, Delta rows zero, so whatever the
@@ -241,7 +244,9 @@ __device__ __forceinline__ void blocked_unit_lower_inverse(const float *At, floa
     }
 }
 
-template <typename E>
+// XO: the call also writes capture or checkpoints (a separate instance, so
+// that the plain prefill carries none of that code).
+template <typename E, bool XO>
 __global__ void __launch_bounds__(kIntraThreads, 3)
 prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap mq,
                      const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv) {
@@ -293,10 +298,32 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
         tma_load_3d(sKQ + 8192, &mq, 0, hk, (int)tok0, bar_ld);
         tma_load_3d(sKQ + 24576, &mq, 64, hk, (int)tok0, bar_ld);
     }
+    // capture: clear the whole buffer when inactive (every CTA a share), else
+    // this chunk's captured tokens' decay and (once per key head) shared key;
+    // their deltas come from the carry phase
+    const long su_slot = (long)Hv + (long)Hk * D + (long)Hv * D;
+    int ncap = 0;
+    float *su0 = nullptr;
+    if constexpr (XO) {
+        prefill_capture_clear(p, su_slot, (long)blockIdx.y * gridDim.x + blockIdx.x,
+                              (long)gridDim.x * gridDim.y, tid, kIntraThreads);
+        ncap = prefill_ncap(p, b, len) - c * C;
+        if (ncap > 0) su0 = p.su + ((long)b * p.capacity + (long)c * C) * su_slot;
+    }
     if (tid < C) {
         const long gi = (tok0 + tid) * Hv + h;
-        vg[tid] = (tid < n) ? logf(ld_gate(p.alpha, gi, p.dt_gate)) : 0.f;
+        const float a = (tid < n) ? ld_gate(p.alpha, gi, p.dt_gate) : 1.f;
+        vg[tid] = (tid < n) ? logf(a) : 0.f;
         vbeta[tid] = (tid < n) ? ld_gate(p.beta, gi, p.dt_gate) : 0.f;
+        if (tid < ncap) su0[tid * su_slot + h] = a;
+    }
+    if (ncap > 0 && h % (Hv / Hk) == 0) {
+        const E *kg = reinterpret_cast<const E *>(p.k);
+        const int nk = ncap < n ? ncap : n;
+        for (int e = tid; e < nk * D; e += kIntraThreads) {
+            const int t = e / D, j = e % D;
+            su0[t * su_slot + Hv + (long)hk * D + j] = ld_f(kg + ((tok0 + t) * Hk + hk) * D + j);
+        }
     }
     fence_before_sync();
     __syncthreads();
@@ -501,7 +528,7 @@ constexpr int kBarThreads = (kCarryComputeWarps + 1) * 32;  // compute warps + i
 constexpr uint32_t kBarDelta = 1;  // named barrier: Delta images written (all warps)
 constexpr uint32_t kBarState = 2;  // named barrier: S image written (all warps)
 
-template <typename E>
+template <typename E, bool XO>
 __global__ void __launch_bounds__(kCarryThreads, 1)
 prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap mq,
                      const __grid_constant__ CUtensorMap mk) {
@@ -523,6 +550,8 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     int len;
     row_range(p.cu_seqlens, b, p.T, rtok0, len);
     const int nc = n_chunks(len);
+    const long su_slot = (long)Hv + (long)Hk * D + (long)Hv * D;
+    const int ncap = XO ? prefill_ncap(p, b, len) : 0;
     const uint8_t *rec0 = reinterpret_cast<const uint8_t *>(p.ws) +
                           (size_t)chunk_base(p.cu_seqlens, p.B, p.T, b) * Hv * REC_BYTES +
                           (size_t)h * REC_BYTES;
@@ -686,6 +715,11 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
                     float ws[16];
                     tmem_ld16(lane_base + d1 + c0, ws);
                     const uint8_t *su = st + ST_U;
+                    // captured tokens: Delta's row t is token t's delta
+                    float *cap = (cc * C + t < ncap)
+                                     ? p.su + ((size_t)b * p.capacity + cc * C + t) * su_slot + Hv + (size_t)Hk * D +
+                                           (size_t)h * D + i0 + c0
+                                     : nullptr;
 #pragma unroll
                     for (int q8 = 0; q8 < 2; ++q8) {
                         float u[8], dd[8], dw[8];
@@ -697,6 +731,9 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
                         }
                         *reinterpret_cast<uint4 *>(sDd + sw128_chunk(t, 2 * half + q8)) = pack8<E>(dd);
                         *reinterpret_cast<uint4 *>(sDw + sw128_chunk(t, 2 * half + q8)) = pack8<E>(dw);
+                        if (cap != nullptr)
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) cap[8 * q8 + e] = dd[e];
                     }
                     fence_proxy_async();
                 }
@@ -718,7 +755,7 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
                     *reinterpret_cast<uint4 *>(sS + sw128_chunk(j, 2 * half + q8)) = pack8<E>(S + 8 * q8);
                 fence_proxy_async();
                 // chunk-boundary checkpoint: the fp32 state after this chunk
-                const int ck = ckpt_slot(p, cc, len);
+                const int ck = XO ? ckpt_slot(p, cc, len) : -1;
                 if (ck >= 0) {
                     float *dst = p.ckpt + ((((size_t)b * p.ckpt_cap + ck) * Hv + h) * D + i0 + c0) * D;
 #pragma unroll
@@ -800,7 +837,7 @@ bool make_map(CUtensorMap *m, const void *ptr, int H, long total_T, bool bf16) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename E>
+template <typename E, bool XO>
 cudaError_t launch_e(const PrefillParams &p, long total_T, long max_chunks, cudaStream_t stream) {
     const bool bf = Elem<E>::kBf16;
     CUtensorMap mq, mk, mv;
@@ -811,19 +848,19 @@ cudaError_t launch_e(const PrefillParams &p, long total_T, long max_chunks, cuda
     if (total_T > 0 && (!make_map(&mq, p.q, p.Hk, total_T, bf) || !make_map(&mk, p.k, p.Hk, total_T, bf) ||
                         !make_map(&mv, p.v, p.Hv, total_T, bf)))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(prefill_intra_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(prefill_intra_kernel<E, XO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)A_SMEM);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(prefill_carry_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)B_SMEM);
+    e = cudaFuncSetAttribute(prefill_carry_kernel<E, XO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)B_SMEM);
     if (e != cudaSuccess) return e;
     if (max_chunks > 0) {
         dim3 ga((unsigned)max_chunks, p.Hv);
-        prefill_intra_kernel<E><<<ga, kIntraThreads, A_SMEM, stream>>>(p, mq, mk, mv);
+        prefill_intra_kernel<E, XO><<<ga, kIntraThreads, A_SMEM, stream>>>(p, mq, mk, mv);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     dim3 gb(D / DVT, p.Hv, p.B);
-    prefill_carry_kernel<E><<<gb, kCarryThreads, B_SMEM, stream>>>(p, mq, mk);
+    prefill_carry_kernel<E, XO><<<gb, kCarryThreads, B_SMEM, stream>>>(p, mq, mk);
     return cudaGetLastError();
 }
 
@@ -845,8 +882,11 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t stream) {
     const bool varlen = p.cu_seqlens != nullptr;
     const long total_T = varlen ? (long)p.T : (long)p.B * p.T;
     const long mc = max_chunks_of(p.B, p.T, varlen);
-    if (p.dt_qkv == GDN_BF16) return launch_e<__nv_bfloat16>(p, total_T, mc, stream);
-    return launch_e<__half>(p, total_T, mc, stream);
+    const bool xo = p.ckpt != nullptr || p.capacity > 0;
+    if (p.dt_qkv == GDN_BF16)
+        return xo ? launch_e<__nv_bfloat16, true>(p, total_T, mc, stream)
+                  : launch_e<__nv_bfloat16, false>(p, total_T, mc, stream);
+    return xo ? launch_e<__half, true>(p, total_T, mc, stream) : launch_e<__half, false>(p, total_T, mc, stream);
 }
 
 }  // namespace gdn

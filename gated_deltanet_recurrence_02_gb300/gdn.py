@@ -51,6 +51,9 @@ def lib() -> ctypes.CDLL:
     L.gdn_prefill_chunked_checkpoints.argtypes = ([vp] * 8 + [i, vp, vp] + [i] * 8 + [f, i, i]
                                                   + [vp, i, i, vp, sz, vp])
     L.gdn_prefill_chunked_checkpoints.restype = i
+    L.gdn_prefill_chunked_capture.argtypes = ([vp] * 8 + [i, vp, vp] + [i] * 8 + [f, i, i]
+                                              + [i, vp, vp, vp, vp, sz, vp])
+    L.gdn_prefill_chunked_capture.restype = i
     L.gdn_recurrent_capture.argtypes = ([vp] * 8 + [i, vp, vp] + [i] * 7 + [f, i, i]
                                         + [i, vp, vp, vp, vp])
     L.gdn_recurrent_capture.restype = i
@@ -171,6 +174,38 @@ def gdn_prefill_chunked_checkpoints(q, k, v, alpha, beta, *, B: int, checkpoint_
         int(checkpoint_interval), _p(workspace), ws_bytes, _stream(stream))
     _check(st, "gdn_prefill_chunked_checkpoints")
     return out, final_state, checkpoints
+
+
+def gdn_prefill_chunked_capture(q, k, v, alpha, beta, *, B: int, state_update_capacity: int,
+                                capture_count, T: Optional[int] = None, cu_seqlens=None,
+                                initial_state=None, initial_state_indices=None,
+                                final_state=None, out=None, state_update_active=None,
+                                state_update=None, chunk: int = 64, scale: float = 1.0,
+                                workspace=None, want_final_state: bool = True, stream=None):
+    """Chunked prefill with the compact capture of gdn_recurrent_capture.
+    Returns (out, final_state, state_update)."""
+    T, Hk, dk, Hv, dv = _dims(q, v, B, T, cu_seqlens)
+    if out is None:
+        out = torch.empty_like(v)
+    if final_state is None and want_final_state:
+        final_state = torch.empty((B, Hv, dv, dk), dtype=torch.float32, device=v.device)
+    cap = int(state_update_capacity)
+    if cap > 0 and state_update is None:
+        state_update = torch.empty((B, cap, slot_width(Hk, Hv, dk, dv)),
+                                   dtype=torch.float32, device=v.device)
+    n0 = initial_state.shape[0] if initial_state is not None else 0
+    need = gdn_prefill_workspace_size(B, T, Hk, Hv, dk, dv, chunk, q.dtype,
+                                      varlen=cu_seqlens is not None)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=v.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().gdn_prefill_chunked_capture(
+        _p(q), _p(k), _p(v), _p(alpha), _p(beta), _p(cu_seqlens), _p(initial_state),
+        _p(initial_state_indices), n0, _p(final_state), _p(out), B, T, Hk, Hk, Hv,
+        dk, dv, chunk, scale, _DT[q.dtype], _DT[alpha.dtype], cap, _p(capture_count),
+        _p(state_update_active), _p(state_update), _p(workspace), ws_bytes, _stream(stream))
+    _check(st, "gdn_prefill_chunked_capture")
+    return out, final_state, state_update
 
 
 def gdn_recurrent_capture(q, k, v, alpha, beta, *, B: int, T: Optional[int] = None,

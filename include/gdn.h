@@ -164,6 +164,29 @@ GDN_API int gdn_prefill_chunked_checkpoints(const void *q, const void *k, const 
                                             void *stream);
 
 /*
+ * gdn_prefill_chunked_capture -- gdn_prefill_chunked that also emits the
+ * compact state-update capture of gdn_recurrent_capture (same arguments, same
+ * slot layout, same clamp, same inactive behaviour).  The chunked form's
+ * Delta rows are the tokens' deltas (the delta rule's delta, formed with the
+ * decayed state), so the chunked path can emit them too; on the page the
+ * chunked path emits none and capture forces the recurrent path [P3
+ * "Changes"].  Accuracy of the captured deltas is that of the path: fp32
+ * arithmetic on the CUDA-core path; on the tensor-core path (16-bit
+ * operands) they carry the same relative error as its outputs.
+ */
+GDN_API int gdn_prefill_chunked_capture(const void *q, const void *k, const void *v,
+                                        const void *alpha, const void *beta,
+                                        const int32_t *cu_seqlens, const float *initial_state,
+                                        const int32_t *initial_state_indices,
+                                        int num_initial_states, float *final_state, void *out,
+                                        int B, int T, int Hq, int Hk, int Hv, int dk, int dv,
+                                        int chunk, float scale, int dtype_qkv, int dtype_gate,
+                                        int state_update_capacity, const int32_t *capture_count,
+                                        const int32_t *state_update_active,
+                                        float *state_update, void *workspace,
+                                        size_t workspace_bytes, void *stream);
+
+/*
  * gdn_recurrent_capture -- per-token recurrent (decode / verify) path with
  * compact state-update capture [P3].  Arguments shared with
  * gdn_prefill_chunked mean the same (alpha = 0 is allowed here).

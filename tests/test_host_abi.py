@@ -88,6 +88,19 @@ def prc(L, **kw):
         a["wsb"], None)
 
 
+def pcap(L, **kw):
+    a = dict(q=A, k=A + GiB, v=A + 2 * GiB, alpha=A + 3 * GiB, beta=A + 4 * GiB, cu=None,
+             s0=A + 5 * GiB, idx=None, n0=1, sf=A + 6 * GiB, out=A + 7 * GiB, B=1, T=100,
+             Hq=16, Hk=16, Hv=32, dk=128, dv=128, chunk=64, scale=1.0, dtq=2, dtg=0,
+             cap=4, cc=A + 9 * GiB, act=None, su=A + 10 * GiB, ws=A + 8 * GiB, wsb=1 << 30)
+    a.update(kw)
+    return L.gdn_prefill_chunked_capture(
+        a["q"], a["k"], a["v"], a["alpha"], a["beta"], a["cu"], a["s0"], a["idx"], a["n0"],
+        a["sf"], a["out"], a["B"], a["T"], a["Hq"], a["Hk"], a["Hv"], a["dk"], a["dv"],
+        a["chunk"], a["scale"], a["dtq"], a["dtg"], a["cap"], a["cc"], a["act"], a["su"],
+        a["ws"], a["wsb"], None)
+
+
 def rv(L, **kw):
     a = dict(q=A, k=A + GiB, v=A + 2 * GiB, alpha=A + 3 * GiB, beta=A + 4 * GiB, cu=None,
              si=A + 5 * GiB, so=A + 5 * GiB, psu=A + 6 * GiB, pcap=4, acc=A + 7 * GiB,
@@ -196,6 +209,25 @@ def test_prefill_checkpoints_rejects(L, kw, code):
 def test_prefill_checkpoints_empty_and_without_slots(L):
     assert prc(L, B=0, T=0) == 0
     assert prc(L, B=0, T=0, ck=None, cap=0) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(cap=-1), INVALID),
+    (dict(cc=None), INVALID),
+    (dict(su=None), INVALID),
+    (dict(su=A + 10 * GiB + 4), ALIGN),
+    (dict(cc=A + 9 * GiB + 2), ALIGN),
+    (dict(su=A + 7 * GiB + 256), ALIAS),     # capture over out
+    (dict(su=A + 8 * GiB), ALIAS),           # capture over the workspace
+    (dict(chunk=48), UNSUP),
+])
+def test_prefill_capture_rejects(L, kw, code):
+    assert pcap(L, **kw) == code
+
+
+def test_prefill_capture_empty(L):
+    assert pcap(L, B=0, T=0) == 0
+    assert pcap(L, B=0, T=0, cap=0, cc=None, su=None) == 0
 
 
 def test_replay_verify_accepts_plain_verify_and_no_replay_buffers(L):
