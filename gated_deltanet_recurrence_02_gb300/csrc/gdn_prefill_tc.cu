@@ -10,7 +10,8 @@
 //   A[t][i] = beta_t e^{g_t - g_i} k_t.k_i (i < t),   T = (I + A)^{-1}
 //   U = T diag(beta) V,   W = T diag(beta gamma) K,   P'[t][i] = e^{g_t - g_i} q_t.k_i (i <= t)
 //   Delta = U - W S0^T
-//   O     = diag(gamma) Q S0^T + P' Delta
+//   O     = diag(gamma) Q S0^T + P' Delta   (Q: scale * q; the scale is folded into
+//                                           P' and into the gamma of the output)
 //   S_end = gamma_last S0 + Delta^T diag(w) K
 //
 // Phase A (prefill_intra_kernel, one CTA per (chunk, value head), all chunks in
@@ -362,7 +363,8 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
         vg[lane + 32] = x1;
         vgam[lane] = g0; vgam[lane + 32] = g1;
         float *rv = reinterpret_cast<float *>(rec + REC_VEC);
-        rv[lane] = g0; rv[lane + 32] = g1; rv[64 + lane] = w0; rv[96 + lane] = w1;
+        // the carry phase uses gamma only for the output gamma (scale q) S^T
+        rv[lane] = p.scale * g0; rv[lane + 32] = p.scale * g1; rv[64 + lane] = w0; rv[96 + lane] = w1;
         if (lane == 0) rv[128] = expf(glast);
     }
     __syncthreads();
@@ -389,9 +391,9 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
                 At[i * LD + t] = (i < t) ? bt * __expf(gt - vg[i]) * v[ii] : 0.f;
             }
         } else {
-            // P'[t][i] = e^{g_t - g_i} q_t.k_i (i <= t), image straight to the workspace
+            // P'[t][i] = e^{g_t - g_i} (scale q_t).k_i (i <= t), image straight to the workspace
             const int t = 32 * (quarter - 2) + lane;
-            const float gt = vg[t];
+            const float gt = vg[t], sc = p.scale;
             uint8_t *dst = rec + REC_P;
             float v[32];
             tmem_ld32(lane_base + 32 * half, v);
@@ -401,7 +403,7 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int i = 32 * half + 8 * q8 + e;
-                    pv[e] = (i <= t) ? __expf(gt - vg[i]) * v[8 * q8 + e] : 0.f;
+                    pv[e] = (i <= t) ? __expf(gt - vg[i]) * (sc * v[8 * q8 + e]) : 0.f;
                 }
                 *reinterpret_cast<uint4 *>(dst + sw128_chunk(t, 4 * half + q8)) = pack8<E>(pv);
             }

@@ -368,3 +368,32 @@ def test_bad_snapshot_index_sets_flag(gdn):
     flags = gdn.gdn_device_errors()
     assert flags & gdn.GDN_DEVERR_BAD_INDEX
     assert gdn.gdn_device_errors() == 0
+
+
+# ------------------------------------------------------------- query scale
+
+@pytest.mark.parametrize("path", ["tensor_core_prefill", "cuda_core_prefill", "recurrent"])
+def test_query_scale_every_path(gdn, oracle_mod, path):
+    """`scale` multiplies q on every path (the workloads pass 1.0 because the
+    generator already scales q, so this is the only test of it): outputs
+    scale with it, the state does not depend on it."""
+    from gated_deltanet_recurrence_02_gb300.inputs import make_inputs
+    d, dt, chunk = (128, "bf16", 64) if path == "tensor_core_prefill" else (32, "f32", 16)
+    x = make_inputs(1400, lengths=[70, 130], Hk=2, Hv=4, dk=d, dv=d, dtype_qkv=dt, dtype_gate=dt)
+    g = to_dev(x)
+    sc = 0.37
+    if path == "recurrent":
+        out, fs, _ = gdn.gdn_recurrent_capture(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=2,
+                                               cu_seqlens=g["cu_seqlens"],
+                                               initial_state=g["initial_state"], scale=sc)
+    else:
+        out, fs = gdn.gdn_prefill_chunked(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=2,
+                                          cu_seqlens=g["cu_seqlens"],
+                                          initial_state=g["initial_state"], chunk=chunk, scale=sc)
+    torch.cuda.synchronize()
+    ro, rS, _ = oracle_mod.recurrent(x.q, x.k, x.v, x.alpha, x.beta, B=2, Hk=2, Hv=4, dk=d, dv=d,
+                                     cu_seqlens=x.cu_seqlens, initial_state=x.initial_state,
+                                     scale=sc, threads=THREADS)
+    tol = TOL[x.q.dtype]
+    assert rel(out, ro) < tol
+    assert rel(fs, rS) < tol
