@@ -267,6 +267,26 @@ def replay_verify(q, k, v, alpha, beta, *, B, Hk, Hv, dk, dv, T=None,
     return o, S, S_final, su
 
 
+def front_end(q, k, alpha, beta, *, qk_l2norm=False, alpha_log=False,
+              beta_logit=False, eps=1e-6):
+    """The layer's input conventions ("adapting layouts, gate/scaling
+    conventions", executorch issue 23097, work list), applied in fp64 to
+    give the recurrence's own inputs: with ``qk_l2norm`` q and k are
+    L2-normalised per head, x / sqrt(sum x^2 + eps); with ``alpha_log``
+    alpha holds the log-decay g and the decay is e^g; with ``beta_logit``
+    beta holds logits and the write strength is 1 / (1 + e^-x).  Returns
+    (q, k, alpha, beta) in fp64."""
+    q, k, alpha, beta = (f64(x) for x in (q, k, alpha, beta))
+    if qk_l2norm:
+        q = q / np.sqrt(np.sum(q * q, axis=-1, keepdims=True) + eps)
+        k = k / np.sqrt(np.sum(k * k, axis=-1, keepdims=True) + eps)
+    if alpha_log:
+        alpha = np.exp(alpha)
+    if beta_logit:
+        beta = 1.0 / (1.0 + np.exp(-beta))
+    return q, k, alpha, beta
+
+
 def _gather_states(initial_state, indices, B, Hv, dv, dk):
     if initial_state is None:
         return np.zeros((B, Hv, dv, dk))

@@ -308,3 +308,47 @@ def test_prefix_checkpoints_match_the_chunked_form_and_resume(oracle_mod):
                                                T=cu[r + 1] - t1, initial_state=ck[r, j][None],
                                                **one)
             assert _rel(S_res[0], S_fin[r]) < 1e-12, (r, j)
+
+
+# --- input conventions (front end) -----------------------------------------
+
+def test_front_end_closed_forms(oracle_mod):
+    """Normalised vectors have norm sqrt(s / (s + eps)), s = |x|^2; the log-
+    decay round-trips; sigmoid(0) = 1/2 and sigmoid(x) + sigmoid(-x) = 1."""
+    rng = np.random.default_rng(80)
+    q = rng.standard_normal((5, 2, 7)) * 3.0
+    k = rng.standard_normal((5, 2, 7)) * 0.4
+    a = rng.uniform(0.6, 1.0, size=(5, 3))
+    x = rng.standard_normal((5, 3))
+    qn, kn, an, bn = oracle_mod.front_end(q, k, np.log(a), x, qk_l2norm=True, alpha_log=True,
+                                          beta_logit=True)
+    for raw, got in ((q, qn), (k, kn)):
+        s = np.sum(raw * raw, axis=-1)
+        assert np.allclose(np.linalg.norm(got, axis=-1), np.sqrt(s / (s + 1e-6)), rtol=1e-14)
+        assert np.allclose(got / np.linalg.norm(got, axis=-1, keepdims=True),
+                           raw / np.linalg.norm(raw, axis=-1, keepdims=True), rtol=1e-14)
+    assert np.allclose(an, a, rtol=1e-15)
+    _, _, _, b0 = oracle_mod.front_end(q, k, a, np.zeros((5, 3)), beta_logit=True)
+    assert np.all(b0 == 0.5)
+    _, _, _, bneg = oracle_mod.front_end(q, k, a, -x, beta_logit=True)
+    assert np.allclose(bn + bneg, 1.0, rtol=1e-15)
+    # without flags the inputs pass through unchanged
+    q2, k2, a2, b2 = oracle_mod.front_end(q, k, a, x)
+    assert np.array_equal(q2, q) and np.array_equal(a2, a) and np.array_equal(b2, x)
+
+
+def test_front_end_composes_with_the_recurrence(oracle_mod):
+    """Raw inputs in the layer's conventions -- q and k scaled by arbitrary
+    per-token magnitudes, alpha as log-decay, beta as logits -- give, through
+    the front end, the recurrence of the normalised inputs (to the eps effect)."""
+    rng = np.random.default_rng(81)
+    T, Hk, Hv, dk, dv = 9, 1, 2, 6, 4
+    q, k, v, a, b, S0 = _rand_case(rng, T, Hk, Hv, dk, dv)
+    mq = rng.uniform(0.5, 2.0, size=(T, Hk, 1))
+    mk = rng.uniform(0.5, 2.0, size=(T, Hk, 1))
+    dims = dict(B=1, Hk=Hk, Hv=Hv, dk=dk, dv=dv, T=T, initial_state=S0)
+    o_ref, S_ref, _ = oracle_mod.recurrent(q, k, v, a, b, **dims)
+    qf, kf, af, bf = oracle_mod.front_end(q * mq, k * mk, np.log(a), np.log(b / (1 - b)),
+                                          qk_l2norm=True, alpha_log=True, beta_logit=True)
+    o, S, _ = oracle_mod.recurrent(qf, kf, v, af, bf, **dims)
+    assert _rel(o, o_ref) < 1e-5 and _rel(S, S_ref) < 1e-5
