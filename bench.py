@@ -365,6 +365,7 @@ def run_ours(args, rank, world, local_rank):
     unfused = run_verify_unfused(gdn, stream, gv, su_prev, v_acc_d, v_full, S_ver, d)
     ckpt = run_prefill_variant(gdn, stream, gp, p_out, p_fs, ws, flush, "checkpoints")
     pcap = run_prefill_variant(gdn, stream, gp, p_out, p_fs, ws, flush, "capture")
+    fe = run_front_end(gdn, stream, q, k, v, a, bt, S, out, cc, su, gp, p_out, p_fs, ws, flush, d)
     ms_per_step = (sum(pre_ms) + sum(dec_ms) + sum(rep_ms) + sum(ver_ms)) / args.steps
     ms_per_step = reduce_scalar(ms_per_step, "max", dev)
 
@@ -458,6 +459,15 @@ def run_ours(args, rank, world, local_rank):
                 "unfused_us": unfused,
                 "speedup_vs_unfused": round(unfused["total"] / (ver_avg_s * 1e6), 3),
             },
+            "front_end": {
+                "workload": "in-kernel input conventions (q/k L2 normalisation, alpha as "
+                            "log-decay, beta as logits): decode_B256 (one T=1 call) and "
+                            "prefill_T4100, against the same calls without them",
+                "decode_us": fe["decode_us"], "decode_plain_us": round(launch_avg_s * 1e6, 2),
+                "decode_overhead": round(fe["decode_us"] / (launch_avg_s * 1e6) - 1.0, 4),
+                "prefill_us": fe["prefill_us"], "prefill_plain_us": round(pre_avg_s * 1e6, 2),
+                "prefill_overhead": round(fe["prefill_us"] / (pre_avg_s * 1e6) - 1.0, 4),
+            },
             "e2e": e2e,
             "gpu_launches": args.steps * (PREFILL_LAUNCHES + S_ + 2),
             "clocks": clocks,
@@ -534,6 +544,46 @@ def run_prefill_variant(gdn, stream, gp, out, fs, ws, flush, kind, n=10, warm=3)
     assert torch.isfinite(buf).all()
     us = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) * 1e3
     return {"us": round(us, 2), "bytes": extra}
+
+
+def run_front_end(gdn, stream, q, k, v, a, bt, S, out, cc, su, gp, p_out, p_fs, ws, flush, d,
+                  n=10, warm=3):
+    """Decode (one T=1 call on the decode state, kept finite) and prefill with
+    every input convention on (GDN_QK_L2NORM | GDN_ALPHA_LOG | GDN_BETA_LOGIT),
+    timed outside the step: mean microseconds per call.  The gates are the
+    workload's, re-expressed as log-decay and logits on the host beforehand."""
+    import torch
+    conv = gdn.GDN_QK_L2NORM | gdn.GDN_ALPHA_LOG | gdn.GDN_BETA_LOGIT
+    a_log = torch.log(a[0].float()).to(a.dtype)
+    b_logit = torch.logit(bt[0].float().clamp(1e-4, 1 - 1e-4)).to(bt.dtype)
+    S_fe = S.clone()
+    pa = torch.log(gp["alpha"].float()).to(gp["alpha"].dtype)
+    pb = torch.logit(gp["beta"].float().clamp(1e-4, 1 - 1e-4)).to(gp["beta"].dtype)
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    res = {}
+    for kind in ("decode", "prefill"):
+        ev = [[E(), E()] for _ in range(n)]
+        for i in range(warm + n):
+            if kind == "prefill":
+                flush.fill_(3)
+            e = ev[i - warm] if i >= warm else None
+            if e: e[0].record(stream)
+            if kind == "decode":
+                gdn.gdn_recurrent_capture(q[0], k[0], v[0], a_log, b_logit, B=d["B"], T=1,
+                                          initial_state=S_fe, final_state=S_fe, out=out[0],
+                                          state_update_capacity=d["cap"], capture_count=cc,
+                                          state_update=su, conventions=conv)
+            else:
+                gdn.gdn_prefill_chunked(gp["q"], gp["k"], gp["v"], pa, pb, B=1, T=PRE["T"],
+                                        initial_state=gp["initial_state"], final_state=p_fs,
+                                        out=p_out, chunk=PRE["chunk"], workspace=ws,
+                                        conventions=conv)
+            if e: e[1].record(stream)
+        torch.cuda.synchronize()
+        res[kind + "_us"] = round(statistics.mean(e[0].elapsed_time(e[1]) for e in ev) * 1e3, 2)
+    assert torch.isfinite(S_fe).all() and torch.isfinite(p_out.float()).all()
+    del S_fe
+    return res
 
 
 PREFILL_LAUNCHES = 2  # kernels one gdn_prefill_chunked call launches on this workload (tensor-core path)

@@ -69,6 +69,16 @@ int check_alias(const Span *s, int n, int allow_a, int allow_b) {
     return GDN_OK;
 }
 
+// Splits a dtype argument into the storage type and its convention bits;
+// false if it carries bits outside `allowed`.
+bool split_dtype(int code, int allowed, int *dt, int *conv) {
+    const int flags = code & ~0xFF;
+    if (flags & ~allowed) return false;
+    *dt = code & 0xFF;
+    *conv |= flags;
+    return true;
+}
+
 bool mul_ok(size_t a, size_t b, size_t *out) {
     if (a != 0 && b > SIZE_MAX / a) return false;
     *out = a * b;
@@ -144,6 +154,12 @@ int gdn_recurrent_capture(const void *q, const void *k, const void *v, const voi
                           int dtype_gate, int state_update_capacity,
                           const int32_t *capture_count, const int32_t *state_update_active,
                           float *state_update, void *stream) {
+    int conv = 0, dtq = 0, dtg = 0;
+    if (!split_dtype(dtype_qkv, GDN_QK_L2NORM, &dtq, &conv) ||
+        !split_dtype(dtype_gate, GDN_ALPHA_LOG | GDN_BETA_LOGIT, &dtg, &conv))
+        return GDN_ERR_INVALID_ARG;
+    dtype_qkv = dtq;
+    dtype_gate = dtg;
     Shapes sh;
     int st = check_common(q, k, v, alpha, beta, cu_seqlens, initial_state, initial_state_indices,
                           num_initial_states, final_state, out, B, T, Hq, Hk, Hv, dk, dv,
@@ -187,7 +203,7 @@ int gdn_recurrent_capture(const void *q, const void *k, const void *v, const voi
     p.s0 = initial_state; p.s0_idx = initial_state_indices; p.n_s0 = num_initial_states;
     p.s_final = final_state; p.out = out;
     p.B = B; p.T = T; p.Hk = Hk; p.Hv = Hv; p.dk = dk; p.dv = dv;
-    p.scale = scale; p.dt_qkv = dtype_qkv; p.dt_gate = dtype_gate;
+    p.scale = scale; p.dt_qkv = dtype_qkv; p.dt_gate = dtype_gate; p.conv = conv;
     p.capacity = cap; p.capture_count = capture_count; p.active = state_update_active;
     p.su = cap > 0 ? state_update : nullptr;
     p.rp_su = nullptr; p.rp_capacity = 0; p.rp_accepted = nullptr; p.s_commit = nullptr;
@@ -202,6 +218,12 @@ int gdn_replay_verify(const void *q, const void *k, const void *v, const void *a
                       int T, int Hq, int Hk, int Hv, int dk, int dv, float scale, int dtype_qkv,
                       int dtype_gate, int state_update_capacity, const int32_t *capture_count,
                       const int32_t *state_update_active, float *state_update, void *stream) {
+    int conv = 0, dtq = 0, dtg = 0;
+    if (!split_dtype(dtype_qkv, GDN_QK_L2NORM, &dtq, &conv) ||
+        !split_dtype(dtype_gate, GDN_ALPHA_LOG | GDN_BETA_LOGIT, &dtg, &conv))
+        return GDN_ERR_INVALID_ARG;
+    dtype_qkv = dtq;
+    dtype_gate = dtg;
     Shapes sh;
     int st = check_common(q, k, v, alpha, beta, cu_seqlens, state_in, nullptr, B, draft_final_state,
                           out, B, T, Hq, Hk, Hv, dk, dv, dtype_qkv, dtype_gate, &sh);
@@ -252,7 +274,7 @@ int gdn_replay_verify(const void *q, const void *k, const void *v, const void *a
     p.s0 = state_in; p.s0_idx = nullptr; p.n_s0 = B;
     p.s_final = draft_final_state; p.out = out;
     p.B = B; p.T = T; p.Hk = Hk; p.Hv = Hv; p.dk = dk; p.dv = dv;
-    p.scale = scale; p.dt_qkv = dtype_qkv; p.dt_gate = dtype_gate;
+    p.scale = scale; p.dt_qkv = dtype_qkv; p.dt_gate = dtype_gate; p.conv = conv;
     p.capacity = cap; p.capture_count = capture_count; p.active = state_update_active;
     p.su = cap > 0 ? state_update : nullptr;
     p.rp_su = prev_capacity > 0 ? prev_state_update : nullptr;
@@ -321,6 +343,12 @@ int prefill_call(const void *q, const void *k, const void *v, const void *alpha,
                  int checkpoint_capacity, int checkpoint_interval, int capacity,
                  const int32_t *capture_count, const int32_t *state_update_active,
                  float *state_update, void *workspace, size_t workspace_bytes, void *stream) {
+    int conv = 0, dtq = 0, dtg = 0;
+    if (!split_dtype(dtype_qkv, GDN_QK_L2NORM, &dtq, &conv) ||
+        !split_dtype(dtype_gate, GDN_ALPHA_LOG | GDN_BETA_LOGIT, &dtg, &conv))
+        return GDN_ERR_INVALID_ARG;
+    dtype_qkv = dtq;
+    dtype_gate = dtg;
     Shapes sh;
     int st = check_common(q, k, v, alpha, beta, cu_seqlens, initial_state, initial_state_indices,
                           num_initial_states, final_state, out, B, T, Hq, Hk, Hv, dk, dv,
@@ -380,7 +408,7 @@ int prefill_call(const void *q, const void *k, const void *v, const void *alpha,
     p.s0 = initial_state; p.s0_idx = initial_state_indices; p.n_s0 = num_initial_states;
     p.s_final = final_state; p.out = out;
     p.B = B; p.T = T; p.Hk = Hk; p.Hv = Hv; p.dk = dk; p.dv = dv; p.chunk = chunk;
-    p.scale = scale; p.dt_qkv = dtype_qkv; p.dt_gate = dtype_gate;
+    p.scale = scale; p.dt_qkv = dtype_qkv; p.dt_gate = dtype_gate; p.conv = conv;
     p.ws = workspace; p.ws_bytes = workspace_bytes;
     p.ckpt = checkpoint_capacity > 0 ? checkpoints : nullptr;
     p.ckpt_cap = checkpoint_capacity; p.ckpt_every = checkpoint_interval;

@@ -27,6 +27,7 @@ struct RecurrentParams {
     int B, T, Hk, Hv, dk, dv;
     float scale;
     int dt_qkv, dt_gate;
+    int conv;  // GDN_QK_L2NORM | GDN_ALPHA_LOG | GDN_BETA_LOGIT bits
     int capacity;
     const int32_t *capture_count;
     const int32_t *active;
@@ -63,6 +64,7 @@ struct PrefillParams {
     int B, T, Hk, Hv, dk, dv, chunk;
     float scale;
     int dt_qkv, dt_gate;
+    int conv;  // GDN_QK_L2NORM | GDN_ALPHA_LOG | GDN_BETA_LOGIT bits
     void *ws;
     size_t ws_bytes;
     // Chunk-boundary checkpoints (nullptr: none): slot j of row b receives the
@@ -188,6 +190,19 @@ __device__ __forceinline__ const float *initial_state_ptr(const float *s0, const
     }
     return s0 + ((src * Hv + h) * (long)dv) * dk;
 }
+
+// Input conventions: the decay and the write strength from the stored gates,
+// and the L2-normalisation factor of a q or k vector with squared norm ss.
+__device__ __forceinline__ float conv_alpha(float x, int conv) {
+    return (conv & GDN_ALPHA_LOG) ? expf(x) : x;
+}
+__device__ __forceinline__ float conv_log_alpha(float x, int conv) {
+    return (conv & GDN_ALPHA_LOG) ? x : logf(x);
+}
+__device__ __forceinline__ float conv_beta(float x, int conv) {
+    return (conv & GDN_BETA_LOGIT) ? 1.0f / (1.0f + expf(-x)) : x;
+}
+__device__ __forceinline__ float l2norm_factor(float ss) { return rsqrtf(ss + 1e-6f); }
 
 template <int W>
 __device__ __forceinline__ float group_sum(float x) {

@@ -96,7 +96,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(const Prefill
                 const long off = ((tok0 + c0 + t) * Hk + hk) * DK + j;
                 kk = ld4(kb + off);
                 qq = ld4(qb + off);
-                qq.x *= scale; qq.y *= scale; qq.z *= scale; qq.w *= scale;
+                if (!(p.conv & GDN_QK_L2NORM)) {
+                    qq.x *= scale; qq.y *= scale; qq.z *= scale; qq.w *= scale;
+                }
             }
             *reinterpret_cast<float4 *>(Ks + t * KS + j) = kk;
             *reinterpret_cast<float4 *>(Qs + t * KS + j) = qq;
@@ -107,10 +109,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(const Prefill
         }
         for (int t = tid; t < C; t += kThreads) {
             const long g = (tok0 + c0 + t) * Hv + h;
-            lg[t] = (t < n) ? logf(ld_gate(p.alpha, g, p.dt_gate)) : 0.f;
-            bt[t] = (t < n) ? ld_gate(p.beta, g, p.dt_gate) : 0.f;
+            lg[t] = (t < n) ? conv_log_alpha(ld_gate(p.alpha, g, p.dt_gate), p.conv) : 0.f;
+            bt[t] = (t < n) ? conv_beta(ld_gate(p.beta, g, p.dt_gate), p.conv) : 0.f;
         }
         __syncthreads();
+        if (p.conv & GDN_QK_L2NORM) {
+            // q and k normalised in the kernel, one warp per row; q then scaled
+            for (int r = warp; r < 2 * C; r += kThreads / 32) {
+                float *row = (r < C) ? Ks + r * KS : Qs + (r - C) * KS;
+                float ss = 0.f;
+                for (int j = lane; j < DK; j += 32) ss += row[j] * row[j];
+                ss = group_sum<32>(ss);
+                const float f = l2norm_factor(ss) * ((r < C) ? 1.f : scale);
+                for (int j = lane; j < DK; j += 32) row[j] *= f;
+            }
+            __syncthreads();
+        }
 
         // ---- 2. cumulative log decay (warp 0) ------------------------------
         if (warp == 0) {
@@ -220,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(const Prefill
             }
             if (tile == 0) {
                 for (int t = tid; t < nc; t += kThreads)
-                    su0[t * slot + h] = ld_gate(p.alpha, (tok0 + c0 + t) * Hv + h, p.dt_gate);
+                    su0[t * slot + h] = conv_alpha(ld_gate(p.alpha, (tok0 + c0 + t) * Hv + h, p.dt_gate), p.conv);
                 if (h % (Hv / Hk) == 0)
                     for (int e = tid; e < nc * DK; e += kThreads) {
                         const int t = e / DK, j = e % DK;

@@ -176,8 +176,8 @@ constexpr uint32_t A_IMG = 32768;     // [T*beta ; T*beta*gamma] bf16 image (16 
 constexpr uint32_t A_AT = A_IMG;      //   ... aliasing, before it exists, A^T fp32 [64][68]
 constexpr uint32_t A_X = A_IMG + 64 * 68 * 4;  //   and the blocked-inverse scratch, 3 x 16 x 16 fp32
 constexpr uint32_t A_T = A_X + 3 * 256 * 4;    // T fp32 [64][68]
-constexpr uint32_t A_VEC = A_T + 64 * 68 * 4;  // g, beta, gamma: 3 x 64 floats (1 KB reserved)
-constexpr uint32_t A_BAR = A_VEC + 1024;
+constexpr uint32_t A_VEC = A_T + 64 * 68 * 4;  // g, beta, gamma, 1/|k|, 1/|q|: 5 x 64 floats
+constexpr uint32_t A_BAR = A_VEC + 1536;
 constexpr uint32_t A_SMEM = A_BAR + 64 + 1024;  // + alignment slack
 constexpr uint32_t A_TMEM_COLS = 128;
 constexpr int LD = 68;                           // fp32 row stride of A^T and T
@@ -245,9 +245,12 @@ __device__ __forceinline__ void blocked_unit_lower_inverse(const float *At, floa
     }
 }
 
-// XO: the call also writes capture or checkpoints (a separate instance, so
-// that the plain prefill carries none of that code).
-template <typename E, bool XO>
+// XO: the call also writes capture or checkpoints; NORM: q and k are
+// L2-normalised in the kernel.  Separate instances, so that the plain prefill
+// carries none of that code.  The norms enter as per-token scalars:
+// A gets r_t r_i, P' rq_t r_i, the W image beta gamma r, and the record's
+// gamma (output) and w (state update) rq_t and r_t, with r = 1/|k|, rq = 1/|q|.
+template <typename E, bool XO, bool NORM>
 __global__ void __launch_bounds__(kIntraThreads, 3)
 prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap mq,
                      const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv) {
@@ -259,7 +262,7 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     float *X = reinterpret_cast<float *>(sm + A_X);
     float *sT = reinterpret_cast<float *>(sm + A_T);
     float *vg = reinterpret_cast<float *>(sm + A_VEC);
-    float *vbeta = vg + 64, *vgam = vg + 128;
+    float *vbeta = vg + 64, *vgam = vg + 128, *vkn = vg + 192, *vqn = vg + 256;
     uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + A_BAR);
     uint64_t *bar_mma = bar_ld + 1;
     uint64_t *bar_v = bar_ld + 2;
@@ -313,18 +316,10 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     }
     if (tid < C) {
         const long gi = (tok0 + tid) * Hv + h;
-        const float a = (tid < n) ? ld_gate(p.alpha, gi, p.dt_gate) : 1.f;
-        vg[tid] = (tid < n) ? logf(a) : 0.f;
-        vbeta[tid] = (tid < n) ? ld_gate(p.beta, gi, p.dt_gate) : 0.f;
-        if (tid < ncap) su0[tid * su_slot + h] = a;
-    }
-    if (ncap > 0 && h % (Hv / Hk) == 0) {
-        const E *kg = reinterpret_cast<const E *>(p.k);
-        const int nk = ncap < n ? ncap : n;
-        for (int e = tid; e < nk * D; e += kIntraThreads) {
-            const int t = e / D, j = e % D;
-            su0[t * su_slot + Hv + (long)hk * D + j] = ld_f(kg + ((tok0 + t) * Hk + hk) * D + j);
-        }
+        const float a = (tid < n) ? ld_gate(p.alpha, gi, p.dt_gate) : 0.f;
+        vg[tid] = (tid < n) ? conv_log_alpha(a, p.conv) : 0.f;
+        vbeta[tid] = (tid < n) ? conv_beta(ld_gate(p.beta, gi, p.dt_gate), p.conv) : 0.f;
+        if (tid < ncap) su0[tid * su_slot + h] = conv_alpha(a, p.conv);
     }
     fence_before_sync();
     __syncthreads();
@@ -347,8 +342,10 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
             }
             mma_commit(bar_mma);
         }
-    } else if (warp == 1) {
-        // cumulative log-decay g, gamma, w while the MMA runs
+    }
+    // warp 1: cumulative log-decay g, gamma, w while the MMA runs
+    float g0 = 0.f, g1 = 0.f, w0 = 0.f, w1 = 0.f, glast = 0.f;
+    if (warp == 1) {
         float x0 = vg[lane], x1 = vg[lane + 32];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -357,17 +354,52 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
             if (lane >= o) { x0 += y0; x1 += y1; }
         }
         x1 += __shfl_sync(0xffffffffu, x0, 31);
-        const float glast = __shfl_sync(0xffffffffu, x1, 31);
-        const float g0 = expf(x0), g1 = expf(x1), w0 = expf(glast - x0), w1 = expf(glast - x1);
+        glast = __shfl_sync(0xffffffffu, x1, 31);
+        g0 = expf(x0); g1 = expf(x1); w0 = expf(glast - x0); w1 = expf(glast - x1);
         vg[lane] = x0;
         vg[lane + 32] = x1;
         vgam[lane] = g0; vgam[lane + 32] = g1;
-        float *rv = reinterpret_cast<float *>(rec + REC_VEC);
-        // the carry phase uses gamma only for the output gamma (scale q) S^T
-        rv[lane] = p.scale * g0; rv[lane + 32] = p.scale * g1; rv[64 + lane] = w0; rv[96 + lane] = w1;
-        if (lane == 0) rv[128] = expf(glast);
+    }
+    // record: gamma for the output gamma (scale q) S^T, w for the state update
+    float *rv = reinterpret_cast<float *>(rec + REC_VEC);
+    if constexpr (NORM) {
+        // 1/|k_t| and 1/|q_t| from the staged tiles (rows 0-63 K, 64-127 Q;
+        // two threads per row, one per 64-column block), before V replaces Q
+        if (!mbar_wait(bar_ld, 0, kWaitNs)) ok = false;
+        const int r = tid >> 1, kb = tid & 1;
+        float ss = 0.f;
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) {
+            float x[8];
+            unpack8<E>(*reinterpret_cast<const uint4 *>(sKQ + kb * 16384 + sw128_chunk(r, q8)), x);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+        }
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        if (kb == 0) (r < C ? vkn[r] : vqn[r - C]) = l2norm_factor(ss);
+        __syncthreads();
+        if (warp == 1) {
+            rv[lane] = p.scale * g0 * vqn[lane]; rv[lane + 32] = p.scale * g1 * vqn[lane + 32];
+            rv[64 + lane] = w0 * vkn[lane]; rv[96 + lane] = w1 * vkn[lane + 32];
+            if (lane == 0) rv[128] = expf(glast);
+        }
+    } else {
+        if (warp == 1) {
+            rv[lane] = p.scale * g0; rv[lane + 32] = p.scale * g1; rv[64 + lane] = w0; rv[96 + lane] = w1;
+            if (lane == 0) rv[128] = expf(glast);
+        }
     }
     __syncthreads();
+    if (ncap > 0 && h % (Hv / Hk) == 0) {
+        // captured keys: the (normalised) key the recurrence used
+        const E *kg = reinterpret_cast<const E *>(p.k);
+        const int nk = ncap < n ? ncap : n;
+        for (int e = tid; e < nk * D; e += kIntraThreads) {
+            const int t = e / D, j = e % D;
+            su0[t * su_slot + Hv + (long)hk * D + j] =
+                ld_f(kg + ((tok0 + t) * Hk + hk) * D + j) * (NORM ? vkn[t] : 1.f);
+        }
+    }
     ok = ok && mbar_wait(bar_mma, 0, kWaitNs);
     fence_after_sync();
     if (ok && tid == 0) {
@@ -382,18 +414,18 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
         if (quarter < 2) {
             // A, stored transposed: At[i][t] = A[t][i] = beta_t e^{g_t - g_i} k_t.k_i  (i < t)
             const int t = 32 * quarter + lane;
-            const float gt = vg[t], bt = vbeta[t];
+            const float gt = vg[t], bt = vbeta[t] * (NORM ? vkn[t] : 1.f);
             float v[32];
             tmem_ld32(lane_base + 32 * half, v);
 #pragma unroll
             for (int ii = 0; ii < 32; ++ii) {
                 const int i = 32 * half + ii;
-                At[i * LD + t] = (i < t) ? bt * __expf(gt - vg[i]) * v[ii] : 0.f;
+                At[i * LD + t] = (i < t) ? bt * __expf(gt - vg[i]) * (NORM ? v[ii] * vkn[i] : v[ii]) : 0.f;
             }
         } else {
             // P'[t][i] = e^{g_t - g_i} (scale q_t).k_i (i <= t), image straight to the workspace
             const int t = 32 * (quarter - 2) + lane;
-            const float gt = vg[t], sc = p.scale;
+            const float gt = vg[t], sc = p.scale * (NORM ? vqn[t] : 1.f);
             uint8_t *dst = rec + REC_P;
             float v[32];
             tmem_ld32(lane_base + 32 * half, v);
@@ -403,7 +435,8 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int i = 32 * half + 8 * q8 + e;
-                    pv[e] = (i <= t) ? __expf(gt - vg[i]) * (sc * v[8 * q8 + e]) : 0.f;
+                    pv[e] = (i <= t) ? __expf(gt - vg[i]) * (sc * (NORM ? v[8 * q8 + e] * vkn[i] : v[8 * q8 + e]))
+                                     : 0.f;
                 }
                 *reinterpret_cast<uint4 *>(dst + sw128_chunk(t, 4 * half + q8)) = pack8<E>(pv);
             }
@@ -428,7 +461,7 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int s = 8 * q8 + e;
-                val[e] = sT[t * LD + s] * (which ? vbeta[s] * vgam[s] : vbeta[s]);
+                val[e] = sT[t * LD + s] * (which ? vbeta[s] * vgam[s] * (NORM ? vkn[s] : 1.f) : vbeta[s]);
             }
             *reinterpret_cast<uint4 *>(sImg + sw128_chunk(r, q8)) = pack8<E>(val);
         }
@@ -850,14 +883,14 @@ cudaError_t launch_e(const PrefillParams &p, long total_T, long max_chunks, cuda
     if (total_T > 0 && (!make_map(&mq, p.q, p.Hk, total_T, bf) || !make_map(&mk, p.k, p.Hk, total_T, bf) ||
                         !make_map(&mv, p.v, p.Hv, total_T, bf)))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(prefill_intra_kernel<E, XO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)A_SMEM);
+    auto intra = (p.conv & GDN_QK_L2NORM) ? prefill_intra_kernel<E, XO, true> : prefill_intra_kernel<E, XO, false>;
+    cudaError_t e = cudaFuncSetAttribute(intra, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)A_SMEM);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(prefill_carry_kernel<E, XO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)B_SMEM);
     if (e != cudaSuccess) return e;
     if (max_chunks > 0) {
         dim3 ga((unsigned)max_chunks, p.Hv);
-        prefill_intra_kernel<E, XO><<<ga, kIntraThreads, A_SMEM, stream>>>(p, mq, mk, mv);
+        intra<<<ga, kIntraThreads, A_SMEM, stream>>>(p, mq, mk, mv);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -191,8 +191,8 @@ recurrent_kernel(const RecurrentParams p) {
             float *sg = reinterpret_cast<float *>(st + L::oG);
             if (lane < nts) {
                 const long gi = (hd.tok0 + lane) * Hv + hd.h;
-                sg[lane] = ld_gate(p.alpha, gi, p.dt_gate);
-                sg[TS + lane] = ld_gate(p.beta, gi, p.dt_gate);
+                sg[lane] = conv_alpha(ld_gate(p.alpha, gi, p.dt_gate), p.conv);
+                sg[TS + lane] = conv_beta(ld_gate(p.beta, gi, p.dt_gate), p.conv);
             }
             if constexpr (RS > 0) {
                 // the first RS replayed slots (all loads issued, then stored)
@@ -288,8 +288,19 @@ recurrent_kernel(const RecurrentParams p) {
                 const long tok = hd.tok0 + t;
                 load_pairs<F4>(kb + (tok * Hk + hk) * DK, l8, kf);
                 load_pairs<F4>(qb + (tok * Hk + hk) * DK, l8, qf);
-                a = ld_gate(p.alpha, tok * Hv + h, p.dt_gate);
-                bt = ld_gate(p.beta, tok * Hv + h, p.dt_gate);
+                a = conv_alpha(ld_gate(p.alpha, tok * Hv + h, p.dt_gate), p.conv);
+                bt = conv_beta(ld_gate(p.beta, tok * Hv + h, p.dt_gate), p.conv);
+            }
+            if (p.conv & GDN_QK_L2NORM) {
+                // q and k normalised in the kernel (8-lane sums of squares)
+                const float nk = l2norm_factor(group_sum<kLanesPerRow>(dot_pairs<F2>(kf, kf)));
+                const float nq = l2norm_factor(group_sum<kLanesPerRow>(dot_pairs<F2>(qf, qf)));
+                const float2 rk = make_float2(nk, nk), rq = make_float2(nq, nq);
+#pragma unroll
+                for (int i = 0; i < F2; ++i) {
+                    kf[i] = __fmul2_rn(kf[i], rk);
+                    qf[i] = __fmul2_rn(qf[i], rq);
+                }
             }
         };
         // One row, one token: delta with the decayed state, the rank-1

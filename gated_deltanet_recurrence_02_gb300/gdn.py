@@ -21,6 +21,8 @@ from . import build as _build
 GDN_OK = 0
 GDN_F32, GDN_F16, GDN_BF16 = 0, 1, 2
 GDN_DEVERR_BAD_INDEX, GDN_DEVERR_TIMEOUT = 1, 2
+# input conventions (include/gdn.h): OR'd into dtype_qkv / dtype_gate
+GDN_QK_L2NORM, GDN_ALPHA_LOG, GDN_BETA_LOGIT = 0x100, 0x200, 0x400
 _DT = {torch.float32: GDN_F32, torch.float16: GDN_F16, torch.bfloat16: GDN_BF16}
 
 _lib = None
@@ -94,6 +96,13 @@ def _stream(stream) -> Optional[int]:
     return stream.cuda_stream
 
 
+def _codes(q, alpha, conventions: int):
+    """dtype_qkv and dtype_gate arguments: storage types plus the input
+    convention bits (GDN_QK_L2NORM goes with q/k, the gate bits with alpha/beta)."""
+    return (_DT[q.dtype] | (conventions & GDN_QK_L2NORM),
+            _DT[alpha.dtype] | (conventions & (GDN_ALPHA_LOG | GDN_BETA_LOGIT)))
+
+
 def _check(status: int, where: str):
     if status != GDN_OK:
         raise GdnError(status, where)
@@ -123,7 +132,7 @@ def gdn_prefill_chunked(q, k, v, alpha, beta, *, B: int, T: Optional[int] = None
                         cu_seqlens=None, initial_state=None,
                         initial_state_indices=None, final_state=None, out=None,
                         chunk: int = 64, scale: float = 1.0, workspace=None,
-                        want_final_state: bool = True, stream=None):
+                        want_final_state: bool = True, conventions: int = 0, stream=None):
     """Chunked prefill.  Returns (out, final_state)."""
     T, Hk, dk, Hv, dv = _dims(q, v, B, T, cu_seqlens)
     if out is None:
@@ -139,7 +148,7 @@ def gdn_prefill_chunked(q, k, v, alpha, beta, *, B: int, T: Optional[int] = None
     st = lib().gdn_prefill_chunked(
         _p(q), _p(k), _p(v), _p(alpha), _p(beta), _p(cu_seqlens), _p(initial_state),
         _p(initial_state_indices), n0, _p(final_state), _p(out), B, T, Hk, Hk, Hv,
-        dk, dv, chunk, scale, _DT[q.dtype], _DT[alpha.dtype], _p(workspace),
+        dk, dv, chunk, scale, *_codes(q, alpha, conventions), _p(workspace),
         ws_bytes, _stream(stream))
     _check(st, "gdn_prefill_chunked")
     return out, final_state
@@ -150,7 +159,8 @@ def gdn_prefill_chunked_checkpoints(q, k, v, alpha, beta, *, B: int, checkpoint_
                                     cu_seqlens=None, initial_state=None,
                                     initial_state_indices=None, final_state=None, out=None,
                                     checkpoints=None, chunk: int = 64, scale: float = 1.0,
-                                    workspace=None, want_final_state: bool = True, stream=None):
+                                    workspace=None, want_final_state: bool = True,
+                                    conventions: int = 0, stream=None):
     """Chunked prefill that also writes the state every checkpoint_interval
     chunks.  Returns (out, final_state, checkpoints [B, capacity, Hv, dv, dk])."""
     T, Hk, dk, Hv, dv = _dims(q, v, B, T, cu_seqlens)
@@ -170,7 +180,7 @@ def gdn_prefill_chunked_checkpoints(q, k, v, alpha, beta, *, B: int, checkpoint_
     st = lib().gdn_prefill_chunked_checkpoints(
         _p(q), _p(k), _p(v), _p(alpha), _p(beta), _p(cu_seqlens), _p(initial_state),
         _p(initial_state_indices), n0, _p(final_state), _p(out), B, T, Hk, Hk, Hv,
-        dk, dv, chunk, scale, _DT[q.dtype], _DT[alpha.dtype], _p(checkpoints), cap,
+        dk, dv, chunk, scale, *_codes(q, alpha, conventions), _p(checkpoints), cap,
         int(checkpoint_interval), _p(workspace), ws_bytes, _stream(stream))
     _check(st, "gdn_prefill_chunked_checkpoints")
     return out, final_state, checkpoints
@@ -181,7 +191,8 @@ def gdn_prefill_chunked_capture(q, k, v, alpha, beta, *, B: int, state_update_ca
                                 initial_state=None, initial_state_indices=None,
                                 final_state=None, out=None, state_update_active=None,
                                 state_update=None, chunk: int = 64, scale: float = 1.0,
-                                workspace=None, want_final_state: bool = True, stream=None):
+                                workspace=None, want_final_state: bool = True,
+                                conventions: int = 0, stream=None):
     """Chunked prefill with the compact capture of gdn_recurrent_capture.
     Returns (out, final_state, state_update)."""
     T, Hk, dk, Hv, dv = _dims(q, v, B, T, cu_seqlens)
@@ -202,7 +213,7 @@ def gdn_prefill_chunked_capture(q, k, v, alpha, beta, *, B: int, state_update_ca
     st = lib().gdn_prefill_chunked_capture(
         _p(q), _p(k), _p(v), _p(alpha), _p(beta), _p(cu_seqlens), _p(initial_state),
         _p(initial_state_indices), n0, _p(final_state), _p(out), B, T, Hk, Hk, Hv,
-        dk, dv, chunk, scale, _DT[q.dtype], _DT[alpha.dtype], cap, _p(capture_count),
+        dk, dv, chunk, scale, *_codes(q, alpha, conventions), cap, _p(capture_count),
         _p(state_update_active), _p(state_update), _p(workspace), ws_bytes, _stream(stream))
     _check(st, "gdn_prefill_chunked_capture")
     return out, final_state, state_update
@@ -214,7 +225,7 @@ def gdn_recurrent_capture(q, k, v, alpha, beta, *, B: int, T: Optional[int] = No
                           scale: float = 1.0, state_update_capacity: int = 0,
                           capture_count=None, state_update_active=None,
                           state_update=None, want_final_state: bool = True,
-                          stream=None):
+                          conventions: int = 0, stream=None):
     """Recurrent path with compact capture.  Returns (out, final_state,
     state_update).  final_state may be initial_state itself (in place)."""
     T, Hk, dk, Hv, dv = _dims(q, v, B, T, cu_seqlens)
@@ -230,7 +241,7 @@ def gdn_recurrent_capture(q, k, v, alpha, beta, *, B: int, T: Optional[int] = No
     st = lib().gdn_recurrent_capture(
         _p(q), _p(k), _p(v), _p(alpha), _p(beta), _p(cu_seqlens), _p(initial_state),
         _p(initial_state_indices), n0, _p(final_state), _p(out), B, T, Hk, Hk, Hv,
-        dk, dv, scale, _DT[q.dtype], _DT[alpha.dtype], cap, _p(capture_count),
+        dk, dv, scale, *_codes(q, alpha, conventions), cap, _p(capture_count),
         _p(state_update_active), _p(state_update), _stream(stream))
     _check(st, "gdn_recurrent_capture")
     return out, final_state, state_update
@@ -258,7 +269,7 @@ def gdn_replay_verify(q, k, v, alpha, beta, *, B: int, T: Optional[int] = None,
                       scale: float = 1.0, state_update_capacity: int = 0,
                       capture_count=None, state_update_active=None,
                       state_update=None, want_draft_final_state: bool = False,
-                      stream=None):
+                      conventions: int = 0, stream=None):
     """One speculative step: replay the accepted prefix of prev_state_update
     onto state_in, write it to state_out (state_in itself allowed), then run
     the draft tokens with capture.  Returns (out, state_out, state_update,
@@ -278,7 +289,7 @@ def gdn_replay_verify(q, k, v, alpha, beta, *, B: int, T: Optional[int] = None,
         _p(q), _p(k), _p(v), _p(alpha), _p(beta), _p(cu_seqlens), _p(state_in),
         _p(state_out), _p(prev_state_update), int(prev_capacity), _p(accepted_count),
         _p(draft_final_state), _p(out), B, T, Hk, Hk, Hv, dk, dv, scale,
-        _DT[q.dtype], _DT[alpha.dtype], cap, _p(capture_count),
+        *_codes(q, alpha, conventions), cap, _p(capture_count),
         _p(state_update_active), _p(state_update), _stream(stream))
     _check(st, "gdn_replay_verify")
     return out, state_out, state_update, draft_final_state
@@ -299,7 +310,8 @@ NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 def gdn_prefill_chunked_noalloc(q, k, v, alpha, beta, *, B: int, T: Optional[int] = None,
                                 cu_seqlens=None, initial_state=None,
                                 initial_state_indices=None, final_state, out,
-                                chunk: int = 64, scale: float = 1.0, stream=None):
+                                chunk: int = 64, scale: float = 1.0, conventions: int = 0,
+                                stream=None):
     """Chunked prefill that allocates nothing: the library's fixed device
     scratch replaces the workspace, and the caller passes `out` and
     `final_state` (None allowed for final_state only if not wanted).  For
@@ -315,6 +327,6 @@ def gdn_prefill_chunked_noalloc(q, k, v, alpha, beta, *, B: int, T: Optional[int
     n0 = initial_state.shape[0] if initial_state is not None else 0
     st = fn(_p(q), _p(k), _p(v), _p(alpha), _p(beta), _p(cu_seqlens), _p(initial_state),
             _p(initial_state_indices), n0, _p(final_state), _p(out), B, T, Hk, Hk, Hv, dk, dv,
-            chunk, scale, _DT[q.dtype], _DT[alpha.dtype], _stream(stream))
+            chunk, scale, *_codes(q, alpha, conventions), _stream(stream))
     _check(st, "gdn_prefill_chunked_noalloc")
     return out, final_state

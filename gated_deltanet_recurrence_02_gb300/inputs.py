@@ -91,6 +91,37 @@ def make_inputs(seed: int, *, lengths: Sequence[int], Hk: int, Hv: int,
         dk=dk, dv=dv, scale=1.0, lengths=[int(x) for x in lengths])
 
 
+def make_raw_inputs(seed: int, *, lengths: Sequence[int], Hk: int, Hv: int, dk: int,
+                    dv: int, dtype_qkv: str = "bf16", dtype_gate: str = "f32",
+                    zero_state: bool = False) -> GdnInputs:
+    """Inputs in a layer's raw conventions, for the in-kernel front end: q, k
+    ~ N(0, 1) times a per-token, per-head magnitude ~ U(0.5, 2) (neither
+    normalised nor scaled), v ~ N(0, 1), beta as logits ~ N(0, 1), alpha as the
+    log-decay g = -U(0.01, 0.5), initial state 0.1 * N(0, 1).  Drawn in that
+    order from PCG64(seed), rounded to the storage dtypes."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    B = len(lengths)
+    total = int(sum(lengths))
+    q = rng.standard_normal((total, Hk, dk), dtype=np.float32)
+    k = rng.standard_normal((total, Hk, dk), dtype=np.float32)
+    q *= rng.uniform(0.5, 2.0, size=(total, Hk, 1)).astype(np.float32)
+    k *= rng.uniform(0.5, 2.0, size=(total, Hk, 1)).astype(np.float32)
+    v = rng.standard_normal((total, Hv, dv), dtype=np.float32)
+    beta = rng.standard_normal((total, Hv), dtype=np.float32)
+    alpha = -rng.uniform(0.01, 0.5, size=(total, Hv)).astype(np.float32)
+    S0 = None
+    if not zero_state:
+        S0 = torch.from_numpy(
+            np.float32(0.1) * rng.standard_normal((B, Hv, dv, dk), dtype=np.float32))
+    cu = np.zeros(B + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(np.asarray(lengths, dtype=np.int64))
+    return GdnInputs(
+        q=_round(q, dtype_qkv), k=_round(k, dtype_qkv), v=_round(v, dtype_qkv),
+        alpha=_round(alpha, dtype_gate), beta=_round(beta, dtype_gate),
+        cu_seqlens=torch.from_numpy(cu), initial_state=S0, B=B, Hk=Hk, Hv=Hv,
+        dk=dk, dv=dv, scale=float(1.0 / np.sqrt(dk)), lengths=[int(x) for x in lengths])
+
+
 def capture_counts(seed: int, B: int, capacity: int) -> torch.Tensor:
     """capture_count[b] ~ U{0..capacity}, int32."""
     rng = np.random.Generator(np.random.PCG64(seed))

@@ -82,6 +82,24 @@ enum {
 /* Storage types of q / k / v / out (dtype_qkv) and alpha / beta (dtype_gate). */
 enum { GDN_F32 = 0, GDN_F16 = 1, GDN_BF16 = 2 };
 
+/*
+ * Input conventions ("gate/scaling conventions" of the layer feeding the
+ * recurrence [P2]), OR'd into the dtype arguments of every entry point that
+ * reads q / k / alpha / beta.  Without them, q and k arrive normalised, alpha
+ * is the decay itself and beta the write strength.
+ *  GDN_QK_L2NORM   in dtype_qkv:  q and k are L2-normalised per head inside
+ *                  the kernel, x / sqrt(sum_j x_j^2 + 1e-6), before q is
+ *                  multiplied by scale.
+ *  GDN_ALPHA_LOG   in dtype_gate: alpha holds g = log(decay) (<= 0 expected);
+ *                  the decay is e^g (the chunked form uses g directly).
+ *  GDN_BETA_LOGIT  in dtype_gate: beta holds logits; beta = 1 / (1 + e^-x).
+ * A capture stores the factors the recurrence actually used: the decay e^g
+ * and the normalised key, so that a replay rebuilds the same state.
+ */
+#define GDN_QK_L2NORM 0x100
+#define GDN_ALPHA_LOG 0x200
+#define GDN_BETA_LOGIT 0x400
+
 /* Slot width, in floats, of one captured token in `state_update`:
  * Hv decays, then Hk*dk keys, then Hv*dv deltas. */
 #define GDN_STATE_UPDATE_SLOT(Hk, Hv, dk, dv) \

@@ -257,3 +257,16 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(gdn, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         gdn.lib()
+
+
+def test_convention_bits_are_validated(L):
+    """GDN_QK_L2NORM belongs to dtype_qkv, the gate bits to dtype_gate; any
+    other bit is an invalid argument (checked before anything is launched)."""
+    QK, ALOG, BLOG = 0x100, 0x200, 0x400
+    assert rec(L, dtq=2 | ALOG) == INVALID
+    assert rec(L, dtg=2 | QK) == INVALID
+    assert rec(L, dtq=2 | 0x800) == INVALID
+    assert pre(L, dtg=0 | QK) == INVALID
+    assert rv(L, dtq=2 | BLOG) == INVALID
+    assert rec(L, B=0, T=0, dtq=2 | QK, dtg=2 | ALOG | BLOG) == 0
+    assert pre(L, B=0, T=0, dtq=2 | QK, dtg=0 | ALOG | BLOG) == 0
