@@ -339,6 +339,7 @@ def run_ours(args, rank, world, local_rank):
     ver_ms = [ev[s][2 + S_].elapsed_time(ev[s][3 + S_]) for s in range(args.steps)]
     assert torch.isfinite(out).all() and torch.isfinite(S).all() and torch.isfinite(p_out.float()).all()
     assert torch.isfinite(S_ver).all() and torch.isfinite(v_out.float()).all()
+    p_ref = p_out.clone()  # the step's prefill output (one call), before the extra legs
 
     if args.only != "all":
         # profiling mode: one phase only, no JSON contract line
@@ -371,7 +372,8 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- end to end through the public API with host buffers (decode) ----
     e2e = run_e2e(args, gdn, dev, stream, hq, hk_, hv, ha, hb, S0_host, counts, d)
-    e2e_pre = run_e2e_prefill(args, gdn, dev, stream, xp)
+    # the step's prefill output (same inputs, one call) checks the segmented e2e run
+    e2e_pre = run_e2e_prefill(args, gdn, dev, stream, xp, ref_out=p_ref if do_pre else None)
 
     line = None
     if rank == 0:
@@ -594,94 +596,169 @@ DECODE_TRAFFIC_BYTES = 541_225_984 + 483_706_880
 VERIFY_TRAFFIC_BYTES = 567_217_408 + 391_318_528
 
 
+E2E_GROUPS = 4       # decode e2e: row groups pipelined on their own streams
+E2E_SEGMENT = 1024   # prefill e2e: tokens per call (a multiple of the 64-token chunk)
+
+
 def run_e2e(args, gdn, dev, stream, hq, hk_, hv, ha, hb, S0_host, counts, d):
-    """Decode through the public API with host-resident data: every step copies
-    the initial state and the 64 tokens' inputs from pinned host memory, runs
-    the 64 calls, and copies the final state, outputs and capture back."""
+    """Decode through the public API with host-resident data.  Every step
+    copies the initial state and the 64 tokens' inputs from pinned host memory,
+    runs the 64 calls and copies the final state, outputs and capture back.
+    Rows are independent, so the batch runs as E2E_GROUPS row groups, each on
+    its own stream (copy in, 64 calls, copy out): one group's copies overlap
+    the others' kernels."""
     import torch
     B, S_, cap = d["B"], d["steps"], d["cap"]
-    pin = lambda t: t.pin_memory()  # noqa: E731
-    h_in = [pin(t) for t in (hq, hk_, hv, ha, hb)]
-    h_S0, h_cc = pin(S0_host), pin(counts)
-    d_in = [torch.empty_like(t, device=dev) for t in h_in]
-    d_S = torch.empty_like(h_S0, device=dev)
-    d_cc = torch.empty_like(h_cc, device=dev)
-    d_out = torch.empty_like(d_in[2])
+    G = E2E_GROUPS if B % E2E_GROUPS == 0 else 1
+    Bg = B // G
     slot = gdn.slot_width(d["Hk"], d["Hv"], d["dk"], d["dv"])
-    d_su = torch.empty((B, cap, slot), dtype=torch.float32, device=dev)
-    h_S = torch.empty_like(h_S0).pin_memory()
-    h_out = torch.empty_like(d_out, device="cpu").pin_memory()
-    h_su = torch.empty_like(d_su, device="cpu").pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in h_in) + h_S0.numel() * 4 + h_cc.numel() * 4
-    d2h = h_S.numel() * 4 + h_out.numel() * h_out.element_size() + h_su.numel() * 4
+    pin = lambda t: t.contiguous().pin_memory()  # noqa: E731
+    grp = []
+    for g in range(G):
+        r = slice(g * Bg, (g + 1) * Bg)
+        h_in = [pin(t[:, r]) for t in (hq, hk_, hv, ha, hb)]  # step-major [S_, rows, ...]
+        e = dict(h_in=h_in, h_S0=pin(S0_host[r]), h_cc=pin(counts[r]),
+                 d_in=[torch.empty_like(t, device=dev) for t in h_in],
+                 d_S=torch.empty(S0_host[r].shape, dtype=torch.float32, device=dev),
+                 d_cc=torch.empty(Bg, dtype=torch.int32, device=dev),
+                 d_su=torch.empty((Bg, cap, slot), dtype=torch.float32, device=dev),
+                 stream=torch.cuda.Stream(dev))
+        e["d_out"] = torch.empty_like(e["d_in"][2])
+        e["h_S"] = torch.empty_like(e["h_S0"]).pin_memory()
+        e["h_out"] = torch.empty_like(e["d_out"], device="cpu").pin_memory()
+        e["h_su"] = torch.empty_like(e["d_su"], device="cpu").pin_memory()
+        grp.append(e)
+    h2d = sum(sum(t.numel() * t.element_size() for t in e["h_in"]) + e["h_S0"].numel() * 4
+              + e["h_cc"].numel() * 4 for e in grp)
+    d2h = sum(e["h_S"].numel() * 4 + e["h_out"].numel() * e["h_out"].element_size()
+              + e["h_su"].numel() * 4 for e in grp)
 
-    def one():
-        for dt, ht in zip(d_in, h_in):
-            dt.copy_(ht, non_blocking=True)
-        d_S.copy_(h_S0, non_blocking=True)
-        d_cc.copy_(h_cc, non_blocking=True)
-        q, k, v, a, bt = d_in
-        for t in range(S_):
-            gdn.gdn_recurrent_capture(q[t], k[t], v[t], a[t], bt[t], B=B, T=1, initial_state=d_S,
-                                      final_state=d_S, out=d_out[t], state_update_capacity=cap,
-                                      capture_count=d_cc, state_update=d_su)
-        h_S.copy_(d_S, non_blocking=True)
-        h_out.copy_(d_out, non_blocking=True)
-        h_su.copy_(d_su, non_blocking=True)
+    def one(start):
+        done = []
+        for e in grp:
+            s = e["stream"]
+            s.wait_event(start)
+            with torch.cuda.stream(s):
+                for dt, ht in zip(e["d_in"], e["h_in"]):
+                    dt.copy_(ht, non_blocking=True)
+                e["d_S"].copy_(e["h_S0"], non_blocking=True)
+                e["d_cc"].copy_(e["h_cc"], non_blocking=True)
+                q, k, v, a, bt = e["d_in"]
+                for t in range(S_):
+                    gdn.gdn_recurrent_capture(q[t], k[t], v[t], a[t], bt[t], B=Bg, T=1,
+                                              initial_state=e["d_S"], final_state=e["d_S"],
+                                              out=e["d_out"][t], state_update_capacity=cap,
+                                              capture_count=e["d_cc"], state_update=e["d_su"],
+                                              stream=s)
+                e["h_S"].copy_(e["d_S"], non_blocking=True)
+                e["h_out"].copy_(e["d_out"], non_blocking=True)
+                e["h_su"].copy_(e["d_su"], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(s)
+            done.append(ev)
+        for ev in done:
+            stream.wait_event(ev)
+
+    def mark():
+        ev = torch.cuda.Event(enable_timing=True)
+        ev.record(stream)
+        return ev
 
     for _ in range(max(1, args.warmup)):
-        one()
+        one(mark())
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     n = max(1, args.steps // 2)
-    e0.record(stream)
+    e0 = mark()
     for _ in range(n):
-        one()
-    e1.record(stream)
+        one(mark())
+    e1 = mark()
     torch.cuda.synchronize()
     sec = e0.elapsed_time(e1) / 1e3
     byts = decode_bytes(counts.tolist(), d) * S_ * n
     val = reduce_scalar(byts, "sum", dev) / reduce_scalar(sec, "max", dev) / 1e9
     return {"value": round(val, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "steps": n}
+            "d2h_bytes_per_step": int(d2h), "steps": n, "row_groups": G}
 
 
-def run_e2e_prefill(args, gdn, dev, stream, xp):
-    """Prefill through the public API with host-resident inputs and results."""
+def run_e2e_prefill(args, gdn, dev, stream, xp, ref_out=None):
+    """Prefill through the public API with host-resident inputs and results.
+    The row runs as calls of E2E_SEGMENT tokens (chunk-aligned, so the result
+    is the single call's), the state carried between them; a copy-in stream,
+    the compute stream and a copy-out stream overlap segment j + 1's inputs and
+    segment j - 1's outputs with segment j's prefill."""
     import torch
-    names = ("q", "k", "v", "alpha", "beta", "initial_state")
+    T, C = PRE["T"], PRE["chunk"]
+    names = ("q", "k", "v", "alpha", "beta")
     h = {n: getattr(xp, n).pin_memory() for n in names}
+    h_S0 = xp.initial_state.pin_memory()
     dd = {n: torch.empty_like(h[n], device=dev) for n in names}
+    d_S = [torch.empty_like(h_S0, device=dev) for _ in range(3)]  # S0, then ping-pong
     d_out = torch.empty_like(dd["v"])
-    d_fs = torch.empty_like(dd["initial_state"])
     h_out = torch.empty_like(d_out, device="cpu").pin_memory()
-    h_fs = torch.empty_like(d_fs, device="cpu").pin_memory()
-    T = PRE["T"]
+    h_fs = torch.empty_like(h_S0).pin_memory()
+    bounds = list(range(0, T, E2E_SEGMENT)) + [T]
+    if len(bounds) > 2 and bounds[-1] - bounds[-2] < C:
+        bounds.pop(-2)  # a short tail joins the previous segment
+    seg_max = max(b1 - b0 for b0, b1 in zip(bounds, bounds[1:]))
+    ws_n = gdn.gdn_prefill_workspace_size(1, seg_max, PRE["Hk"], PRE["Hv"], PRE["dk"], PRE["dv"],
+                                          C, torch.bfloat16)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-    def one():
-        for n in names:
-            dd[n].copy_(h[n], non_blocking=True)
-        gdn.gdn_prefill_chunked(dd["q"], dd["k"], dd["v"], dd["alpha"], dd["beta"], B=1, T=T,
-                                initial_state=dd["initial_state"], final_state=d_fs, out=d_out,
-                                chunk=PRE["chunk"])
-        h_out.copy_(d_out, non_blocking=True)
-        h_fs.copy_(d_fs, non_blocking=True)
+    def one(start):
+        s_in.wait_event(start)
+        with torch.cuda.stream(s_in):
+            d_S[0].copy_(h_S0, non_blocking=True)
+        loaded = []
+        for b0, b1 in zip(bounds, bounds[1:]):
+            with torch.cuda.stream(s_in):
+                for n in names:
+                    dd[n][b0:b1].copy_(h[n][b0:b1], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(s_in)
+                loaded.append(ev)
+        for j, (b0, b1) in enumerate(zip(bounds, bounds[1:])):
+            stream.wait_event(loaded[j])
+            s_prev = d_S[0] if j == 0 else d_S[1 + (j - 1) % 2]
+            s_next = d_S[1 + j % 2]
+            gdn.gdn_prefill_chunked(dd["q"][b0:b1], dd["k"][b0:b1], dd["v"][b0:b1],
+                                    dd["alpha"][b0:b1], dd["beta"][b0:b1], B=1, T=b1 - b0,
+                                    initial_state=s_prev, final_state=s_next,
+                                    out=d_out[b0:b1], chunk=C, workspace=ws, stream=stream)
+            ev = torch.cuda.Event()
+            ev.record(stream)
+            s_out.wait_event(ev)
+            with torch.cuda.stream(s_out):
+                h_out[b0:b1].copy_(d_out[b0:b1], non_blocking=True)
+                if b1 == T:
+                    h_fs.copy_(s_next, non_blocking=True)
+        fin = torch.cuda.Event()
+        fin.record(s_out)
+        stream.wait_event(fin)
+
+    def mark():
+        ev = torch.cuda.Event(enable_timing=True)
+        ev.record(stream)
+        return ev
 
     for _ in range(max(1, args.warmup)):
-        one()
+        one(mark())
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     n = max(1, args.steps)
-    e0.record(stream)
+    e0 = mark()
     for _ in range(n):
-        one()
-    e1.record(stream)
+        one(mark())
+    e1 = mark()
     torch.cuda.synchronize()
     sec = e0.elapsed_time(e1) / 1e3
+    if ref_out is not None:
+        # chunk-aligned segments reproduce the single call bit for bit
+        assert torch.equal(h_out.to(dev), ref_out)
     val = reduce_scalar(T * n, "sum", dev) / reduce_scalar(sec, "max", dev)
-    return {"value": round(val, 1), "unit": "tokens/s",
-            "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in h.values())),
-            "d2h_bytes_per_step": int(h_out.numel() * 2 + h_fs.numel() * 4)}
+    h2d = sum(t.numel() * t.element_size() for t in h.values()) + h_S0.numel() * 4
+    return {"value": round(val, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(h_out.numel() * 2 + h_fs.numel() * 4),
+            "segments": len(bounds) - 1}
 
 
 # ------------------------------------------------------ oracle (CPU) arm --
