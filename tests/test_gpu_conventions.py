@@ -109,3 +109,42 @@ def test_conventions(gdn, oracle_mod, path, conv):
             assert rel(su[r, :nb, :Hv], rsu[r, :nb, :Hv]) < 1e-6, r
             assert rel(su[r, :nb, Hv:off], rsu[r, :nb, Hv:off]) < 1e-6, r
             assert rel(su[r, :nb, off:], rsu[r, :nb, off:]) < dtol, r
+
+
+def test_conventions_fused_replay_verify(gdn, oracle_mod):
+    """The fused speculative step with every convention on: the replayed
+    factors are the stored (converted) ones; the drafts go through the front
+    end in the kernel."""
+    from gated_deltanet_recurrence_02_gb300.inputs import make_raw_inputs
+    Hk, Hv, d, cap, B, T = 2, 4, 128, 4, 3, 4
+    x1 = make_raw_inputs(1600, lengths=[T] * B, Hk=Hk, Hv=Hv, dk=d, dv=d, dtype_qkv="bf16",
+                         dtype_gate="bf16")
+    x2 = make_raw_inputs(1601, lengths=[T] * B, Hk=Hk, Hv=Hv, dk=d, dv=d, dtype_qkv="bf16",
+                         dtype_gate="bf16", zero_state=True)
+    flags = dict(qk_l2norm=True, alpha_log=True, beta_logit=True)
+    # previous verify pass: the oracle's capture of x1's drafts (converted factors), as fp32
+    q1, k1, a1, b1 = oracle_mod.front_end(x1.q, x1.k, x1.alpha, x1.beta, **flags)
+    _, _, su1 = oracle_mod.recurrent(q1, k1, x1.v, a1, b1, B=B, Hk=Hk, Hv=Hv, dk=d, dv=d, T=T,
+                                     initial_state=x1.initial_state, scale=x1.scale,
+                                     capacity=cap, capture_count=[cap] * B)
+    su1 = torch.from_numpy(su1.astype(np.float32))
+    accepted = [0, 2, 4]
+    g = {n: getattr(x2, n).cuda() for n in ("q", "k", "v", "alpha", "beta")}
+    out, Sc, su2, _ = gdn.gdn_replay_verify(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=B,
+                                            T=T, state_in=x1.initial_state.cuda(),
+                                            prev_state_update=su1.cuda(), prev_capacity=cap,
+                                            accepted_count=_acc(accepted), scale=x2.scale,
+                                            state_update_capacity=cap,
+                                            capture_count=_acc([cap] * B), conventions=0x700)
+    torch.cuda.synchronize()
+    q2, k2, a2, b2 = oracle_mod.front_end(x2.q, x2.k, x2.alpha, x2.beta, **flags)
+    ro, rSc, _, rsu = oracle_mod.replay_verify(
+        q2, k2, x2.v, a2, b2, B=B, Hk=Hk, Hv=Hv, dk=d, dv=d, T=T, state_in=x1.initial_state,
+        prev_state_update=su1, prev_capacity=cap, accepted_count=accepted, scale=x2.scale,
+        capacity=cap, capture_count=[cap] * B)
+    tol = TOL[torch.bfloat16]
+    assert rel(Sc, rSc) < tol
+    assert rel(out, ro) < tol
+    off = Hv + Hk * d
+    assert rel(su2[:, :, :off], rsu[:, :, :off]) < 1e-6
+    assert rel(su2[:, :, off:], rsu[:, :, off:]) < TOL_CAPTURE
