@@ -596,7 +596,7 @@ DECODE_TRAFFIC_BYTES = 541_223_680 + 483_353_856
 VERIFY_TRAFFIC_BYTES = 567_209_216 + 391_220_736
 
 
-E2E_GROUPS = 4       # decode e2e: row groups pipelined on their own streams
+E2E_GROUPS = 8       # decode e2e: row groups pipelined on their own streams
 E2E_SEGMENT = 1024   # prefill e2e: tokens per call (a multiple of the 64-token chunk)
 
 
