@@ -187,20 +187,33 @@ constexpr int LD = 68;                           // fp32 row stride of A^T and T
 // forward substitution, then the off-diagonal tiles by increasing distance,
 // T_JI = -D_J (sum_{I <= K < J} A_JK T_KI).  In the level stages each thread
 // computes a 1 x 4 piece of a tile (row r, columns c0 .. c0 + 3), fed by one
-// float4 of T per step.  256 threads; T written to sT.
+// float4 of T per step, with four partial sums; the diagonal solves load each
+// row of A one step ahead.  256 threads; T written to sT.
 constexpr int kIntraThreads = 256;
 __device__ __forceinline__ void blocked_unit_lower_inverse(const float *At, float *sT, float *X, int tid) {
     if (tid < 64) {
         const int bb = tid >> 4, cl = tid & 15, o = 16 * bb;
-        float acc[16];
+        float acc[16], row[16];  // row: A[o+t][o+r], loaded one step ahead
 #pragma unroll
-        for (int r = 0; r < 16; ++r) acc[r] = 0.f;
+        for (int r = 0; r < 16; ++r) {
+            acc[r] = 0.f;
+            row[r] = At[o * LD + o + r];
+        }
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
+            float nxt[16];
+            if (t + 1 < 16) {
+#pragma unroll
+                for (int r = 0; r < 16; ++r) nxt[r] = (r > t + 1) ? At[(o + t + 1) * LD + o + r] : 0.f;
+            }
             const float x = (t < cl) ? 0.f : ((t == cl) ? 1.f : -acc[t]);
             sT[(o + t) * LD + o + cl] = x;
 #pragma unroll
-            for (int r = t + 1; r < 16; ++r) acc[r] = fmaf(At[(o + t) * LD + o + r], x, acc[r]);
+            for (int r = t + 1; r < 16; ++r) acc[r] = fmaf(row[r], x, acc[r]);
+            if (t + 1 < 16) {
+#pragma unroll
+                for (int r = 0; r < 16; ++r) row[r] = nxt[r];
+            }
         }
     } else {
         // zero the tiles above the diagonal
@@ -212,34 +225,50 @@ __device__ __forceinline__ void blocked_unit_lower_inverse(const float *At, floa
         }
     }
     __syncthreads();
+    // four partial sums per dot product (independent chains hide the
+    // shared-memory latency), added at the end
+    auto sum4 = [](const float4 (&a)[4]) {
+        return make_float4((a[0].x + a[1].x) + (a[2].x + a[3].x), (a[0].y + a[1].y) + (a[2].y + a[3].y),
+                           (a[0].z + a[1].z) + (a[2].z + a[3].z), (a[0].w + a[1].w) + (a[2].w + a[3].w));
+    };
     const int q = tid & 63, r = q >> 2, c0 = (q & 3) * 4;
+#pragma unroll
     for (int d = 1; d < 4; ++d) {
         const int nb = 4 - d;
         const int blk = tid >> 6, I = blk, J = blk + d;
         if (blk < nb) {
-            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int K = I; K < J; ++K) {
-#pragma unroll 8
+            float4 a[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) a[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int kk = 0; kk < d; ++kk) {
+                const int K = I + kk;
+#pragma unroll
                 for (int m = 0; m < 16; ++m) {
                     const float x = At[(16 * K + m) * LD + 16 * J + r];
                     const float4 t4 = *reinterpret_cast<const float4 *>(sT + (16 * K + m) * LD + 16 * I + c0);
-                    a.x = fmaf(x, t4.x, a.x); a.y = fmaf(x, t4.y, a.y);
-                    a.z = fmaf(x, t4.z, a.z); a.w = fmaf(x, t4.w, a.w);
+                    float4 &acc = a[m & 3];
+                    acc.x = fmaf(x, t4.x, acc.x); acc.y = fmaf(x, t4.y, acc.y);
+                    acc.z = fmaf(x, t4.z, acc.z); acc.w = fmaf(x, t4.w, acc.w);
                 }
             }
-            *reinterpret_cast<float4 *>(X + blk * 256 + r * 16 + c0) = a;
+            *reinterpret_cast<float4 *>(X + blk * 256 + r * 16 + c0) = sum4(a);
         }
         __syncthreads();
         if (blk < nb) {
-            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
+            float4 a[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) a[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
             for (int m = 0; m < 16; ++m) {
                 const float dd = sT[(16 * J + r) * LD + 16 * J + m];
                 const float4 x4 = *reinterpret_cast<const float4 *>(X + blk * 256 + m * 16 + c0);
-                a.x = fmaf(dd, x4.x, a.x); a.y = fmaf(dd, x4.y, a.y);
-                a.z = fmaf(dd, x4.z, a.z); a.w = fmaf(dd, x4.w, a.w);
+                float4 &acc = a[m & 3];
+                acc.x = fmaf(dd, x4.x, acc.x); acc.y = fmaf(dd, x4.y, acc.y);
+                acc.z = fmaf(dd, x4.z, acc.z); acc.w = fmaf(dd, x4.w, acc.w);
             }
-            *reinterpret_cast<float4 *>(sT + (16 * J + r) * LD + 16 * I + c0) = make_float4(-a.x, -a.y, -a.z, -a.w);
+            const float4 s4 = sum4(a);
+            *reinterpret_cast<float4 *>(sT + (16 * J + r) * LD + 16 * I + c0) = make_float4(-s4.x, -s4.y, -s4.z, -s4.w);
         }
         __syncthreads();
     }
