@@ -416,6 +416,7 @@ int prefill_call(const void *q, const void *k, const void *v, const void *alpha,
     p.capture_count = capacity > 0 ? capture_count : nullptr;
     p.active = capacity > 0 ? state_update_active : nullptr;
     p.su = capacity > 0 ? state_update : nullptr;
+    p.chunk_table = nullptr;  // set by the tensor-core launcher for packed rows
     if (error_word(&p.err) != cudaSuccess) return GDN_ERR_CUDA;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     const cudaError_t e = use_tc ? launch_prefill_tc(p, s) : launch_prefill_simt(p, s);

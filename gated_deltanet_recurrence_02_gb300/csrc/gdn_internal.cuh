@@ -79,6 +79,10 @@ struct PrefillParams {
     const int32_t *capture_count;
     const int32_t *active;
     float *su;
+    // Packed rows on the tensor-core path: the first global chunk index of
+    // every row (B + 1 entries), written into the head of the workspace by a
+    // prologue kernel; nullptr for uniform rows.
+    const int32_t *chunk_table;
     uint32_t *err;
 };
 

@@ -125,42 +125,89 @@ __device__ __forceinline__ uint32_t u32_chunk(int r, int q) {
 
 __device__ __forceinline__ int n_chunks(int len) { return (len + C - 1) / C; }
 
-// First global chunk index of row b.
-__device__ __forceinline__ long chunk_base(const int32_t *cu, int B, int T, int b) {
-    if (cu == nullptr) return (long)b * n_chunks(T);
-    long acc = 0;
-    for (int r = 0; r < b; ++r) {
-        long tok0;
-        int len;
-        row_range(cu, r, T, tok0, len);
-        acc += n_chunks(len);
-    }
-    return acc;
+// Bytes at the head of the workspace that hold the per-row chunk table
+// (packed rows only).
+__host__ __device__ constexpr size_t chunk_table_bytes(int B) { return ((size_t)(B + 1) * 4 + 1023) / 1024 * 1024; }
+
+// First global chunk index of row b (uniform rows: b * chunks per row; packed
+// rows: the table).
+__device__ __forceinline__ long chunk_base(const PrefillParams &p, int b) {
+    if (p.chunk_table == nullptr) return (long)b * n_chunks(p.T);
+    return p.chunk_table[b];
 }
 
-// Global chunk index -> (row, chunk in row); false past the last chunk.
-__device__ __forceinline__ bool chunk_of(const int32_t *cu, int B, int T, long gc, int &b, int &c) {
-    if (cu == nullptr) {
-        const int nc = n_chunks(T);
+// Global chunk index -> (row, chunk in row); false past the last chunk.  With
+// packed rows a binary search over the table (rows without chunks have equal
+// neighbouring entries and are skipped by taking the last row that starts at
+// or before gc).
+__device__ __forceinline__ bool chunk_of(const PrefillParams &p, long gc, int &b, int &c) {
+    if (p.chunk_table == nullptr) {
+        const int nc = n_chunks(p.T);
         if (nc == 0) return false;
         b = (int)(gc / nc);
         c = (int)(gc % nc);
-        return b < B;
+        return b < p.B;
     }
-    long acc = 0;
-    for (int r = 0; r < B; ++r) {
-        long tok0;
-        int len;
-        row_range(cu, r, T, tok0, len);
-        const int nc = n_chunks(len);
-        if (gc < acc + nc) {
-            b = r;
-            c = (int)(gc - acc);
-            return true;
+    const int32_t *tbl = p.chunk_table;
+    if (gc >= tbl[p.B]) return false;
+    int lo = 0, hi = p.B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tbl[mid] <= gc) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+    c = (int)(gc - tbl[lo]);
+    return true;
+}
+
+// The records follow the chunk table (if any) in the workspace.
+__device__ __forceinline__ uint8_t *records(const PrefillParams &p) {
+    return reinterpret_cast<uint8_t *>(p.ws) + (p.chunk_table ? chunk_table_bytes(p.B) : 0);
+}
+
+// Prologue for packed rows: table[b] = chunks of rows 0 .. b-1 (table[0] = 0,
+// table[B] = all chunks), one CTA scanning the rows 1024 at a time.
+__global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t *cu, int B, int T, int32_t *table) {
+    __shared__ int32_t warp_incl[32];
+    __shared__ int32_t carry;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        carry = 0;
+        table[0] = 0;
+    }
+    __syncthreads();
+    for (int r0 = 0; r0 < B; r0 += 1024) {
+        const int r = r0 + tid;
+        int x = 0;
+        if (r < B) {
+            long tok0;
+            int len;
+            row_range(cu, r, T, tok0, len);
+            x = n_chunks(len);
         }
-        acc += nc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_incl[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int w = warp_incl[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += y;
+            }
+            warp_incl[lane] = w;
+        }
+        __syncthreads();
+        const int incl = carry + (warp ? warp_incl[warp - 1] : 0) + x;
+        if (r < B) table[r + 1] = incl;
+        __syncthreads();
+        if (tid == 1023) carry = incl;
+        __syncthreads();
     }
-    return false;
 }
 
 struct TcMaps {
@@ -301,14 +348,13 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     const int h = blockIdx.y, Hv = p.Hv, Hk = p.Hk;
     const int hk = h / (Hv / Hk);
     int b, c;
-    if (!chunk_of(p.cu_seqlens, p.B, p.T, blockIdx.x, b, c)) return;
+    if (!chunk_of(p, blockIdx.x, b, c)) return;
     long rtok0;
     int len;
     row_range(p.cu_seqlens, b, p.T, rtok0, len);
     const long tok0 = rtok0 + (long)c * C;
     const int n = min(C, len - c * C);
-    uint8_t *rec = reinterpret_cast<uint8_t *>(p.ws) +
-                   ((size_t)(chunk_base(p.cu_seqlens, p.B, p.T, b) + c) * Hv + h) * REC_BYTES;
+    uint8_t *rec = records(p) + ((size_t)(chunk_base(p, b) + c) * Hv + h) * REC_BYTES;
 
     if (tid == 0) {
         prefetch_tensormap(&mq);
@@ -616,8 +662,7 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     const int nc = n_chunks(len);
     const long su_slot = (long)Hv + (long)Hk * D + (long)Hv * D;
     const int ncap = XO ? prefill_ncap(p, b, len) : 0;
-    const uint8_t *rec0 = reinterpret_cast<const uint8_t *>(p.ws) +
-                          (size_t)chunk_base(p.cu_seqlens, p.B, p.T, b) * Hv * REC_BYTES +
+    const uint8_t *rec0 = records(p) + (size_t)chunk_base(p, b) * Hv * REC_BYTES +
                           (size_t)h * REC_BYTES;
     const size_t rec_stride = (size_t)Hv * REC_BYTES;
 
@@ -939,14 +984,24 @@ bool prefill_tc_supported(int dk, int dv, int chunk, int dt_qkv) {
 }
 
 size_t prefill_tc_workspace_bytes(int B, int T, int Hv, bool varlen) {
-    return (size_t)max_chunks_of(B, T, varlen) * (size_t)Hv * REC_BYTES;
+    return (varlen ? chunk_table_bytes(B) : 0) + (size_t)max_chunks_of(B, T, varlen) * (size_t)Hv * REC_BYTES;
 }
 
-cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t stream) {
+cudaError_t launch_prefill_tc(const PrefillParams &p_in, cudaStream_t stream) {
+    PrefillParams p = p_in;
     const bool varlen = p.cu_seqlens != nullptr;
     const long total_T = varlen ? (long)p.T : (long)p.B * p.T;
     const long mc = max_chunks_of(p.B, p.T, varlen);
     const bool xo = p.ckpt != nullptr || p.capacity > 0;
+    p.chunk_table = nullptr;
+    if (varlen && p.B > 0) {
+        // packed rows: per-row chunk table at the head of the workspace
+        int32_t *tbl = reinterpret_cast<int32_t *>(p.ws);
+        chunk_table_kernel<<<1, 1024, 0, stream>>>(p.cu_seqlens, p.B, p.T, tbl);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        p.chunk_table = tbl;
+    }
     if (p.dt_qkv == GDN_BF16)
         return xo ? launch_e<__nv_bfloat16, true>(p, total_T, mc, stream)
                   : launch_e<__nv_bfloat16, false>(p, total_T, mc, stream);

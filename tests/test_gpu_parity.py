@@ -397,3 +397,28 @@ def test_query_scale_every_path(gdn, oracle_mod, path):
     tol = TOL[x.q.dtype]
     assert rel(out, ro) < tol
     assert rel(fs, rS) < tol
+
+
+def test_many_packed_rows_tensor_core_prefill(gdn, oracle_mod):
+    """300 packed rows of 0 .. 40 tokens (many empty or shorter than a chunk)
+    through the tensor-core prefill: every row's output and final state
+    against the oracle (the per-row chunk table maps chunks to rows)."""
+    from gated_deltanet_recurrence_02_gb300.inputs import make_inputs, ragged_lengths
+    lengths = ragged_lengths(2000, 300, 0, 40)
+    lengths[7] = 130  # one row spanning three chunks
+    x = make_inputs(2001, lengths=lengths, Hk=2, Hv=4, dk=128, dv=128, dtype_qkv="bf16",
+                    dtype_gate="bf16")
+    g = to_dev(x)
+    B = len(lengths)
+    o, fs = gdn.gdn_prefill_chunked(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=B,
+                                    cu_seqlens=g["cu_seqlens"], initial_state=g["initial_state"],
+                                    chunk=64)
+    torch.cuda.synchronize()
+    ro, rS, _ = oracle_mod.recurrent(x.q, x.k, x.v, x.alpha, x.beta, B=B, Hk=2, Hv=4, dk=128,
+                                     dv=128, cu_seqlens=x.cu_seqlens,
+                                     initial_state=x.initial_state, threads=THREADS)
+    tol = TOL[torch.bfloat16]
+    assert rel(o, ro) < tol
+    assert rel(fs, rS) < tol
+    empty = [b for b, L in enumerate(lengths) if L == 0]
+    assert empty and all(torch.equal(fs[b], g["initial_state"][b]) for b in empty)
