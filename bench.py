@@ -366,6 +366,7 @@ def run_ours(args, rank, world, local_rank):
     unfused = run_verify_unfused(gdn, stream, gv, su_prev, v_acc_d, v_full, S_ver, d)
     ckpt = run_prefill_variant(gdn, stream, gp, p_out, p_fs, ws, flush, "checkpoints")
     pcap = run_prefill_variant(gdn, stream, gp, p_out, p_fs, ws, flush, "capture")
+    pbatch = run_prefill_batch(gdn, dev, stream, rank, hbm_peak, tf_peak)
     fe = run_front_end(gdn, stream, q, k, v, a, bt, S, out, cc, su, gp, p_out, p_fs, ws, flush, d)
     ms_per_step = (sum(pre_ms) + sum(dec_ms) + sum(rep_ms) + sum(ver_ms)) / args.steps
     ms_per_step = reduce_scalar(ms_per_step, "max", dev)
@@ -433,6 +434,7 @@ def run_ours(args, rank, world, local_rank):
                     "frac": round((pb + ckpt["bytes"]) / (ckpt["us"] * 1e-6) / 1e9 / hbm_peak, 4),
                     "overhead_vs_plain": round(ckpt["us"] / (pre_avg_s * 1e6) - 1.0, 4),
                 },
+                "batch": pbatch,
                 "capture": {
                     "workload": "prefill_T4100 with the compact capture of its first 64 tokens "
                                 "(capacity 64, gdn_prefill_chunked_capture)",
@@ -505,6 +507,46 @@ def run_verify_unfused(gdn, stream, gv, su_prev, acc_d, full, S_src, d, n=20, wa
     ver = statistics.mean(e[1].elapsed_time(e[2]) for e in ev) * 1e3
     del S
     return {"replay": round(rep, 2), "verify": round(ver, 2), "total": round(rep + ver, 2)}
+
+
+def run_prefill_batch(gdn, dev, stream, rank, hbm_peak, tf_peak, n=5, warm=3):
+    """prefill_batch_B64: 64 packed rows of 500 .. 1500 tokens in one call, timed
+    outside the step (the inputs, ~2 GB, exceed L2).  Tokens/s and the bytes
+    and flops rooflines of the call."""
+    import torch
+    from gated_deltanet_recurrence_02_gb300.inputs import WORKLOADS, make_inputs, ragged_lengths
+    w = WORKLOADS["prefill_batch_B64"]
+    lengths = ragged_lengths(w["seed"] + 100 * rank, w["B"], w["lo"], w["hi"])
+    x = make_inputs(w["seed"] + 1 + 100 * rank, lengths=lengths, Hk=w["Hk"], Hv=w["Hv"],
+                    dk=w["dk"], dv=w["dv"], dtype_qkv=w["dtype_qkv"], dtype_gate=w["dtype_gate"])
+    g = {n: getattr(x, n).to(dev) for n in ("q", "k", "v", "alpha", "beta", "initial_state")}
+    cu = x.cu_seqlens.to(dev)
+    B, T, Hk, Hv, d, C = w["B"], int(x.cu_seqlens[-1]), w["Hk"], w["Hv"], w["dk"], w["chunk"]
+    out = torch.empty_like(g["v"])
+    fs = torch.empty_like(g["initial_state"])
+    ws = torch.empty(gdn.gdn_prefill_workspace_size(B, T, Hk, Hv, d, d, C, torch.bfloat16,
+                                                    varlen=True), dtype=torch.uint8, device=dev)
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    ev = [[E(), E()] for _ in range(n)]
+    for i in range(warm + n):
+        e = ev[i - warm] if i >= warm else None
+        if e: e[0].record(stream)
+        gdn.gdn_prefill_chunked(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=B, cu_seqlens=cu,
+                                initial_state=g["initial_state"], final_state=fs, out=out,
+                                chunk=C, workspace=ws)
+        if e: e[1].record(stream)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all() and torch.isfinite(fs).all()
+    sec = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / 1e3
+    byts = (T * (2 * Hk * d * 2 + 2 * Hv * d * 2 + 2 * Hv * 4) + 2 * B * Hv * d * d * 4)
+    flops = T * Hv * (6 * d * d + 10 * C * d)
+    del g, out, fs, ws
+    return {"workload": f"prefill_batch_B64: {B} packed rows of {w['lo']}..{w['hi']} tokens "
+                        f"({T} in all), Hk=16, Hv=32, d=128, bf16 q/k/v, fp32 alpha/beta",
+            "avg_launch_us": round(sec * 1e6, 2), "value": round(T / sec, 1), "unit": "tokens/s",
+            "frac": round(byts / sec / 1e9 / hbm_peak, 4),
+            "tensor_frac": round(flops / sec / 1e12 / tf_peak, 4),
+            "algorithmic_bytes_per_launch": byts, "algorithmic_flops_per_launch": flops}
 
 
 def run_prefill_variant(gdn, stream, gp, out, fs, ws, flush, kind, n=10, warm=3):

@@ -158,6 +158,9 @@ WORKLOADS = {
     "decode_B256": dict(seed=1004, B=256, steps=64, Hk=16, Hv=32, dk=128,
                         dv=128, dtype_qkv="bf16", dtype_gate="bf16",
                         capacity=4),
+    # batched prefill of packed rows: 64 rows of 500 .. 1500 tokens
+    "prefill_batch_B64": dict(seed=1006, B=64, lo=500, hi=1500, Hk=16, Hv=32, dk=128,
+                              dv=128, dtype_qkv="bf16", dtype_gate="f32", chunk=64),
     # speculative decoding: each step replays the accepted prefix of the
     # previous step's 4 captured drafts (accepted ~ U{0..4}) and verifies 4
     # new draft tokens per row, all captured
