@@ -19,13 +19,16 @@
  *      q, k        [total_T, Hk, dk]     (Hq must equal Hk)
  *      v, out      [total_T, Hv, dv]
  *      alpha, beta [total_T, Hv]         alpha is the decay itself, in (0, 1]
+ *                                        (or its log, with GDN_ALPHA_LOG below)
  *      state       [N, Hv, dv, dk] fp32  (dk fastest)
  *    Rows are either uniform (cu_seqlens == NULL: row b owns tokens
  *    b*T .. b*T+T-1, total_T = B*T) or packed (cu_seqlens: int32 [B+1] on the
  *    device, cu_seqlens[0] = 0, non-decreasing, cu_seqlens[B] = total_T; the
  *    `T` argument is then total_T).  Token bounds read from cu_seqlens are
  *    clamped to [0, total_T] on the device.
- *  - q is used as given (already normalised); `scale` multiplies it.
+ *  - q and k are used as given (already normalised) unless GDN_QK_L2NORM asks
+ *    the kernel to normalise them (see "Input conventions"); `scale` then
+ *    multiplies q.
  *  - Float pointers (q, k, v, out, alpha, beta, states, state_update,
  *    workspace) must be 16-byte aligned; int32 pointers 4-byte aligned.
  *  - Argument errors are reported synchronously, before anything is launched.
