@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/gdn.h"
 
 namespace gdn {
@@ -124,6 +126,22 @@ bool prefill_simt_supported(int dk, int dv, int chunk);
 cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t stream);
 bool prefill_tc_supported(int dk, int dv, int chunk, int dt_qkv);
 size_t prefill_tc_workspace_bytes(int B, int T, int Hv, bool varlen);
+
+// Raises kernel Kern's dynamic shared-memory limit to `bytes`, once per device
+// (function attributes belong to the device's context): later calls make no
+// CUDA call, so launches captured into a CUDA graph carry none.
+template <auto Kern>
+inline cudaError_t set_smem_once(int bytes) {
+    static std::atomic<uint64_t> done{0};  // one bit per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+    if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+    e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
 
 // ------------------------------------------------------------- helpers --
 

@@ -308,7 +308,7 @@ template <int DK, int C, typename TQ>
 cudaError_t launch_t(const PrefillParams &p, cudaStream_t stream) {
     auto kern = prefill_simt_kernel<DK, C, TQ>;
     const size_t bytes = SimtSmem<DK, C>::kBytes;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    cudaError_t e = set_smem_once<prefill_simt_kernel<DK, C, TQ>>((int)bytes);
     if (e != cudaSuccess) return e;
     dim3 grid(p.dv / kDVT, p.Hv, p.B);
     kern<<<grid, kThreads, bytes, stream>>>(p);

@@ -957,10 +957,12 @@ cudaError_t launch_e(const PrefillParams &p, long total_T, long max_chunks, cuda
     if (total_T > 0 && (!make_map(&mq, p.q, p.Hk, total_T, bf) || !make_map(&mk, p.k, p.Hk, total_T, bf) ||
                         !make_map(&mv, p.v, p.Hv, total_T, bf)))
         return cudaErrorInvalidValue;
-    auto intra = (p.conv & GDN_QK_L2NORM) ? prefill_intra_kernel<E, XO, true> : prefill_intra_kernel<E, XO, false>;
-    cudaError_t e = cudaFuncSetAttribute(intra, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)A_SMEM);
+    const bool norm = (p.conv & GDN_QK_L2NORM) != 0;
+    auto intra = norm ? prefill_intra_kernel<E, XO, true> : prefill_intra_kernel<E, XO, false>;
+    cudaError_t e = norm ? set_smem_once<prefill_intra_kernel<E, XO, true>>((int)A_SMEM)
+                         : set_smem_once<prefill_intra_kernel<E, XO, false>>((int)A_SMEM);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(prefill_carry_kernel<E, XO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)B_SMEM);
+    e = set_smem_once<prefill_carry_kernel<E, XO>>((int)B_SMEM);
     if (e != cudaSuccess) return e;
     if (max_chunks > 0) {
         dim3 ga((unsigned)max_chunks, p.Hv);

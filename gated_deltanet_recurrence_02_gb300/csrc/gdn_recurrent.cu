@@ -491,7 +491,7 @@ template <int DK, typename TQ, int TS, int RS, int CPS>
 cudaError_t launch_v(const RecurrentParams &p, cudaStream_t stream) {
     auto kern = recurrent_kernel<DK, TQ, TS, RS, CPS>;
     const size_t bytes = (size_t)kStages * StageLayout<DK, TQ, TS, RS>::kBytes + 2 * kStages * sizeof(uint64_t);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    cudaError_t e = set_smem_once<recurrent_kernel<DK, TQ, TS, RS, CPS>>((int)bytes);
     if (e != cudaSuccess) return e;
     const long tiles = (long)p.B * p.Hv * (p.dv / kRowsPerCta);
     const long cap = (long)sm_count() * CPS;
