@@ -2,13 +2,14 @@
 // prefill) with compact capture, and the fused replay + verify step.
 //
 // Work unit: a tile of 32 rows of one state matrix (row b, value head h),
-// processed by 4 warps -- each lane holds its dk/8 columns of two rows.  The
+// processed by CW compute warps (4 in both instances launched: each lane
+// holds its dk/8 columns of two rows).  The
 // 32 rows are contiguous in HBM, so one bulk (1-D TMA) copy stages a tile in
 // shared memory.  The kernel is persistent and warp-specialised: a grid of
 // (SMs x CTAs-per-SM) walks the tiles with a grid stride; in each CTA a
 // producer warp stages three tiles ahead -- the state tile and the first TS
 // tokens' k, q and v slice (bulk copies), their gates, the first RS replayed
-// slots' factors and a header -- and four compute warps work from shared
+// slots' factors and a header -- and the compute warps work from shared
 // memory only, so neither HBM nor L2 latency sits on their path.  The compute
 // lanes keep their state columns in registers (float2 pairs for the packed
 // fp32x2 FMA) across all tokens of the call and write them back once with
@@ -38,11 +39,7 @@ namespace gdn {
 namespace {
 
 constexpr int kLanesPerRow = 8;
-constexpr int kWarps = 4;
-constexpr int kPasses = 2;
-constexpr int kRowsPerWarp = (32 / kLanesPerRow) * kPasses;  // 8
-constexpr int kRowsPerCta = kWarps * kRowsPerWarp;            // 32
-constexpr int kThreads = kWarps * 32;
+constexpr int kRowsPerCta = 32;
 
 __device__ __forceinline__ void split4(float4 v, float2 &lo, float2 &hi) {
     lo = make_float2(v.x, v.y);
@@ -75,8 +72,6 @@ __device__ __forceinline__ void store_row(float *dst, const float2 (&Sr)[2 * F4]
 }
 
 constexpr int kStages = 3;       // tiles in flight per CTA
-constexpr int kComputeWarps = kWarps;
-constexpr int kCtaThreads = kThreads + 32;  // + one producer warp
 
 // Per-stage header, written by the producer before it arrives on the stage.
 struct TileHeader {
@@ -109,10 +104,14 @@ struct StageLayout {
 // TS tokens and RS replayed slots per tile are staged in shared memory by the
 // producer; later ones (long rows, large acceptance counts) are read by the
 // compute warps straight from memory.  CPS = resident CTAs per SM.
-template <int DK, typename TQ, int TS, int RS, int CPS>
-__global__ void __launch_bounds__(kCtaThreads, CPS)
+template <int DK, typename TQ, int TS, int RS, int CPS, int CW>
+__global__ void __launch_bounds__(CW * 32 + 32, CPS)
 recurrent_kernel(const RecurrentParams p) {
     using L = StageLayout<DK, TQ, TS, RS>;
+    // CW compute warps share the tile's 32 rows: each 8-lane group of a warp
+    // holds NP rows (CW = 4: two rows, CW = 8: one row)
+    constexpr int NP = 32 / (CW * 4);
+    constexpr int kRowsW = 4 * NP;  // rows per compute warp
     constexpr int F4 = DK / (4 * kLanesPerRow);  // float4 per lane per row
     constexpr int F2 = 2 * F4;                   // the same columns as float2 pairs
     constexpr int KPL = DK / 32;                 // replay-key floats per producer lane
@@ -132,7 +131,7 @@ recurrent_kernel(const RecurrentParams p) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             tc::mbar_init(&full[s], 1);
-            tc::mbar_init(&empty[s], kComputeWarps);
+            tc::mbar_init(&empty[s], CW);
         }
         tc::fence_mbar_init();
     }
@@ -142,7 +141,7 @@ recurrent_kernel(const RecurrentParams p) {
     // Lane 0 issues the bulk copies; the lanes load the gates and the replay
     // factors (plain loads: slots are not 16-byte aligned in general) and
     // store them into the stage; lane 0's arrive then releases the stage.
-    if (warp == kComputeWarps) {
+    if (warp == CW) {
         int it = 0;
         for (long id = blockIdx.x; id < n_tiles; id += gridDim.x, ++it) {
             const int stage = it % kStages;
@@ -250,7 +249,7 @@ recurrent_kernel(const RecurrentParams p) {
         const long per = (total + gridDim.x - 1) / gridDim.x;
         const long e0 = (long)blockIdx.x * per;
         const long e1 = (e0 + per < total) ? e0 + per : total;
-        for (long e = e0 + threadIdx.x; e < e1; e += kThreads) p.su[e] = 0.0f;
+        for (long e = e0 + threadIdx.x; e < e1; e += CW * 32) p.su[e] = 0.0f;
     }
     const TQ *qb = reinterpret_cast<const TQ *>(p.q);
     const TQ *kb = reinterpret_cast<const TQ *>(p.k);
@@ -258,9 +257,9 @@ recurrent_kernel(const RecurrentParams p) {
     TQ *ob = reinterpret_cast<TQ *>(p.out);
     const float scale = p.scale;
     const bool commit_in_place = (p.s_commit == p.s0);
-    int lrow[kPasses];  // row inside the tile
+    int lrow[NP];  // row inside the tile
 #pragma unroll
-    for (int r = 0; r < kPasses; ++r) lrow[r] = warp * kRowsPerWarp + r * (32 / kLanesPerRow) + grp;
+    for (int r = 0; r < NP; ++r) lrow[r] = warp * kRowsW + r * (32 / kLanesPerRow) + grp;
 
     int it = 0;
     for (long id = blockIdx.x; id < n_tiles; id += gridDim.x, ++it) {
@@ -362,7 +361,7 @@ recurrent_kernel(const RecurrentParams p) {
                 if (hd.ncap > 0) su_t = su_row;
             }
 #pragma unroll
-            for (int r = 0; r < kPasses; ++r) {
+            for (int r = 0; r < NP; ++r) {
                 float2 Sr[F2];
                 load_row(r, Sr);
                 if (Tb > 0) row_step(Sr, r, 0, kf, qf, a, bt, kq, su_t);
@@ -370,9 +369,9 @@ recurrent_kernel(const RecurrentParams p) {
             }
             if (su_t != nullptr) capture_token(su_t, a, kf);
         } else {
-            float2 S[kPasses][F2];
+            float2 S[NP][F2];
 #pragma unroll
-            for (int r = 0; r < kPasses; ++r) load_row(r, S[r]);
+            for (int r = 0; r < NP; ++r) load_row(r, S[r]);
 
             // Replay of the accepted prefix, S <- decay S + delta key^T per
             // slot, then the committed state (skipped in place when nothing
@@ -380,14 +379,14 @@ recurrent_kernel(const RecurrentParams p) {
             if (hd.m > 0) {
                 const float *su_b = p.rp_su + (long)b * p.rp_capacity * slot;
                 for (int j = 0; j < hd.m; ++j) {
-                    float dec, dl[kPasses];
+                    float dec, dl[NP];
                     float2 kk[F2];
                     if (j < RS) {
                         const float *rk = reinterpret_cast<const float *>(st + L::oRK) + j * DK;
                         const float *rd = reinterpret_cast<const float *>(st + L::oRD) + j * kRowsPerCta;
                         dec = reinterpret_cast<const float *>(st + L::oRA)[j];
 #pragma unroll
-                        for (int r = 0; r < kPasses; ++r) dl[r] = rd[lrow[r]];
+                        for (int r = 0; r < NP; ++r) dl[r] = rd[lrow[r]];
 #pragma unroll
                         for (int f = 0; f < F4; ++f)
                             split4(*reinterpret_cast<const float4 *>(rk + (f * kLanesPerRow + l8) * 4), kk[2 * f],
@@ -398,7 +397,7 @@ recurrent_kernel(const RecurrentParams p) {
                         const float *del = s + Hv + (long)Hk * DK + (long)h * dv + row0;
                         dec = __ldg(s + h);
 #pragma unroll
-                        for (int r = 0; r < kPasses; ++r) dl[r] = __ldg(del + lrow[r]);
+                        for (int r = 0; r < NP; ++r) dl[r] = __ldg(del + lrow[r]);
 #pragma unroll
                         for (int f = 0; f < F4; ++f) {
                             const int col = (f * kLanesPerRow + l8) * 4;
@@ -408,7 +407,7 @@ recurrent_kernel(const RecurrentParams p) {
                     }
                     const float2 dec2 = make_float2(dec, dec);
 #pragma unroll
-                    for (int r = 0; r < kPasses; ++r) {
+                    for (int r = 0; r < NP; ++r) {
                         const float2 d2 = make_float2(dl[r], dl[r]);
 #pragma unroll
                         for (int i = 0; i < F2; ++i) S[r][i] = __ffma2_rn(dec2, S[r][i], __fmul2_rn(d2, kk[i]));
@@ -418,41 +417,41 @@ recurrent_kernel(const RecurrentParams p) {
             if (p.s_commit != nullptr && (hd.m > 0 || !commit_in_place)) {
                 float *sc = p.s_commit + (((long)b * Hv + h) * dv + row0) * DK;
 #pragma unroll
-                for (int r = 0; r < kPasses; ++r) store_row<DK, F4>(sc, S[r], lrow[r], l8);
+                for (int r = 0; r < NP; ++r) store_row<DK, F4>(sc, S[r], lrow[r], l8);
             }
 
             for (int t = 0; t < Tb; ++t) {
                 float2 kf[F2], qf[F2];
-                float a, bt, vi[kPasses];
+                float a, bt, vi[NP];
                 token_in(t, kf, qf, a, bt);
                 const long tok = hd.tok0 + t;
                 if (t < TS) {
                     const TQ *vs = reinterpret_cast<const TQ *>(st + L::oV + t * L::kV);
 #pragma unroll
-                    for (int r = 0; r < kPasses; ++r) vi[r] = ld_f(vs + lrow[r]);
+                    for (int r = 0; r < NP; ++r) vi[r] = ld_f(vs + lrow[r]);
                 } else {
                     const TQ *vg = vb + (tok * Hv + h) * (long)dv + row0;
 #pragma unroll
-                    for (int r = 0; r < kPasses; ++r) vi[r] = ld_f(vg + lrow[r]);
+                    for (int r = 0; r < NP; ++r) vi[r] = ld_f(vg + lrow[r]);
                 }
                 // every row's dot products first, then all reductions together
                 // (independent shuffle chains), then the updates
-                float kq = dot_pairs<F2>(kf, qf), sk[kPasses], sq[kPasses];
+                float kq = dot_pairs<F2>(kf, qf), sk[NP], sq[NP];
 #pragma unroll
-                for (int r = 0; r < kPasses; ++r) {
+                for (int r = 0; r < NP; ++r) {
                     sk[r] = dot_pairs<F2>(S[r], kf);
                     sq[r] = dot_pairs<F2>(S[r], qf);
                 }
                 kq = group_sum<kLanesPerRow>(kq) * scale;
 #pragma unroll
-                for (int r = 0; r < kPasses; ++r) {
+                for (int r = 0; r < NP; ++r) {
                     sk[r] = group_sum<kLanesPerRow>(sk[r]);
                     sq[r] = group_sum<kLanesPerRow>(sq[r]) * scale;
                 }
                 float *su_t = (t < hd.ncap) ? su_row + (long)t * slot : nullptr;
                 const float2 a2 = make_float2(a, a);
 #pragma unroll
-                for (int r = 0; r < kPasses; ++r) {
+                for (int r = 0; r < NP; ++r) {
                     const float delta = bt * (vi[r] - a * sk[r]);
                     const float2 d2 = make_float2(delta, delta);
 #pragma unroll
@@ -466,7 +465,7 @@ recurrent_kernel(const RecurrentParams p) {
             }
             if (sf != nullptr)
 #pragma unroll
-                for (int r = 0; r < kPasses; ++r) store_row<DK, F4>(sf, S[r], lrow[r], l8);
+                for (int r = 0; r < NP; ++r) store_row<DK, F4>(sf, S[r], lrow[r], l8);
         }
         // this warp is done reading the stage
         __syncwarp();
@@ -487,16 +486,16 @@ int sm_count() {
     return n;
 }
 
-template <int DK, typename TQ, int TS, int RS, int CPS>
+template <int DK, typename TQ, int TS, int RS, int CPS, int CW>
 cudaError_t launch_v(const RecurrentParams &p, cudaStream_t stream) {
-    auto kern = recurrent_kernel<DK, TQ, TS, RS, CPS>;
+    auto kern = recurrent_kernel<DK, TQ, TS, RS, CPS, CW>;
     const size_t bytes = (size_t)kStages * StageLayout<DK, TQ, TS, RS>::kBytes + 2 * kStages * sizeof(uint64_t);
-    cudaError_t e = set_smem_once<recurrent_kernel<DK, TQ, TS, RS, CPS>>((int)bytes);
+    cudaError_t e = set_smem_once<recurrent_kernel<DK, TQ, TS, RS, CPS, CW>>((int)bytes);
     if (e != cudaSuccess) return e;
     const long tiles = (long)p.B * p.Hv * (p.dv / kRowsPerCta);
     const long cap = (long)sm_count() * CPS;
     const unsigned grid = (unsigned)(tiles < cap ? tiles : cap);
-    kern<<<grid, kCtaThreads, bytes, stream>>>(p);
+    kern<<<grid, CW * 32 + 32, bytes, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -506,8 +505,8 @@ cudaError_t launch_v(const RecurrentParams &p, cudaStream_t stream) {
 template <int DK, typename TQ>
 cudaError_t launch_t(const RecurrentParams &p, cudaStream_t stream) {
     if (p.rp_capacity == 0 && p.cu_seqlens == nullptr && p.T <= 1)
-        return launch_v<DK, TQ, 1, 0, 4>(p, stream);
-    return launch_v<DK, TQ, 4, 4, 3>(p, stream);
+        return launch_v<DK, TQ, 1, 0, 4, 4>(p, stream);
+    return launch_v<DK, TQ, 4, 4, 3, 4>(p, stream);
 }
 
 template <int DK>
