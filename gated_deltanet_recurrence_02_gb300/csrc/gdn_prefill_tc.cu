@@ -344,6 +344,8 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     uint64_t *bar_v = bar_ld + 2;
     uint32_t *slot = reinterpret_cast<uint32_t *>(bar_ld + 3);
 
+    // the carry kernel may start its prologue once every CTA here has started
+    grid_launch_dependents();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = blockIdx.y, Hv = p.Hv, Hk = p.Hk;
     const int hk = h / (Hv / Hk);
@@ -718,6 +720,7 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
             bulk_prefetch_l2(rec + REC_VEC, 1024);
         };
         if (lane == 0) {
+            grid_dependency_wait();  // the records are the chunk-parallel kernel's output
             for (int cc = 0; cc < NS && cc < nc; ++cc) issue_stage(cc);
             for (int cc = NS; cc < NS + 2 && cc < nc; ++cc) prefetch_chunk(cc);
             for (int cc = NS; cc < nc; ++cc) {
@@ -798,6 +801,7 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
         for (int q8 = 0; q8 < 2; ++q8)
             *reinterpret_cast<uint4 *>(sS + sw128_chunk(j, 2 * half + q8)) = pack8<E>(S + 8 * q8);
         fence_proxy_async();
+        grid_dependency_wait();  // global writes below follow the chunk-parallel kernel's
         fence_before_sync();
         named_bar(kBarState, kBarThreads);
         fence_after_sync();
@@ -970,9 +974,20 @@ cudaError_t launch_e(const PrefillParams &p, long total_T, long max_chunks, cuda
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    dim3 gb(D / DVT, p.Hv, p.B);
-    prefill_carry_kernel<E, XO><<<gb, kCarryThreads, B_SMEM, stream>>>(p, mq, mk);
-    return cudaGetLastError();
+    // The carry kernel is a programmatic dependent of the chunk-parallel one:
+    // its prologue (barriers, TMEM, the initial state) overlaps that kernel's
+    // tail, and it waits for that kernel's records before reading them.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(D / DVT, p.Hv, p.B);
+    cfg.blockDim = dim3(kCarryThreads);
+    cfg.dynamicSmemBytes = B_SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = max_chunks > 0 ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, prefill_carry_kernel<E, XO>, p, mq, mk);
 }
 
 long max_chunks_of(int B, int T, bool varlen) {

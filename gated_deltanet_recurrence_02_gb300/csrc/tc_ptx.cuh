@@ -119,6 +119,15 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Programmatic dependent launch: a kernel lets the next one in the stream
+// start its prologue (launch_dependents), and the next one waits, before it
+// touches what the first one wrote, until that grid has completed and its
+// memory is visible (wait).  Without a programmatic launch both are no-ops.
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------- tcgen05 ---
 
 // Whole warp: allocate `ncols` TMEM columns, address written to *slot (smem).
