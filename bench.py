@@ -367,6 +367,7 @@ def run_ours(args, rank, world, local_rank):
     ckpt = run_prefill_variant(gdn, stream, gp, p_out, p_fs, ws, flush, "checkpoints")
     pcap = run_prefill_variant(gdn, stream, gp, p_out, p_fs, ws, flush, "capture")
     pbatch = run_prefill_batch(gdn, dev, stream, rank, hbm_peak, tf_peak)
+    psnap = run_prefix_snapshot(gdn, dev, stream, rank, hbm_peak)
     fe = run_front_end(gdn, stream, q, k, v, a, bt, S, out, cc, su, gp, p_out, p_fs, ws, flush, d)
     ms_per_step = (sum(pre_ms) + sum(dec_ms) + sum(rep_ms) + sum(ver_ms)) / args.steps
     ms_per_step = reduce_scalar(ms_per_step, "max", dev)
@@ -435,6 +436,7 @@ def run_ours(args, rank, world, local_rank):
                     "overhead_vs_plain": round(ckpt["us"] / (pre_avg_s * 1e6) - 1.0, 4),
                 },
                 "batch": pbatch,
+                "snapshot": psnap,
                 "capture": {
                     "workload": "prefill_T4100 with the compact capture of its first 64 tokens "
                                 "(capacity 64, gdn_prefill_chunked_capture)",
@@ -547,6 +549,64 @@ def run_prefill_batch(gdn, dev, stream, rank, hbm_peak, tf_peak, n=5, warm=3):
             "frac": round(byts / sec / 1e9 / hbm_peak, 4),
             "tensor_frac": round(flops / sec / 1e12 / tf_peak, 4),
             "algorithmic_bytes_per_launch": byts, "algorithmic_flops_per_launch": flops}
+
+
+def run_prefix_snapshot(gdn, dev, stream, rank, hbm_peak, n=10, warm=3):
+    """prefix_snapshot_B12: a 2048-token prefill from a zero state gives one
+    snapshot; 12 packed rows of 200 .. 1000 tokens then all start from it
+    (initial_state_indices = 0, read-only).  Tokens/s of the 12-row call, its
+    bytes roofline, and a check that the snapshot bytes never change."""
+    import torch
+    from gated_deltanet_recurrence_02_gb300.inputs import WORKLOADS, make_inputs, ragged_lengths
+    w = WORKLOADS["prefix_snapshot_B12"]
+    dims = dict(Hk=w["Hk"], Hv=w["Hv"], dk=w["dk"], dv=w["dv"])
+    pre = make_inputs(w["seed"] + 100 * rank, lengths=[w["prefix_len"]], dtype_qkv=w["dtype_qkv"],
+                      dtype_gate=w["dtype_gate"], zero_state=True, **dims)
+    lens = ragged_lengths(w["seed"] + 1 + 100 * rank, w["B"], w["lo"], w["hi"])
+    x = make_inputs(w["seed"] + 2 + 100 * rank, lengths=lens, dtype_qkv=w["dtype_qkv"],
+                    dtype_gate=w["dtype_gate"], zero_state=True, **dims)
+    gp = {n: getattr(pre, n).to(dev) for n in ("q", "k", "v", "alpha", "beta")}
+    g = {n: getattr(x, n).to(dev) for n in ("q", "k", "v", "alpha", "beta")}
+    cu = x.cu_seqlens.to(dev)
+    B, T, Hk, Hv, d, C = w["B"], int(x.cu_seqlens[-1]), w["Hk"], w["Hv"], w["dk"], w["chunk"]
+    snap = torch.empty((1, Hv, d, d), dtype=torch.float32, device=dev)
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    e_snap = [E(), E()]
+    with torch.cuda.stream(stream):
+        e_snap[0].record(stream)
+        gdn.gdn_prefill_chunked(gp["q"], gp["k"], gp["v"], gp["alpha"], gp["beta"], B=1,
+                                T=w["prefix_len"], final_state=snap, chunk=C)
+        e_snap[1].record(stream)
+    stream.synchronize()
+    before = snap.clone()
+    idx = torch.zeros(B, dtype=torch.int32, device=dev)
+    out = torch.empty_like(g["v"])
+    fs = torch.empty((B, Hv, d, d), dtype=torch.float32, device=dev)
+    ws = torch.empty(gdn.gdn_prefill_workspace_size(B, T, Hk, Hv, d, d, C, torch.bfloat16,
+                                                    varlen=True), dtype=torch.uint8, device=dev)
+    ev = [[E(), E()] for _ in range(n)]
+    for i in range(warm + n):
+        e = ev[i - warm] if i >= warm else None
+        if e: e[0].record(stream)
+        gdn.gdn_prefill_chunked(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=B, cu_seqlens=cu,
+                                initial_state=snap, initial_state_indices=idx, final_state=fs,
+                                out=out, chunk=C, workspace=ws)
+        if e: e[1].record(stream)
+    torch.cuda.synchronize()
+    assert torch.equal(snap.view(torch.int32), before.view(torch.int32)), "snapshot modified"
+    assert torch.isfinite(out.float()).all() and torch.isfinite(fs).all()
+    sec = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / 1e3
+    # q, k, v, o (bf16), alpha, beta (bf16), the snapshot read once per row, B final states
+    byts = T * (2 * Hk * d * 2 + 2 * Hv * d * 2 + 2 * Hv * 2) + 2 * B * Hv * d * d * 4
+    res = {"workload": f"prefix_snapshot_B12: snapshot of a {w['prefix_len']}-token prefill, then "
+                       f"{B} packed rows of {w['lo']}..{w['hi']} tokens ({T} in all) from it, "
+                       f"Hk=16, Hv=32, d=128, bf16",
+           "snapshot_us": round(e_snap[0].elapsed_time(e_snap[1]) * 1e3, 2),
+           "avg_launch_us": round(sec * 1e6, 2), "value": round(T / sec, 1), "unit": "tokens/s",
+           "frac": round(byts / sec / 1e9 / hbm_peak, 4), "algorithmic_bytes_per_launch": byts,
+           "snapshot_bit_identical": True}
+    del gp, g, out, fs, ws, snap
+    return res
 
 
 def run_prefill_variant(gdn, stream, gp, out, fs, ws, flush, kind, n=10, warm=3):

@@ -143,6 +143,22 @@ inline cudaError_t set_smem_once(int bytes) {
     return e;
 }
 
+// Multiprocessor count of the current device, cached per device (0..63) so
+// that calls after the first make no CUDA call.
+inline int sm_count_of_current_device() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (dev >= 0 && dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) return 1;
+    if (dev >= 0 && dev < 64) cache[dev].store(v, std::memory_order_relaxed);
+    return v;
+}
+
 // ------------------------------------------------------------- helpers --
 
 __device__ __forceinline__ float ld_f(const float *p) { return *p; }

@@ -64,7 +64,6 @@ using namespace tc;
 
 constexpr int C = 64;    // chunk
 constexpr int D = 128;   // dk = dv
-constexpr int DVT = 32;  // state rows per phase-B CTA
 constexpr uint64_t kWaitNs = 1000000000ull;
 
 // Workspace record per (chunk, value head), bytes.
@@ -615,21 +614,35 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
 
 // ============================================================ phase B ====
 
-constexpr uint32_t ST_A1 = 0;        // [Q ; W] image, 2 K-blocks of 128 rows
-constexpr uint32_t ST_K = 32768;     // K image, 2 dk blocks of 64 rows
-constexpr uint32_t ST_P = 49152;     // P' image (rows 0-63 of the [P'; X] operand; X = what follows)
-constexpr uint32_t ST_U = 57344;     // U tile, [64 t][32 i]
-constexpr uint32_t ST_VEC = 61440;   // gamma, w, gamma_last
-constexpr uint32_t ST_BYTES = 62464;
-constexpr int NS = 3;
-constexpr uint32_t B_S = NS * ST_BYTES;        // S^T image (MN-major, 128 K-rows, 32 N used)
-constexpr uint32_t B_DW = B_S + 16384;         // diag(w) Delta image (64 K-rows)
-constexpr uint32_t B_DD = B_DW + 8192;         // Delta image
-constexpr uint32_t B_BAR = B_DD + 8192;
-constexpr uint32_t B_SMEM = B_BAR + 128 + 1024;
-constexpr uint32_t STAGE_TX = 16384 + 16384 + 16384 + 8192 + 4096 + 1024;
+// One carry CTA owns TV rows of one (row, value head) state: TV = 32 (the
+// latency instance: the most CTAs, three stages) or TV = 64 (the throughput
+// instance, for grids of many rows: twice the work per MMA for about the same
+// issue time, two stages).
+template <int TV>
+struct CarryCfg {
+    static constexpr int kCols = TV / 2;             // state columns per compute thread
+    static constexpr int NS = TV == 32 ? 3 : 2;      // stages in the ring
+    static constexpr uint32_t ST_A1 = 0;             // [Q ; W] image, 2 K-blocks of 128 rows
+    static constexpr uint32_t ST_K = 32768;          // K image, 2 dk blocks of 64 rows
+    static constexpr uint32_t ST_P = 49152;          // P' image (rows 0-63 of the [P'; X] operand)
+    static constexpr uint32_t ST_U = 57344;          // U tiles, TV / 32 of [64 t][32 i]
+    static constexpr uint32_t kUBytes = TV * 128;
+    static constexpr uint32_t ST_VEC = ST_U + kUBytes;  // gamma, w, gamma_last
+    static constexpr uint32_t ST_BYTES = ST_VEC + 1024;
+    static constexpr uint32_t B_S = NS * ST_BYTES;   // S^T image (MN-major, 128 K-rows, TV N used)
+    static constexpr uint32_t B_DW = B_S + 16384;    // diag(w) Delta image (64 K-rows)
+    static constexpr uint32_t B_DD = B_DW + 8192;    // Delta image
+    static constexpr uint32_t B_BAR = B_DD + 8192;
+    static constexpr uint32_t B_SMEM = B_BAR + 128 + 1024;
+    static constexpr uint32_t STAGE_TX = 16384 + 16384 + 16384 + 8192 + kUBytes + 1024;
+    // TMEM columns: D1 = [Q; W] S^T at 0 / TV (by chunk parity), D2 = K^T w Delta
+    // at 2 TV, D3 = P' Delta at 3 TV / 4 TV (by chunk parity)
+    static constexpr uint32_t T_D2 = 2 * TV, T_D3 = 3 * TV;
+    static constexpr uint32_t T_COLS = TV == 32 ? 256 : 512;
+    static_assert(B_SMEM <= 232448, "carry CTA exceeds the shared memory of an SM");
+};
 // 8 compute warps: warp w reads TMEM lane quarter w % 4, warps w and w + 4
-// split the tile's 32 columns.  Warp 8 issues every MMA; warp 9 refills the
+// split the tile's TV columns.  Warp 8 issues every MMA; warp 9 refills the
 // stage ring, each stage once the output MMA of its chunk has retired (that
 // MMA's commit arrives on the stage's `empty` barrier).
 constexpr int kCarryComputeWarps = 8;
@@ -640,15 +653,24 @@ constexpr int kBarThreads = (kCarryComputeWarps + 1) * 32;  // compute warps + i
 constexpr uint32_t kBarDelta = 1;  // named barrier: Delta images written (all warps)
 constexpr uint32_t kBarState = 2;  // named barrier: S image written (all warps)
 
-template <typename E, bool XO>
+// The calling warp's N consecutive TMEM columns (N = 16 or 32), see tmem_ld16.
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[N]) {
+    if constexpr (N == 16) tmem_ld16(taddr, v);
+    else tmem_ld32(taddr, v);
+}
+
+template <typename E, bool XO, int TV>
 __global__ void __launch_bounds__(kCarryThreads, 1)
 prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap mq,
                      const __grid_constant__ CUtensorMap mk) {
+    using Cfg = CarryCfg<TV>;
+    constexpr int NS = Cfg::NS, NC = Cfg::kCols, Q8 = NC / 8;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sS = sm + B_S, *sDw = sm + B_DW, *sDd = sm + B_DD;
-    uint64_t *full = reinterpret_cast<uint64_t *>(sm + B_BAR);  // [NS]
-    uint64_t *empty = full + NS;                                  // [NS]
+    uint8_t *sS = sm + Cfg::B_S, *sDw = sm + Cfg::B_DW, *sDd = sm + Cfg::B_DD;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + Cfg::B_BAR);  // [NS]
+    uint64_t *empty = full + NS;                                       // [NS]
     uint64_t *bar1 = full + 2 * NS, *bar2 = bar1 + 1, *bar3 = bar1 + 2;
     uint32_t *slot = reinterpret_cast<uint32_t *>(bar1 + 3);
 
@@ -657,7 +679,7 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     const int vt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int Hv = p.Hv, Hk = p.Hk;
     const int hk = h / (Hv / Hk);
-    const int i0 = vt * DVT;
+    const int i0 = vt * TV;
     long rtok0;
     int len;
     row_range(p.cu_seqlens, b, p.T, rtok0, len);
@@ -682,31 +704,29 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     }
     __syncthreads();
     if (warp == 0) {
-        tmem_alloc(slot, 256);
+        tmem_alloc(slot, Cfg::T_COLS);
         tmem_relinquish();
     }
     const bool kbf = Elem<E>::kBf16;
-    // TMEM columns: D1 = [Q; W] S^T at 0 / 32 (double-buffered), D2 = K^T w Delta
-    // at 64, D3 = P' Delta at 96 / 128 (double-buffered)
     bool ok = true;
 
     if (warp == kCopierWarp) {
         // ======================= copier warp ============================
         auto issue_stage = [&](int cc) {
             const int s = cc % NS;
-            uint8_t *st = sm + s * ST_BYTES;
+            uint8_t *st = sm + s * Cfg::ST_BYTES;
             const uint8_t *rec = rec0 + (size_t)cc * rec_stride;
             const int t0 = (int)(rtok0 + (long)cc * C);
-            mbar_arrive_expect_tx(&full[s], STAGE_TX);
-            tma_load_3d(st + ST_A1, &mq, 0, hk, t0, &full[s]);
-            tma_load_3d(st + ST_A1 + 16384, &mq, 64, hk, t0, &full[s]);
-            bulk_load(st + ST_A1 + 8192, rec + REC_W, 8192, &full[s]);
-            bulk_load(st + ST_A1 + 24576, rec + REC_W + 8192, 8192, &full[s]);
-            tma_load_3d(st + ST_K, &mk, 0, hk, t0, &full[s]);
-            tma_load_3d(st + ST_K + 8192, &mk, 64, hk, t0, &full[s]);
-            bulk_load(st + ST_P, rec + REC_P, 8192, &full[s]);
-            bulk_load(st + ST_U, rec + REC_U + vt * 4096, 4096, &full[s]);
-            bulk_load(st + ST_VEC, rec + REC_VEC, 1024, &full[s]);
+            mbar_arrive_expect_tx(&full[s], Cfg::STAGE_TX);
+            tma_load_3d(st + Cfg::ST_A1, &mq, 0, hk, t0, &full[s]);
+            tma_load_3d(st + Cfg::ST_A1 + 16384, &mq, 64, hk, t0, &full[s]);
+            bulk_load(st + Cfg::ST_A1 + 8192, rec + REC_W, 8192, &full[s]);
+            bulk_load(st + Cfg::ST_A1 + 24576, rec + REC_W + 8192, 8192, &full[s]);
+            tma_load_3d(st + Cfg::ST_K, &mk, 0, hk, t0, &full[s]);
+            tma_load_3d(st + Cfg::ST_K + 8192, &mk, 64, hk, t0, &full[s]);
+            bulk_load(st + Cfg::ST_P, rec + REC_P, 8192, &full[s]);
+            bulk_load(st + Cfg::ST_U, rec + REC_U + vt * Cfg::kUBytes, Cfg::kUBytes, &full[s]);
+            bulk_load(st + Cfg::ST_VEC, rec + REC_VEC, 1024, &full[s]);
         };
         auto prefetch_chunk = [&](int cc) {
             const uint8_t *rec = rec0 + (size_t)cc * rec_stride;
@@ -716,7 +736,7 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
             tma_prefetch_l2_3d(&mk, 0, hk, t0);
             tma_prefetch_l2_3d(&mk, 64, hk, t0);
             bulk_prefetch_l2(rec + REC_W, 16384 + 8192);
-            bulk_prefetch_l2(rec + REC_U + vt * 4096, 4096);
+            bulk_prefetch_l2(rec + REC_U + vt * Cfg::kUBytes, Cfg::kUBytes);
             bulk_prefetch_l2(rec + REC_VEC, 1024);
         };
         if (lane == 0) {
@@ -739,21 +759,21 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
         named_bar(kBarState, kBarThreads);  // initial S image written
         fence_after_sync();
         const uint32_t tbase = *slot;
-        const uint32_t id1 = idesc_f16(128, DVT, false, true, kbf);
-        const uint32_t id2 = idesc_f16(128, DVT, true, true, kbf);
-        const uint32_t id3 = idesc_f16(128, DVT, false, true, kbf);
+        const uint32_t id1 = idesc_f16(128, TV, false, true, kbf);
+        const uint32_t id2 = idesc_f16(128, TV, true, true, kbf);
+        const uint32_t id3 = idesc_f16(128, TV, false, true, kbf);
         const uint64_t bS0 = desc_sw128(smem_u32(sS), 8192, 1024);
         const uint64_t bDw0 = desc_sw128(smem_u32(sDw), 8192, 1024);
         const uint64_t bDd0 = desc_sw128(smem_u32(sDd), 8192, 1024);
         for (int cc = 0; cc < nc; ++cc) {
             const int s = cc % NS;
-            uint8_t *st = sm + s * ST_BYTES;
+            uint8_t *st = sm + s * Cfg::ST_BYTES;
             if (lane == 0) {
                 ok = mbar_wait(&full[s], (cc / NS) & 1, kWaitNs);
                 if (ok) {
                     // D1 = [Q; W] S^T
-                    const uint64_t a0 = desc_sw128(smem_u32(st + ST_A1), 16, 1024);
-                    const uint32_t d1 = (cc & 1) ? 32u : 0u;
+                    const uint64_t a0 = desc_sw128(smem_u32(st + Cfg::ST_A1), 16, 1024);
+                    const uint32_t d1 = (cc & 1) ? (uint32_t)TV : 0u;
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
                         mma_f16(tbase + d1, desc_add(a0, (k >> 2) * 16384 + (k & 3) * 32), desc_add(bS0, k * 2048),
@@ -766,12 +786,12 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
             named_bar(kBarDelta, kBarThreads);  // Delta images written
             fence_after_sync();
             if (lane == 0 && ok) {
-                const uint64_t k0 = desc_sw128(smem_u32(st + ST_K), 8192, 1024);
-                const uint64_t p0 = desc_sw128(smem_u32(st + ST_P), 16, 1024);
-                const uint32_t d3 = (cc & 1) ? 128u : 96u;
+                const uint64_t k0 = desc_sw128(smem_u32(st + Cfg::ST_K), 8192, 1024);
+                const uint64_t p0 = desc_sw128(smem_u32(st + Cfg::ST_P), 16, 1024);
+                const uint32_t d3 = Cfg::T_D3 + ((cc & 1) ? (uint32_t)TV : 0u);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_f16(tbase + 64, desc_add(k0, k * 2048), desc_add(bDw0, k * 2048), id2, k > 0);
+                    mma_f16(tbase + Cfg::T_D2, desc_add(k0, k * 2048), desc_add(bDw0, k * 2048), id2, k > 0);
                 mma_commit(bar2);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
@@ -790,16 +810,16 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     } else {
         // ======================= compute warps ==========================
         // state tile: thread (quarter, lane) owns dk row j = 32 * quarter + lane of
-        // S^T for the 16 columns [16 * half, 16 * half + 16) of the tile
+        // S^T for the NC columns [NC * half, NC * half + NC) of the tile
         const int j = 32 * quarter + lane;
-        const int c0 = 16 * half;
-        float S[16];
+        const int c0 = NC * half;
+        float S[NC];
         const float *s0 = initial_state_ptr(p.s0, p.s0_idx, p.n_s0, b, h, Hv, D, D, p.err);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) S[i] = s0 ? s0[(size_t)(i0 + c0 + i) * D + j] : 0.f;
+        for (int i = 0; i < NC; ++i) S[i] = s0 ? s0[(size_t)(i0 + c0 + i) * D + j] : 0.f;
 #pragma unroll
-        for (int q8 = 0; q8 < 2; ++q8)
-            *reinterpret_cast<uint4 *>(sS + sw128_chunk(j, 2 * half + q8)) = pack8<E>(S + 8 * q8);
+        for (int q8 = 0; q8 < Q8; ++q8)
+            *reinterpret_cast<uint4 *>(sS + sw128_chunk(j, c0 / 8 + q8)) = pack8<E>(S + 8 * q8);
         fence_proxy_async();
         grid_dependency_wait();  // global writes below follow the chunk-parallel kernel's
         fence_before_sync();
@@ -811,39 +831,41 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
 
         for (int cc = 0; cc < nc; ++cc) {
             const int s = cc % NS;
-            uint8_t *st = sm + s * ST_BYTES;
-            const uint32_t d1 = (cc & 1) ? 32u : 0u;
-            const uint32_t d3 = (cc & 1) ? 128u : 96u;
+            uint8_t *st = sm + s * Cfg::ST_BYTES;
+            const uint32_t d1 = (cc & 1) ? (uint32_t)TV : 0u;
+            const uint32_t d3 = Cfg::T_D3 + ((cc & 1) ? (uint32_t)TV : 0u);
             const int n = min(C, len - cc * C);
             if (ok) ok = mbar_wait(&full[s], (cc / NS) & 1, kWaitNs);
-            const float *vec = reinterpret_cast<const float *>(st + ST_VEC);
+            const float *vec = reinterpret_cast<const float *>(st + Cfg::ST_VEC);
             const float gC = ok ? vec[128] : 0.f;
             if (quarter >= 2) {
-                // Delta = U - W S^T for token t, 16 of the 32 columns
+                // Delta = U - W S^T for token t, NC of the TV columns
                 const int t = 32 * (quarter - 2) + lane;
                 const float wt = ok ? vec[64 + t] : 0.f;
                 if (ok) ok = mbar_wait(bar1, cc & 1, kWaitNs);
                 if (ok) {
                     fence_after_sync();
-                    float ws[16];
-                    tmem_ld16(lane_base + d1 + c0, ws);
-                    const uint8_t *su = st + ST_U;
+                    float ws[NC];
+                    tmem_ld_cols<NC>(lane_base + d1 + c0, ws);
                     // captured tokens: Delta's row t is token t's delta
                     float *cap = (cc * C + t < ncap)
                                      ? p.su + ((size_t)b * p.capacity + cc * C + t) * su_slot + Hv + (size_t)Hk * D +
                                            (size_t)h * D + i0 + c0
                                      : nullptr;
 #pragma unroll
-                    for (int q8 = 0; q8 < 2; ++q8) {
+                    for (int q8 = 0; q8 < Q8; ++q8) {
+                        // column c0 + 8 q8 of the tile: U tile (c / 32), chunk (c % 32) / 8
+                        const int c = c0 + 8 * q8;
+                        const uint8_t *su = st + Cfg::ST_U + (c >> 5) * 4096;
                         float u[8], dd[8], dw[8];
-                        unpack8<E>(*reinterpret_cast<const uint4 *>(su + u32_chunk(t, 2 * half + q8)), u);
+                        unpack8<E>(*reinterpret_cast<const uint4 *>(su + u32_chunk(t, (c & 31) >> 3)), u);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             dd[e] = u[e] - ws[8 * q8 + e];
                             dw[e] = wt * dd[e];
                         }
-                        *reinterpret_cast<uint4 *>(sDd + sw128_chunk(t, 2 * half + q8)) = pack8<E>(dd);
-                        *reinterpret_cast<uint4 *>(sDw + sw128_chunk(t, 2 * half + q8)) = pack8<E>(dw);
+                        *reinterpret_cast<uint4 *>(sDd + sw128_chunk(t, c >> 3)) = pack8<E>(dd);
+                        *reinterpret_cast<uint4 *>(sDw + sw128_chunk(t, c >> 3)) = pack8<E>(dw);
                         if (cap != nullptr)
 #pragma unroll
                             for (int e = 0; e < 8; ++e) cap[8 * q8 + e] = dd[e];
@@ -859,38 +881,40 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
             if (ok) ok = mbar_wait(bar2, cc & 1, kWaitNs);
             if (ok) {
                 fence_after_sync();
-                float v[16];
-                tmem_ld16(lane_base + 64 + c0, v);
+                float v[NC];
+                tmem_ld_cols<NC>(lane_base + Cfg::T_D2 + c0, v);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) S[i] = fmaf(gC, S[i], v[i]);
+                for (int i = 0; i < NC; ++i) S[i] = fmaf(gC, S[i], v[i]);
 #pragma unroll
-                for (int q8 = 0; q8 < 2; ++q8)
-                    *reinterpret_cast<uint4 *>(sS + sw128_chunk(j, 2 * half + q8)) = pack8<E>(S + 8 * q8);
+                for (int q8 = 0; q8 < Q8; ++q8)
+                    *reinterpret_cast<uint4 *>(sS + sw128_chunk(j, c0 / 8 + q8)) = pack8<E>(S + 8 * q8);
                 fence_proxy_async();
-                // chunk-boundary checkpoint: the fp32 state after this chunk
-                const int ck = XO ? ckpt_slot(p, cc, len) : -1;
-                if (ck >= 0) {
-                    float *dst = p.ckpt + ((((size_t)b * p.ckpt_cap + ck) * Hv + h) * D + i0 + c0) * D;
+                if constexpr (XO) {
+                    // chunk-boundary checkpoint: the fp32 state after this chunk
+                    const int ck = ckpt_slot(p, cc, len);
+                    if (ck >= 0) {
+                        float *dst = p.ckpt + ((((size_t)b * p.ckpt_cap + ck) * Hv + h) * D + i0 + c0) * D;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) __stcs(dst + (size_t)i * D + j, S[i]);
+                        for (int i = 0; i < NC; ++i) __stcs(dst + (size_t)i * D + j, S[i]);
+                    }
                 }
             }
             fence_before_sync();
             named_bar(kBarState, kBarThreads);
             fence_after_sync();
             if (quarter < 2 && ok) {
-                // O = gamma_t (Q S^T) + P' Delta for token t, 16 columns
+                // O = gamma_t (Q S^T) + P' Delta for token t, NC columns
                 const int t = 32 * quarter + lane;
                 ok = mbar_wait(bar3, cc & 1, kWaitNs);
                 if (ok) {
                     fence_after_sync();
-                    float qs[16], pd[16];
-                    tmem_ld16(lane_base + d1 + c0, qs);
-                    tmem_ld16(lane_base + d3 + c0, pd);
+                    float qs[NC], pd[NC];
+                    tmem_ld_cols<NC>(lane_base + d1 + c0, qs);
+                    tmem_ld_cols<NC>(lane_base + d3 + c0, pd);
                     if (t < n) {
                         E *dst = ob + ((rtok0 + (long)cc * C + t) * Hv + h) * (long)D + i0 + c0;
 #pragma unroll
-                        for (int q8 = 0; q8 < 2; ++q8) {
+                        for (int q8 = 0; q8 < Q8; ++q8) {
                             float o[8];
 #pragma unroll
                             for (int e = 0; e < 8; ++e) o[e] = fmaf(gt, qs[8 * q8 + e], pd[8 * q8 + e]);
@@ -903,7 +927,7 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
         if (ok && p.s_final != nullptr) {
             float *sf = p.s_final + (((size_t)b * Hv + h) * D + i0 + c0) * D;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) sf[(size_t)i * D + j] = S[i];
+            for (int i = 0; i < NC; ++i) sf[(size_t)i * D + j] = S[i];
         }
     }
     if (!ok && tid == 0) atomicOr(p.err, (uint32_t)GDN_DEVERR_TIMEOUT);
@@ -912,7 +936,7 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     if (!ok && tid == 0)
         for (int s = 0; s < NS; ++s) mbar_wait(&full[s], 0, kWaitNs / 8);  // copies must land first
     __syncthreads();
-    if (warp == 0) tmem_dealloc(*slot, 256);
+    if (warp == 0) tmem_dealloc(*slot, Cfg::T_COLS);
 }
 
 // ============================================================== host =====
@@ -966,7 +990,11 @@ cudaError_t launch_e(const PrefillParams &p, long total_T, long max_chunks, cuda
     cudaError_t e = norm ? set_smem_once<prefill_intra_kernel<E, XO, true>>((int)A_SMEM)
                          : set_smem_once<prefill_intra_kernel<E, XO, false>>((int)A_SMEM);
     if (e != cudaSuccess) return e;
-    e = set_smem_once<prefill_carry_kernel<E, XO>>((int)B_SMEM);
+    // carry instance: 32-row tiles while one wave of them fits the GPU (the
+    // chain's latency decides), 64-row tiles for more rows (throughput decides)
+    const bool wide = (long)(D / 32) * p.Hv * p.B > (long)sm_count_of_current_device();
+    e = wide ? set_smem_once<prefill_carry_kernel<E, XO, 64>>((int)CarryCfg<64>::B_SMEM)
+             : set_smem_once<prefill_carry_kernel<E, XO, 32>>((int)CarryCfg<32>::B_SMEM);
     if (e != cudaSuccess) return e;
     if (max_chunks > 0) {
         dim3 ga((unsigned)max_chunks, p.Hv);
@@ -978,16 +1006,17 @@ cudaError_t launch_e(const PrefillParams &p, long total_T, long max_chunks, cuda
     // its prologue (barriers, TMEM, the initial state) overlaps that kernel's
     // tail, and it waits for that kernel's records before reading them.
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(D / DVT, p.Hv, p.B);
+    cfg.gridDim = dim3(D / (wide ? 64 : 32), p.Hv, p.B);
     cfg.blockDim = dim3(kCarryThreads);
-    cfg.dynamicSmemBytes = B_SMEM;
+    cfg.dynamicSmemBytes = wide ? CarryCfg<64>::B_SMEM : CarryCfg<32>::B_SMEM;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = max_chunks > 0 ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, prefill_carry_kernel<E, XO>, p, mq, mk);
+    return wide ? cudaLaunchKernelEx(&cfg, prefill_carry_kernel<E, XO, 64>, p, mq, mk)
+                : cudaLaunchKernelEx(&cfg, prefill_carry_kernel<E, XO, 32>, p, mq, mk);
 }
 
 long max_chunks_of(int B, int T, bool varlen) {

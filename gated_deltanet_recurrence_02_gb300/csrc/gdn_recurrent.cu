@@ -473,19 +473,6 @@ recurrent_kernel(const RecurrentParams p) {
     }
 }
 
-int sm_count() {
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0, v = 0;
-        if (cudaGetDevice(&dev) == cudaSuccess &&
-            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-            n = v;
-        else
-            n = 132;
-    }
-    return n;
-}
-
 template <int DK, typename TQ, int TS, int RS, int CPS, int CW>
 cudaError_t launch_v(const RecurrentParams &p, cudaStream_t stream) {
     auto kern = recurrent_kernel<DK, TQ, TS, RS, CPS, CW>;
@@ -493,7 +480,7 @@ cudaError_t launch_v(const RecurrentParams &p, cudaStream_t stream) {
     cudaError_t e = set_smem_once<recurrent_kernel<DK, TQ, TS, RS, CPS, CW>>((int)bytes);
     if (e != cudaSuccess) return e;
     const long tiles = (long)p.B * p.Hv * (p.dv / kRowsPerCta);
-    const long cap = (long)sm_count() * CPS;
+    const long cap = (long)sm_count_of_current_device() * CPS;
     const unsigned grid = (unsigned)(tiles < cap ? tiles : cap);
     kern<<<grid, CW * 32 + 32, bytes, stream>>>(p);
     return cudaGetLastError();

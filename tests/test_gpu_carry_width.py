@@ -1,0 +1,134 @@
+"""GPU parity of the tensor-core prefill's 64-row carry tiles.
+
+The carry phase runs on 32-row state tiles while one wave of them fits the
+GPU and on 64-row tiles for more (row, value head) pairs.  These cases have
+4 Hv B > the SM count, so every call below takes the 64-row instance: plain,
+with capture, with checkpoints and with the in-kernel input conventions,
+against the fp64 oracle.
+
+Sources: the chunked form of the gated delta rule (the prefill path of
+"Enable the native Kev example on NVIDIA GPUs through ExecuTorch's AOTI CUDA
+backend", executorch issue 23097, "Work to cover"); "[WebGPU EP] adds state
+update capacity support for GatedDeltaNet" (onnxruntime PR 32767),
+"Changes" (the capture contract); "Enable the native Kev example on the
+WebGPU backend" (executorch issue 23099): prefix snapshots, here kept at
+chunk boundaries.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import TOL, Guarded, rel
+
+pytestmark = pytest.mark.gpu
+THREADS = min(32, os.cpu_count() or 4)
+F32 = torch.float32
+LENGTHS = [150, 64, 37, 200, 90, 129]
+HK, HV, D, C = 2, 8, 128, 64
+
+
+@pytest.fixture(scope="module")
+def gdn():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gated_deltanet_recurrence_02_gb300 import build, gdn as g
+    build.build()
+    g.lib()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if 4 * HV * len(LENGTHS) <= sms:
+        pytest.skip("the 64-row carry instance needs more (row, head) tiles than SMs")
+    return g
+
+
+@pytest.fixture(scope="module")
+def case():
+    from gated_deltanet_recurrence_02_gb300.inputs import make_inputs
+    return make_inputs(2500, lengths=LENGTHS, Hk=HK, Hv=HV, dk=D, dv=D, dtype_qkv="bf16",
+                       dtype_gate="bf16")
+
+
+def _dev(x):
+    return {n: getattr(x, n).cuda() for n in ("q", "k", "v", "alpha", "beta")}
+
+
+def test_plain_and_capture(gdn, oracle_mod, case):
+    x = case
+    B, cap = len(LENGTHS), 70
+    counts = [70, 10, 37, 0, 64, 129]
+    g = _dev(x)
+    cu, S0 = x.cu_seqlens.cuda(), x.initial_state.cuda()
+    out, fs = gdn.gdn_prefill_chunked(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=B,
+                                      cu_seqlens=cu, initial_state=S0, chunk=C)
+    su = Guarded((B, cap, gdn.slot_width(HK, HV, D, D)), F32)
+    out2, fs2, _ = gdn.gdn_prefill_chunked_capture(
+        g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=B, cu_seqlens=cu, initial_state=S0,
+        chunk=C, state_update_capacity=cap,
+        capture_count=torch.tensor(counts, dtype=torch.int32, device="cuda"), state_update=su.t)
+    torch.cuda.synchronize()
+    ro, rS, rsu = oracle_mod.recurrent(x.q, x.k, x.v, x.alpha, x.beta, B=B, Hk=HK, Hv=HV, dk=D,
+                                       dv=D, cu_seqlens=x.cu_seqlens,
+                                       initial_state=x.initial_state, capacity=cap,
+                                       capture_count=counts, threads=THREADS)
+    tol = TOL[torch.bfloat16]
+    cuh = x.cu_seqlens.tolist()
+    for b in range(B):
+        sl = slice(cuh[b], cuh[b + 1])
+        assert rel(out[sl], ro[sl]) < tol, b
+        assert rel(fs[b], rS[b]) < tol, b
+    # the capture variant computes the same outputs; the deltas it stores
+    # are the chunked form's, to the path's tolerance
+    assert torch.equal(out, out2) and torch.equal(fs, fs2)
+    off = HV + HK * D
+    for b, nb in enumerate(min(c, cap, L) for c, L in zip(counts, LENGTHS)):
+        if nb > 0:
+            gsu = su.t[b, :nb].cpu().double().numpy()
+            assert np.array_equal(gsu[:, :off], rsu[b, :nb, :off]), b
+            assert rel(su.t[b, :nb, off:], rsu[b, :nb, off:]) < tol, b
+        if nb < cap:
+            assert bool(torch.all(su.untouched((b, slice(nb, cap)))).item()), b
+    assert su.guards_intact()
+
+
+def test_checkpoints(gdn, oracle_mod, case):
+    x = case
+    B, cap = len(LENGTHS), 3
+    g = _dev(x)
+    cu, S0 = x.cu_seqlens.cuda(), x.initial_state.cuda()
+    ck = Guarded((B, cap, HV, D, D), F32)
+    out, fs, _ = gdn.gdn_prefill_chunked_checkpoints(
+        g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=B, cu_seqlens=cu, initial_state=S0,
+        checkpoints=ck.t, checkpoint_capacity=cap, checkpoint_interval=1, chunk=C)
+    torch.cuda.synchronize()
+    ref = oracle_mod.prefix_checkpoints(x.q, x.k, x.v, x.alpha, x.beta, B=B, Hk=HK, Hv=HV,
+                                        dk=D, dv=D, every=C, capacity=cap,
+                                        cu_seqlens=x.cu_seqlens, initial_state=x.initial_state,
+                                        threads=THREADS)
+    for b, tb in enumerate(LENGTHS):
+        n = min(cap, tb // C)
+        for j in range(n):
+            assert rel(ck.t[b, j], ref[b, j]) < TOL[torch.bfloat16], (b, j)
+        if n < cap:
+            assert bool(torch.all(ck.untouched((b, slice(n, cap)))).item()), b
+    assert ck.guards_intact()
+
+
+def test_conventions(gdn, oracle_mod):
+    from gated_deltanet_recurrence_02_gb300.inputs import make_raw_inputs
+    x = make_raw_inputs(2501, lengths=LENGTHS, Hk=HK, Hv=HV, dk=D, dv=D, dtype_qkv="bf16",
+                        dtype_gate="bf16")
+    B = len(LENGTHS)
+    g = _dev(x)
+    out, fs = gdn.gdn_prefill_chunked(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=B,
+                                      cu_seqlens=x.cu_seqlens.cuda(),
+                                      initial_state=x.initial_state.cuda(), scale=x.scale,
+                                      chunk=C, conventions=0x700)
+    torch.cuda.synchronize()
+    rq, rk, ra, rb = oracle_mod.front_end(x.q, x.k, x.alpha, x.beta, qk_l2norm=True,
+                                          alpha_log=True, beta_logit=True)
+    ro, rS, _ = oracle_mod.recurrent(rq, rk, x.v, ra, rb, B=B, Hk=HK, Hv=HV, dk=D, dv=D,
+                                     cu_seqlens=x.cu_seqlens, initial_state=x.initial_state,
+                                     scale=x.scale, threads=THREADS)
+    assert rel(out, ro) < TOL[torch.bfloat16]
+    assert rel(fs, rS) < TOL[torch.bfloat16]
