@@ -25,15 +25,19 @@
 // the workspace.
 //
 // Phase B (prefill_carry_kernel, one CTA per (value head, 32-row dv tile,
-// row), serial over chunks): per chunk two dependent tensor-core steps,
+// row), serial over chunks; a 64-row-tile instance with a two-stage ring
+// takes over when the 32-row grid is larger than the SM count, where
+// throughput rather than the chain's latency decides; it is launched as a
+// programmatic dependent of phase A): per chunk two dependent tensor-core
+// steps,
 //   D1 = [Q; W] S^T                       (M=128: Q S^T and W S^T at once)
 //   Delta = U - (W S^T)                   (threads, fp32)
 //   D2 = K^T diag(w) Delta,  D3 = P' Delta (tensor cores)
 //   S <- gamma_last S + D2,  O = gamma (Q S^T) + D3
 // The state tile lives in fp32 registers (thread j owns column j of S, i.e.
-// row j of S^T, for the tile's 32 rows) and is re-packed to bf16/fp16 in
+// row j of S^T, for half of the tile's rows) and is re-packed to bf16/fp16 in
 // shared memory as the next chunk's MMA operand.  Chunk operands stream in
-// through a three-stage TMA / bulk-copy ring, with L2 prefetches further
+// through a TMA / bulk-copy ring, with L2 prefetches further
 // ahead; the output MMA (P' Delta) is committed separately so the state
 // update never waits for it, and the next chunk's first MMA is issued as soon
 // as the state image is written.  At a requested chunk boundary the fp32
