@@ -701,8 +701,8 @@ PREFILL_LAUNCHES = 2  # kernels one gdn_prefill_chunked call launches on this wo
 # DRAM bytes (read + write) of one launch, from one ncu capture of the current
 # kernels: decode at B=256 (profiles/recurrent_decode_B256_traffic.md) and the
 # fused replay + verify step (profiles/replay_verify_B256_T4.md).
-DECODE_TRAFFIC_BYTES = 541_223_680 + 483_353_856
-VERIFY_TRAFFIC_BYTES = 567_209_216 + 391_220_736
+DECODE_TRAFFIC_BYTES = 541_250_304 + 483_723_776
+VERIFY_TRAFFIC_BYTES = 567_168_768 + 391_290_624
 
 
 E2E_GROUPS = 8       # decode e2e: row groups pipelined on their own streams
