@@ -132,3 +132,35 @@ def test_conventions(gdn, oracle_mod):
                                      scale=x.scale, threads=THREADS)
     assert rel(out, ro) < TOL[torch.bfloat16]
     assert rel(fs, rS) < TOL[torch.bfloat16]
+
+
+def test_prefill_batch_B64_sampled_units(gdn, oracle_mod):
+    """The benchmark's packed batch (64 rows of 500..1500 tokens, 64.7k in
+    all, the 64-row carry instance) at full size: sampled (row, head) units
+    against the oracle run on those rows alone (rows are independent)."""
+    from gated_deltanet_recurrence_02_gb300.inputs import WORKLOADS, make_inputs, ragged_lengths
+    w = WORKLOADS["prefill_batch_B64"]
+    lengths = ragged_lengths(w["seed"], w["B"], w["lo"], w["hi"])
+    dims = dict(Hk=w["Hk"], Hv=w["Hv"], dk=w["dk"], dv=w["dv"])
+    x = make_inputs(w["seed"] + 1, lengths=lengths, dtype_qkv=w["dtype_qkv"],
+                    dtype_gate=w["dtype_gate"], **dims)
+    B = w["B"]
+    g = {n: getattr(x, n).cuda() for n in ("q", "k", "v", "alpha", "beta", "initial_state")}
+    out, fs = gdn.gdn_prefill_chunked(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=B,
+                                      cu_seqlens=x.cu_seqlens.cuda(),
+                                      initial_state=g["initial_state"], chunk=w["chunk"])
+    torch.cuda.synchronize()
+    out, fs = out.cpu(), fs.cpu()
+    del g
+    rows = sorted({0, 17, B - 1, int(np.argmin(lengths)), int(np.argmax(lengths))})
+    heads = [0, 13, w["Hv"] - 1]
+    cu = x.cu_seqlens.tolist()
+    tol = TOL[torch.bfloat16]
+    for b in rows:
+        sl = slice(cu[b], cu[b + 1])
+        ro, rS, _ = oracle_mod.recurrent(x.q[sl], x.k[sl], x.v[sl], x.alpha[sl], x.beta[sl], B=1,
+                                         T=lengths[b], initial_state=x.initial_state[b:b + 1],
+                                         units=[(0, hh) for hh in heads], threads=THREADS, **dims)
+        for hh in heads:
+            assert rel(out[sl, hh], ro[:, hh]) < tol, (b, hh)
+            assert rel(fs[b, hh], rS[0, hh]) < tol, (b, hh)
