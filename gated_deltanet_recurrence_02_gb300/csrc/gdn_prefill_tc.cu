@@ -695,8 +695,10 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     const size_t rec_stride = (size_t)Hv * REC_BYTES;
 
     if (tid == 0) {
-        prefetch_tensormap(&mq);
-        prefetch_tensormap(&mk);
+        if (nc > 0) {  // with no token at all the maps are left unencoded
+            prefetch_tensormap(&mq);
+            prefetch_tensormap(&mk);
+        }
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);

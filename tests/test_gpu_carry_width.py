@@ -164,3 +164,33 @@ def test_prefill_batch_B64_sampled_units(gdn, oracle_mod):
         for hh in heads:
             assert rel(out[sl, hh], ro[:, hh]) < tol, (b, hh)
             assert rel(fs[b, hh], rS[0, hh]) < tol, (b, hh)
+
+
+@pytest.mark.parametrize("Hv", [4, 32])
+def test_empty_rows_tensor_core_path(gdn, oracle_mod, Hv):
+    """Rows of length 0 next to ragged ones on the tensor-core prefill (both
+    carry instances: Hv = 4 takes the 32-row tiles, Hv = 32 the 64-row ones),
+    and a call whose rows are all empty: every empty row keeps its initial
+    state bit for bit, the others match the oracle."""
+    from gated_deltanet_recurrence_02_gb300.inputs import make_inputs
+    for lengths in ([0, 70, 0, 1, 129, 0], [0, 0]):
+        x = make_inputs(2600 + Hv + len(lengths), lengths=lengths, Hk=2, Hv=Hv, dk=D, dv=D,
+                        dtype_qkv="bf16", dtype_gate="bf16")
+        B = len(lengths)
+        g = _dev(x)
+        S0 = x.initial_state.cuda()
+        out, fs = gdn.gdn_prefill_chunked(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=B,
+                                          cu_seqlens=x.cu_seqlens.cuda(), initial_state=S0,
+                                          chunk=C)
+        torch.cuda.synchronize()
+        assert gdn.gdn_device_errors() == 0
+        for b, L in enumerate(lengths):
+            if L == 0:
+                assert torch.equal(fs[b], S0[b]), b
+        if sum(lengths) == 0:
+            continue
+        ro, rS, _ = oracle_mod.recurrent(x.q, x.k, x.v, x.alpha, x.beta, B=B, Hk=2, Hv=Hv,
+                                         dk=D, dv=D, cu_seqlens=x.cu_seqlens,
+                                         initial_state=x.initial_state, threads=THREADS)
+        assert rel(out, ro) < TOL[torch.bfloat16]
+        assert rel(fs, rS) < TOL[torch.bfloat16]
