@@ -162,3 +162,49 @@ def test_speculative_loop_as_two_alternating_graphs(gdn):
         torch.cuda.synchronize()
         assert torch.equal(out_g, outs_e[s]), s
     assert torch.equal(S_g, S_e)
+
+
+@pytest.mark.parametrize("path", ["tensor_core", "cuda_core"])
+def test_prefill_graph_replay(gdn, path):
+    """The chunked prefill (packed rows; on the tensor-core path the carry
+    kernel is a programmatic dependent of the chunk-parallel one) captured
+    into a CUDA graph over static buffers and replayed with new inputs: bit
+    for bit the eager calls."""
+    from gated_deltanet_recurrence_02_gb300.inputs import make_inputs
+    d, dt, chunk = (128, "bf16", 64) if path == "tensor_core" else (64, "f32", 32)
+    lengths = [150, 64, 0, 37]
+    B = len(lengths)
+    xs = [make_inputs(2400 + i, lengths=lengths, Hk=2, Hv=4, dk=d, dv=d, dtype_qkv=dt,
+                      dtype_gate=dt) for i in range(3)]
+    names = ("q", "k", "v", "alpha", "beta", "initial_state")
+    cu = xs[0].cu_seqlens.cuda()
+    T = int(xs[0].cu_seqlens[-1])
+    ws_bytes = gdn.gdn_prefill_workspace_size(B, T, 2, 4, d, d, chunk, xs[0].q.dtype, varlen=True)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+    # eager
+    ref = []
+    for x in xs:
+        g = {n: getattr(x, n).cuda() for n in names}
+        o, fs = gdn.gdn_prefill_chunked(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=B,
+                                        cu_seqlens=cu, initial_state=g["initial_state"],
+                                        chunk=chunk, workspace=ws)
+        torch.cuda.synchronize()
+        ref.append((o.clone(), fs.clone()))
+    # graph over static buffers
+    inp = {n: getattr(xs[0], n).cuda() for n in names}
+    out = torch.empty_like(inp["v"])
+    fs = torch.empty_like(inp["initial_state"])
+
+    def call():
+        gdn.gdn_prefill_chunked(inp["q"], inp["k"], inp["v"], inp["alpha"], inp["beta"], B=B,
+                                cu_seqlens=cu, initial_state=inp["initial_state"], final_state=fs,
+                                out=out, chunk=chunk, workspace=ws)
+
+    gr = _capture(call)
+    for x, (ro, rfs) in zip(xs, ref):
+        for n in names:
+            inp[n].copy_(getattr(x, n))
+        gr.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ro) and torch.equal(fs, rfs)
+    assert gdn.gdn_device_errors() == 0
