@@ -143,3 +143,52 @@ def test_eight_value_heads_per_key_head(gdn, oracle_mod):
                                         Hk=Hk, Hv=Hv, dk=d, dv=d, T=m,
                                         initial_state=x.initial_state[b:b + 1])
         assert rel(Sr[b], Sm[0]) < TOL[torch.bfloat16], b
+
+
+@pytest.mark.parametrize("path", ["tensor_core_prefill", "cuda_core_prefill", "recurrent"])
+def test_one_value_head_per_key_head(gdn, oracle_mod, path):
+    """Hk = Hv = 4 (G = 1, no key sharing) on each path; the recurrent path
+    with capture (a key stored per value head) and a replay of the capture."""
+    from gated_deltanet_recurrence_02_gb300.inputs import make_inputs
+    Hk = Hv = 4
+    d, dt, chunk = (128, "bf16", 64) if path != "cuda_core_prefill" else (64, "f32", 32)
+    lengths, cap, counts = [100, 9, 64], 5, [5, 3, 0]
+    x = make_inputs(1950, lengths=lengths, Hk=Hk, Hv=Hv, dk=d, dv=d, dtype_qkv=dt, dtype_gate=dt)
+    g = to_dev(x)
+    B = len(lengths)
+    su = None
+    if path == "recurrent":
+        su = Guarded((B, cap, gdn.slot_width(Hk, Hv, d, d)), F32)
+        out, fs, _ = gdn.gdn_recurrent_capture(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=B,
+                                               cu_seqlens=g["cu_seqlens"],
+                                               initial_state=g["initial_state"],
+                                               state_update_capacity=cap,
+                                               capture_count=torch.tensor(counts, dtype=torch.int32,
+                                                                          device="cuda"),
+                                               state_update=su.t)
+    else:
+        out, fs = gdn.gdn_prefill_chunked(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=B,
+                                          cu_seqlens=g["cu_seqlens"],
+                                          initial_state=g["initial_state"], chunk=chunk)
+    torch.cuda.synchronize()
+    ro, rS, rsu = oracle_mod.recurrent(x.q, x.k, x.v, x.alpha, x.beta, B=B, Hk=Hk, Hv=Hv, dk=d,
+                                       dv=d, cu_seqlens=x.cu_seqlens,
+                                       initial_state=x.initial_state, capacity=cap if su else 0,
+                                       capture_count=counts if su else None, threads=THREADS)
+    tol = TOL[DT[dt]]
+    assert rel(out, ro) < tol
+    assert rel(fs, rS) < tol
+    if su is not None:
+        check_capture(su, rsu, counts, x, cap)
+        acc = [4, 3, 0]
+        Sr = gdn.gdn_replay_state_updates(g["initial_state"], su.t,
+                                          torch.tensor(acc, dtype=torch.int32, device="cuda"),
+                                          state_update_capacity=cap, Hk=Hk)
+        torch.cuda.synchronize()
+        for b, m in enumerate(acc):
+            t0 = int(x.cu_seqlens[b])
+            sl = slice(t0, t0 + m)
+            _, Sm, _ = oracle_mod.recurrent(x.q[sl], x.k[sl], x.v[sl], x.alpha[sl], x.beta[sl], B=1,
+                                            Hk=Hk, Hv=Hv, dk=d, dv=d, T=m,
+                                            initial_state=x.initial_state[b:b + 1])
+            assert rel(Sr[b], Sm[0]) < tol, b
