@@ -71,7 +71,8 @@ def test_ragged_f32_cuda_core_path(gdn, oracle_mod, interval):
     assert torch.equal(out, out0) and torch.equal(fs, fs0)
 
 
-def test_ragged_bf16_tensor_core_path(gdn, oracle_mod):
+@pytest.mark.parametrize("interval", [1, 3])
+def test_ragged_bf16_tensor_core_path(gdn, oracle_mod, interval):
     from gated_deltanet_recurrence_02_gb300.inputs import make_inputs
     lengths, Hk, Hv, d, C, cap = [200, 64, 130, 50], 2, 4, 128, 64, 3
     x = make_inputs(1201, lengths=lengths, Hk=Hk, Hv=Hv, dk=d, dv=d, dtype_qkv="bf16",
@@ -83,15 +84,16 @@ def test_ragged_bf16_tensor_core_path(gdn, oracle_mod):
     ck = Guarded((B, cap, Hv, d, d), F32)
     out, fs, _ = gdn.gdn_prefill_chunked_checkpoints(
         g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=B, cu_seqlens=cu, initial_state=S0,
-        checkpoints=ck.t, checkpoint_capacity=cap, checkpoint_interval=1, chunk=C)
+        checkpoints=ck.t, checkpoint_capacity=cap, checkpoint_interval=interval, chunk=C)
     out0, fs0 = gdn.gdn_prefill_chunked(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=B,
                                         cu_seqlens=cu, initial_state=S0, chunk=C)
     torch.cuda.synchronize()
+    L = interval * C
     ref = oracle_mod.prefix_checkpoints(x.q, x.k, x.v, x.alpha, x.beta, B=B, Hk=Hk, Hv=Hv,
-                                        dk=d, dv=d, every=C, capacity=cap,
+                                        dk=d, dv=d, every=L, capacity=cap,
                                         cu_seqlens=x.cu_seqlens, initial_state=x.initial_state,
                                         threads=THREADS)
-    _check_slots(ck, ref, lengths, C, cap, TOL[torch.bfloat16])
+    _check_slots(ck, ref, lengths, L, cap, TOL[torch.bfloat16])
     assert torch.equal(out, out0) and torch.equal(fs, fs0)
 
 
