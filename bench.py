@@ -903,6 +903,28 @@ def cpu_cores() -> int:
         return os.cpu_count() or 1
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (x86 /proc/cpuinfo, else lscpu, else the
+    machine type)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        import subprocess
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.machine()
+
+
 def cpu_baseline():
     import oracle
     oracle.build()
@@ -910,10 +932,18 @@ def cpu_baseline():
     rows = CPU_SAMPLE_ROWS
     x = oracle_decode_sample(rows, DEC["seed"])
     val, sec = time_oracle_decode(x, rows, cores)
+    # the same oracle on one thread, over a sixteenth of the rows
+    rows1 = max(1, rows // 16)
+    x1 = oracle_decode_sample(rows1, DEC["seed"])
+    val1, sec1 = time_oracle_decode(x1, rows1, 1)
     return {"value": round(val, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"decode: {rows} of 256 rows x 32 heads x 64 single-token steps "
                       f"(fp64 C oracle, {cores} threads over (row, head) units, "
-                      f"{sec:.2f} s wall)"}
+                      f"{sec:.2f} s wall)",
+            "single_thread": {"value": round(val1, 4), "unit": "GB/s",
+                              "sample": f"decode: {rows1} rows x 32 heads x 64 single-token steps "
+                                        f"on one thread, {sec1:.2f} s wall"},
+            "cpu_model": cpu_model()}
 
 
 def run_reference(args, rank, world):
@@ -943,7 +973,7 @@ def run_reference(args, rank, world):
                    "steps_per_call_chain": DEC["steps"], "Hk": DEC["Hk"], "Hv": DEC["Hv"],
                    "dk": DEC["dk"], "dv": DEC["dv"], "capacity": DEC["cap"]},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample, "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
