@@ -36,9 +36,10 @@
  *    except where an entry point allows an exact in-place state.
  *  - A failed launch returns GDN_ERR_CUDA; the CUDA error is left for the
  *    caller's next cudaGetLastError.
- *  - Calls can be captured into CUDA graphs.  The first call of a process on
- *    a device sets kernel attributes and resolves the device error word (CUDA
- *    runtime calls); make it before stream capture starts.  Later calls only
+ *  - Calls can be captured into CUDA graphs.  The first call on a device
+ *    that runs a given kernel sets that kernel's attributes (and the first
+ *    call of all resolves the device error word): CUDA runtime calls, so make
+ *    one call of each kind before stream capture starts.  Later calls only
  *    launch kernels.  The tensor-core prefill launches its second kernel as a
  *    programmatic dependent of its first (captured as a programmatic edge).
  *
