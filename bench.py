@@ -698,9 +698,9 @@ def run_front_end(gdn, stream, q, k, v, a, bt, S, out, cc, su, gp, p_out, p_fs, 
 
 
 PREFILL_LAUNCHES = 2  # kernels one gdn_prefill_chunked call launches on this workload (tensor-core path)
-# DRAM bytes (read + write) of one launch, from one ncu capture of the current
-# kernels: decode at B=256 (profiles/recurrent_decode_B256_traffic.md) and the
-# fused replay + verify step (profiles/replay_verify_B256_T4.md).
+# DRAM bytes (read + write) of one launch of the current kernels, each from one
+# ncu capture of that kernel on this workload: decode at B=256 and the fused
+# replay + verify step.  Reset to None whenever the kernel changes.
 DECODE_TRAFFIC_BYTES = 541_250_304 + 483_723_776
 VERIFY_TRAFFIC_BYTES = 567_168_768 + 391_290_624
 
@@ -925,6 +925,50 @@ def cpu_model() -> str:
     return platform.machine()
 
 
+def time_oracle_prefill(x, B, units, threads):
+    """The oracle (the per-token recurrence, fp64) over `units` (row, head)
+    pairs of a prefill workload; returns (tokens/s scaled by the share of
+    units done, seconds)."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.recurrent(x.q, x.k, x.v, x.alpha, x.beta, B=B, Hk=x.Hk, Hv=x.Hv, dk=x.dk, dv=x.dv,
+                     cu_seqlens=x.cu_seqlens, initial_state=x.initial_state, units=units,
+                     threads=threads)
+    sec = time.perf_counter() - t0
+    total_units = B * x.Hv
+    return x.total_T * (len(units) / total_units) / sec, sec
+
+
+def cpu_baseline_prefill(cores):
+    """Oracle tokens/s on the two prefill workloads: every (row, head) unit on
+    all host cores, and a sixteenth of the units on one thread (scaled by the
+    share of units done)."""
+    from gated_deltanet_recurrence_02_gb300.inputs import WORKLOADS, make_inputs, ragged_lengths
+    res = {}
+    w = WORKLOADS["prefill_T4100"]
+    xp = make_inputs(w["seed"], lengths=w["lengths"], Hk=w["Hk"], Hv=w["Hv"], dk=w["dk"],
+                     dv=w["dv"], dtype_qkv=w["dtype_qkv"], dtype_gate=w["dtype_gate"])
+    ws = WORKLOADS["prefix_snapshot_B12"]
+    lens = ragged_lengths(ws["seed"] + 1, ws["B"], ws["lo"], ws["hi"])
+    xs = make_inputs(ws["seed"] + 2, lengths=lens, Hk=ws["Hk"], Hv=ws["Hv"], dk=ws["dk"],
+                     dv=ws["dv"], dtype_qkv=ws["dtype_qkv"], dtype_gate=ws["dtype_gate"],
+                     zero_state=True)  # (the snapshot's values do not change the work)
+    for name, x, B in (("prefill_T4100", xp, 1), ("prefix_snapshot_B12", xs, ws["B"])):
+        units = [(b, h) for b in range(B) for h in range(x.Hv)]
+        val, sec = time_oracle_prefill(x, B, units, cores)
+        one = units[::16]
+        val1, sec1 = time_oracle_prefill(x, B, one, 1)
+        res[name] = {"value": round(val, 1), "unit": "tokens/s", "cores": cores,
+                     "sample": f"all {len(units)} (row, head) units, {x.total_T} tokens "
+                               f"(fp64 C oracle, per-token recurrence, {cores} threads, "
+                               f"{sec:.2f} s wall)",
+                     "single_thread": {"value": round(val1, 1), "unit": "tokens/s",
+                                       "sample": f"{len(one)} of {len(units)} units on one "
+                                                 f"thread, scaled by the share of units, "
+                                                 f"{sec1:.2f} s wall"}}
+    return res
+
+
 def cpu_baseline():
     import oracle
     oracle.build()
@@ -943,6 +987,7 @@ def cpu_baseline():
             "single_thread": {"value": round(val1, 4), "unit": "GB/s",
                               "sample": f"decode: {rows1} rows x 32 heads x 64 single-token steps "
                                         f"on one thread, {sec1:.2f} s wall"},
+            "prefill": cpu_baseline_prefill(cores),
             "cpu_model": cpu_model()}
 
 

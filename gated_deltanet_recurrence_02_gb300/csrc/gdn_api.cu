@@ -1,8 +1,10 @@
 // gdn_api.cu -- the C ABI of libgdn (include/gdn.h): argument validation,
 // buffer-overlap checks and kernel dispatch.  Host code only; every check
 // runs before anything is launched, so a rejected call has no side effects.
+#include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "gdn_internal.cuh"
 
@@ -15,22 +17,38 @@ __device__ uint32_t g_device_errors = 0;
 namespace {
 
 constexpr int kMaxDevices = 64;
-uint32_t *g_err_addr[kMaxDevices] = {};
+// Per-device cache of the error word's address.  Filled under the mutex by
+// the first call on a device; read lock-free afterwards (acquire pairs with
+// the release store), so concurrent first calls from several host threads
+// are safe.
+std::atomic<uint32_t *> g_err_addr[kMaxDevices] = {};
+std::mutex g_err_mutex;
 
 cudaError_t error_word(uint32_t **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    if (g_err_addr[dev] == nullptr) {
-        void *ptr = nullptr;
-        e = cudaGetSymbolAddress(&ptr, g_device_errors);
-        if (e != cudaSuccess) return e;
-        g_err_addr[dev] = static_cast<uint32_t *>(ptr);
+    uint32_t *a = g_err_addr[dev].load(std::memory_order_acquire);
+    if (a == nullptr) {
+        std::lock_guard<std::mutex> lock(g_err_mutex);
+        a = g_err_addr[dev].load(std::memory_order_relaxed);
+        if (a == nullptr) {
+            void *ptr = nullptr;
+            e = cudaGetSymbolAddress(&ptr, g_device_errors);
+            if (e != cudaSuccess) return e;
+            a = static_cast<uint32_t *>(ptr);
+            g_err_addr[dev].store(a, std::memory_order_release);
+        }
     }
-    *out = g_err_addr[dev];
+    *out = a;
     return cudaSuccess;
 }
+
+// Limit of the kernels' waits on work of another warp (see
+// gdn_set_wait_limit_ns); the waits for the CTA's own copies in flight keep
+// the full limit.
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 
 size_t dtype_bytes(int dt) {
     switch (dt) {
@@ -197,7 +215,7 @@ int gdn_recurrent_capture(const void *q, const void *k, const void *v, const voi
     if (st != GDN_OK) return st;
     if (B == 0) return GDN_OK;
 
-    RecurrentParams p;
+    RecurrentParams p{};
     p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.beta = beta;
     p.cu_seqlens = cu_seqlens;
     p.s0 = initial_state; p.s0_idx = initial_state_indices; p.n_s0 = num_initial_states;
@@ -207,6 +225,7 @@ int gdn_recurrent_capture(const void *q, const void *k, const void *v, const voi
     p.capacity = cap; p.capture_count = capture_count; p.active = state_update_active;
     p.su = cap > 0 ? state_update : nullptr;
     p.rp_su = nullptr; p.rp_capacity = 0; p.rp_accepted = nullptr; p.s_commit = nullptr;
+    p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
     if (error_word(&p.err) != cudaSuccess) return GDN_ERR_CUDA;
     return launch_recurrent(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
@@ -268,7 +287,7 @@ int gdn_replay_verify(const void *q, const void *k, const void *v, const void *a
     if (st != GDN_OK) return st;
     if (B == 0) return GDN_OK;
 
-    RecurrentParams p;
+    RecurrentParams p{};
     p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.beta = beta;
     p.cu_seqlens = cu_seqlens;
     p.s0 = state_in; p.s0_idx = nullptr; p.n_s0 = B;
@@ -281,6 +300,7 @@ int gdn_replay_verify(const void *q, const void *k, const void *v, const void *a
     p.rp_capacity = prev_capacity;
     p.rp_accepted = prev_capacity > 0 ? accepted_count : nullptr;
     p.s_commit = state_out;
+    p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
     if (error_word(&p.err) != cudaSuccess) return GDN_ERR_CUDA;
     return launch_recurrent(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
@@ -311,22 +331,28 @@ int gdn_replay_state_updates(const float *state_in, float *state_out, const floa
     int st = check_alias(spans, 4, 0, 3);
     if (st != GDN_OK) return st;
     if (B == 0) return GDN_OK;
-    ReplayParams p;
+    ReplayParams p{};
     p.s_in = state_in; p.s_out = state_out; p.su = state_update;
     p.capacity = state_update_capacity; p.accepted = accepted_count;
     p.B = B; p.Hk = Hk; p.Hv = Hv; p.dk = dk; p.dv = dv;
+    p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
     if (error_word(&p.err) != cudaSuccess) return GDN_ERR_CUDA;
     return launch_replay(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 size_t gdn_prefill_workspace_size(int B, int T, int Hk, int Hv, int dk, int dv, int chunk,
                                   int dtype_qkv, int varlen) {
-    if (B < 0 || T < 0 || Hk <= 0 || Hv <= 0 || dk <= 0 || dv <= 0 || chunk <= 0 ||
-        dtype_bytes(dtype_qkv) == 0)
+    // the storage type decides; the GDN_QK_L2NORM convention bit changes nothing here
+    int conv = 0, dt = 0;
+    if (!split_dtype(dtype_qkv, GDN_QK_L2NORM, &dt, &conv)) return (size_t)-1;
+    if (B < 0 || T < 0 || Hk <= 0 || Hv <= 0 || dk <= 0 || dv <= 0 || chunk <= 0 || dtype_bytes(dt) == 0)
         return (size_t)-1;
-    if (prefill_tc_supported(dk, dv, chunk, dtype_qkv))
-        return prefill_tc_workspace_bytes(B, T, Hv, varlen != 0);
+    if (prefill_tc_supported(dk, dv, chunk, dt)) return prefill_tc_workspace_bytes(B, T, Hk, Hv, varlen != 0);
     return 0;
+}
+
+void gdn_set_wait_limit_ns(uint64_t ns) {
+    g_wait_ns.store(ns == 0 ? kDefaultWaitNs : ns, std::memory_order_relaxed);
 }
 
 }  // extern "C"
@@ -402,7 +428,7 @@ int prefill_call(const void *q, const void *k, const void *v, const void *alpha,
     if (st != GDN_OK) return st;
     if (B == 0) return GDN_OK;
 
-    PrefillParams p;
+    PrefillParams p{};
     p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.beta = beta;
     p.cu_seqlens = cu_seqlens;
     p.s0 = initial_state; p.s0_idx = initial_state_indices; p.n_s0 = num_initial_states;
@@ -417,6 +443,7 @@ int prefill_call(const void *q, const void *k, const void *v, const void *alpha,
     p.active = capacity > 0 ? state_update_active : nullptr;
     p.su = capacity > 0 ? state_update : nullptr;
     p.chunk_table = nullptr;  // set by the tensor-core launcher for packed rows
+    p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
     if (error_word(&p.err) != cudaSuccess) return GDN_ERR_CUDA;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     const cudaError_t e = use_tc ? launch_prefill_tc(p, s) : launch_prefill_simt(p, s);

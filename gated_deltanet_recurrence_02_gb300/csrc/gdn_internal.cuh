@@ -14,7 +14,11 @@
 namespace gdn {
 
 // Every parameter block carries `err`: the device address of the library's
-// error word (GDN_DEVERR_* bits), resolved by the host layer per device.
+// error word (GDN_DEVERR_* bits), resolved by the host layer per device, and
+// `wait_ns`: the limit of waits on another warp's work (kDefaultWaitNs unless
+// a test lowered it with gdn_set_wait_limit_ns).  Waits for a CTA's own copies
+// in flight, before it exits, always use kDefaultWaitNs.
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;
 
 // ---------------------------------------------------------------- params --
 
@@ -42,6 +46,7 @@ struct RecurrentParams {
     int rp_capacity;
     const int32_t *rp_accepted;
     float *s_commit;
+    uint64_t wait_ns;
     uint32_t *err;
 };
 
@@ -52,6 +57,7 @@ struct ReplayParams {
     int capacity;
     const int32_t *accepted;
     int B, Hk, Hv, dk, dv;
+    uint64_t wait_ns;
     uint32_t *err;
 };
 
@@ -85,6 +91,7 @@ struct PrefillParams {
     // every row (B + 1 entries), written into the head of the workspace by a
     // prologue kernel; nullptr for uniform rows.
     const int32_t *chunk_table;
+    uint64_t wait_ns;
     uint32_t *err;
 };
 
@@ -125,7 +132,7 @@ cudaError_t launch_prefill_simt(const PrefillParams &p, cudaStream_t stream);
 bool prefill_simt_supported(int dk, int dv, int chunk);
 cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t stream);
 bool prefill_tc_supported(int dk, int dv, int chunk, int dt_qkv);
-size_t prefill_tc_workspace_bytes(int B, int T, int Hv, bool varlen);
+size_t prefill_tc_workspace_bytes(int B, int T, int Hk, int Hv, bool varlen);
 
 // Raises kernel Kern's dynamic shared-memory limit to `bytes`, once per device
 // (function attributes belong to the device's context): later calls make no

@@ -68,7 +68,7 @@ using namespace tc;
 
 constexpr int C = 64;    // chunk
 constexpr int D = 128;   // dk = dv
-constexpr uint64_t kWaitNs = 1000000000ull;
+constexpr uint64_t kWaitNs = kDefaultWaitNs;  // drains of the CTA's own copies
 
 // Workspace record per (chunk, value head), bytes.
 constexpr uint32_t REC_W = 0;         // W image: 2 SW128 blocks (dk 0-63, 64-127) x 64 rows
@@ -410,7 +410,7 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     bool ok = true;
     if (tid == 0) {
         // [K; Q] K^T -> TMEM cols [0, 64): rows 0-63 K K^T, rows 64-127 Q K^T
-        ok = mbar_wait(bar_ld, 0, kWaitNs);
+        ok = mbar_wait(bar_ld, 0, p.wait_ns);
         if (ok) {
             fence_after_sync();
             const uint64_t d0 = desc_sw128(smem_u32(sKQ), 16, 1024);
@@ -445,7 +445,7 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     if constexpr (NORM) {
         // 1/|k_t| and 1/|q_t| from the staged tiles (rows 0-63 K, 64-127 Q;
         // two threads per row, one per 64-column block), before V replaces Q
-        if (!mbar_wait(bar_ld, 0, kWaitNs)) ok = false;
+        if (!mbar_wait(bar_ld, 0, p.wait_ns)) ok = false;
         const int r = tid >> 1, kb = tid & 1;
         float ss = 0.f;
 #pragma unroll
@@ -480,8 +480,9 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
                 ld_f(kg + ((tok0 + t) * Hk + hk) * D + j) * (NORM ? vkn[t] : 1.f);
         }
     }
-    ok = ok && mbar_wait(bar_mma, 0, kWaitNs);
+    ok = ok && mbar_wait(bar_mma, 0, p.wait_ns);
     fence_after_sync();
+    const bool v_issued = ok;  // the same for every thread (ok is uniform after the wait)
     if (ok && tid == 0) {
         // Q has been consumed: V takes its place (the load overlaps A, P' and T)
         mbar_arrive_expect_tx(bar_v, 16384);
@@ -553,7 +554,7 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     // ---- U = [T b ; T b g] V (rows 0-63 used) -> TMEM cols [0, 128)
     if (ok && tid == 0) {
         fence_after_sync();
-        ok = mbar_wait(bar_v, 0, kWaitNs);
+        ok = mbar_wait(bar_v, 0, p.wait_ns);
         if (ok) {
             const uint64_t a0 = desc_sw128(smem_u32(sImg), 16, 1024), b0 = desc_sw128(smem_u32(sm + A_V0), 16384, 1024);
             const uint32_t id = idesc_f16(128, 128, false, true, kbf);
@@ -562,7 +563,7 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
             mma_commit(bar_mma);
         }
     }
-    ok = ok && mbar_wait(bar_mma, 1, kWaitNs);
+    ok = ok && mbar_wait(bar_mma, 1, p.wait_ns);
     fence_after_sync();
     if (ok && (warp & 3) < 2) {
         // U as four thread-read tiles of 32 dv columns: [64 t][32 i], 16-byte chunks swizzled by t
@@ -590,7 +591,7 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
         for (int k = 0; k < 4; ++k) mma_f16(tbase, desc_add(a0, k * 32), desc_add(b0, k * 2048), id, k > 0);
         mma_commit(bar_mma);
     }
-    ok = ok && mbar_wait(bar_mma, 0, kWaitNs);
+    ok = ok && mbar_wait(bar_mma, 0, p.wait_ns);
     fence_after_sync();
     if (ok && (warp & 3) >= 2) {
         const int t = 32 * ((warp & 3) - 2) + lane, half = warp >> 2;
@@ -609,7 +610,7 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
         if (tid == 0) atomicOr(p.err, (uint32_t)GDN_DEVERR_TIMEOUT);
         // copies in flight must land before the CTA exits
         mbar_wait(bar_ld, 0, kWaitNs);
-        mbar_wait(bar_v, 0, kWaitNs / 4);
+        if (v_issued) mbar_wait(bar_v, 0, kWaitNs);
     }
     fence_before_sync();
     __syncthreads();
@@ -751,7 +752,7 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
             for (int cc = NS; cc < NS + 2 && cc < nc; ++cc) prefetch_chunk(cc);
             for (int cc = NS; cc < nc; ++cc) {
                 // chunk cc reuses the stage of chunk cc - NS
-                if (!mbar_wait(&empty[cc % NS], (cc / NS - 1) & 1, kWaitNs)) {
+                if (!mbar_wait(&empty[cc % NS], (cc / NS - 1) & 1, p.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -775,7 +776,7 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
             const int s = cc % NS;
             uint8_t *st = sm + s * Cfg::ST_BYTES;
             if (lane == 0) {
-                ok = mbar_wait(&full[s], (cc / NS) & 1, kWaitNs);
+                ok = mbar_wait(&full[s], (cc / NS) & 1, p.wait_ns);
                 if (ok) {
                     // D1 = [Q; W] S^T
                     const uint64_t a0 = desc_sw128(smem_u32(st + Cfg::ST_A1), 16, 1024);
@@ -841,14 +842,14 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
             const uint32_t d1 = (cc & 1) ? (uint32_t)TV : 0u;
             const uint32_t d3 = Cfg::T_D3 + ((cc & 1) ? (uint32_t)TV : 0u);
             const int n = min(C, len - cc * C);
-            if (ok) ok = mbar_wait(&full[s], (cc / NS) & 1, kWaitNs);
+            if (ok) ok = mbar_wait(&full[s], (cc / NS) & 1, p.wait_ns);
             const float *vec = reinterpret_cast<const float *>(st + Cfg::ST_VEC);
             const float gC = ok ? vec[128] : 0.f;
             if (quarter >= 2) {
                 // Delta = U - W S^T for token t, NC of the TV columns
                 const int t = 32 * (quarter - 2) + lane;
                 const float wt = ok ? vec[64 + t] : 0.f;
-                if (ok) ok = mbar_wait(bar1, cc & 1, kWaitNs);
+                if (ok) ok = mbar_wait(bar1, cc & 1, p.wait_ns);
                 if (ok) {
                     fence_after_sync();
                     float ws[NC];
@@ -884,7 +885,7 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
             named_bar(kBarDelta, kBarThreads);
             fence_after_sync();
             // S <- gamma_last S + K^T diag(w) Delta   (TMEM lane j = dk index)
-            if (ok) ok = mbar_wait(bar2, cc & 1, kWaitNs);
+            if (ok) ok = mbar_wait(bar2, cc & 1, p.wait_ns);
             if (ok) {
                 fence_after_sync();
                 float v[NC];
@@ -911,7 +912,7 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
             if (quarter < 2 && ok) {
                 // O = gamma_t (Q S^T) + P' Delta for token t, NC columns
                 const int t = 32 * quarter + lane;
-                ok = mbar_wait(bar3, cc & 1, kWaitNs);
+                ok = mbar_wait(bar3, cc & 1, p.wait_ns);
                 if (ok) {
                     fence_after_sync();
                     float qs[NC], pd[NC];
@@ -1035,7 +1036,7 @@ bool prefill_tc_supported(int dk, int dv, int chunk, int dt_qkv) {
     return dk == D && dv == D && chunk == C && (dt_qkv == GDN_BF16 || dt_qkv == GDN_F16);
 }
 
-size_t prefill_tc_workspace_bytes(int B, int T, int Hv, bool varlen) {
+size_t prefill_tc_workspace_bytes(int B, int T, int /*Hk*/, int Hv, bool varlen) {
     return (varlen ? chunk_table_bytes(B) : 0) + (size_t)max_chunks_of(B, T, varlen) * (size_t)Hv * REC_BYTES;
 }
 

@@ -145,7 +145,7 @@ recurrent_kernel(const RecurrentParams p) {
         int it = 0;
         for (long id = blockIdx.x; id < n_tiles; id += gridDim.x, ++it) {
             const int stage = it % kStages;
-            if (it >= kStages && !tc::mbar_wait(&empty[stage], ((it / kStages) - 1) & 1, 1000000000ull)) {
+            if (it >= kStages && !tc::mbar_wait(&empty[stage], ((it / kStages) - 1) & 1, p.wait_ns)) {
                 if (lane == 0) atomicOr(p.err, (uint32_t)GDN_DEVERR_TIMEOUT);
                 break;
             }
@@ -233,7 +233,7 @@ recurrent_kernel(const RecurrentParams p) {
         if (lane == 0)
             for (int s = 0; s < kStages && it - 1 - s >= 0; ++s) {
                 const int j = it - 1 - s;
-                tc::mbar_wait(&full[j % kStages], (j / kStages) & 1, 1000000000ull);
+                tc::mbar_wait(&full[j % kStages], (j / kStages) & 1, kDefaultWaitNs);
             }
         return;
     }
@@ -265,7 +265,7 @@ recurrent_kernel(const RecurrentParams p) {
     for (long id = blockIdx.x; id < n_tiles; id += gridDim.x, ++it) {
         const int stage = it % kStages;
         const uint8_t *st = sbase + stage * L::kBytes;
-        if (!tc::mbar_wait(&full[stage], (it / kStages) & 1, 1000000000ull)) {
+        if (!tc::mbar_wait(&full[stage], (it / kStages) & 1, p.wait_ns)) {
             if (threadIdx.x == 0) atomicOr(p.err, (uint32_t)GDN_DEVERR_TIMEOUT);
             break;
         }

@@ -58,6 +58,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Non-blocking test of the phase with `parity`.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
@@ -65,8 +77,11 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 // Waits for the phase with `parity` to complete.  Gives up after `limit_ns`
 // nanoseconds and returns false; the caller records the timeout and unwinds.
+// A limit below one microsecond (a test setting) gives up at the first
+// check that finds the phase incomplete.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity)) return true;
+    if (limit_ns < 1000) return false;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         for (int i = 0; i < 64; ++i)

@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
     L.gdn_device_errors.restype = i
     L.gdn_status_string.argtypes = [i]
     L.gdn_status_string.restype = ctypes.c_char_p
+    L.gdn_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    L.gdn_set_wait_limit_ns.restype = None
     _lib = L
     return L
 
@@ -293,6 +295,13 @@ def gdn_replay_verify(q, k, v, alpha, beta, *, B: int, T: Optional[int] = None,
         _p(state_update_active), _p(state_update), _stream(stream))
     _check(st, "gdn_replay_verify")
     return out, state_out, state_update, draft_final_state
+
+
+def gdn_set_wait_limit_ns(ns: int) -> None:
+    """Testing hook: limit of the kernels' waits on another warp's work, in
+    nanoseconds (0 restores the 1 s default; below 1000 gives up at the first
+    incomplete check)."""
+    lib().gdn_set_wait_limit_ns(int(ns))
 
 
 def gdn_device_errors(stream=None) -> int:

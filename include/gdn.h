@@ -120,8 +120,9 @@ enum { GDN_F32 = 0, GDN_F16 = 1, GDN_BF16 = 2 };
  * gdn_prefill_chunked; varlen != 0 when cu_seqlens will be passed.  The
  * tensor-core path (dk = dv = 128, chunk 64, 16-bit q/k/v) stores about 41 KB
  * per (chunk, value head), plus, with packed rows, a table of every row's
- * first chunk (4 (B + 1) bytes rounded up to 1 KB).  Returns (size_t)-1 for
- * invalid sizes.
+ * first chunk (4 (B + 1) bytes rounded up to 1 KB).  dtype_qkv may carry the
+ * GDN_QK_L2NORM bit (the same code as passed to the prefill; it does not
+ * change the size).  Returns (size_t)-1 for invalid sizes or other flag bits.
  */
 GDN_API size_t gdn_prefill_workspace_size(int B, int T, int Hk, int Hv, int dk, int dv,
                                           int chunk, int dtype_qkv, int varlen);
@@ -356,6 +357,20 @@ enum {
  * set, GDN_ERR_CUDA on a CUDA failure, else GDN_OK.
  */
 GDN_API int gdn_device_errors(void *stream, uint32_t *flags);
+
+/*
+ * gdn_set_wait_limit_ns -- testing hook for the failure path.  Every kernel
+ * bounds its waits on another warp's work (pipeline hand-offs inside a CTA);
+ * a wait that runs out sets GDN_DEVERR_TIMEOUT, the CTA waits (with the full
+ * limit) for its own copies in flight, releases its tensor memory and exits,
+ * and gdn_device_errors then returns GDN_ERR_TIMEOUT.  The limit is 1 s by
+ * default; this sets it, for calls made afterwards from any thread, to `ns`
+ * nanoseconds (0 restores the default).  A limit below 1000 ns gives up at
+ * the first check that finds a hand-off incomplete, which lets a test drive
+ * the timeout path on a small case.  Results of a call whose wait ran out
+ * are unspecified.  Not meant for production use.
+ */
+GDN_API void gdn_set_wait_limit_ns(uint64_t ns);
 
 /* Human-readable text for a status code (static storage). */
 GDN_API const char *gdn_status_string(int status);

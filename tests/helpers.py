@@ -22,6 +22,31 @@ def rel(gpu, ref) -> float:
     return float(np.linalg.norm(g - r) / (den if den > 0 else 1.0))
 
 
+def rel_per_unit(gpu, ref, bounds, keep_axis=1):
+    """Worst relative Frobenius error over units: each unit is the slice
+    [bounds[u], bounds[u+1]) of the leading (token or row) axis and one index
+    of `keep_axis` (the value head), the norm taken over everything else.
+    Returns (worst error, (u, head)).  Units whose reference is all zero are
+    compared absolutely."""
+    g = gpu.detach().cpu().double().numpy() if hasattr(gpu, "detach") else np.asarray(gpu)
+    r = np.asarray(ref, dtype=np.float64)
+    assert g.shape == r.shape, (g.shape, r.shape)
+    assert np.all(np.isfinite(g)), "non-finite values in the GPU result"
+    worst, where = 0.0, None
+    for u in range(len(bounds) - 1):
+        a, b = int(bounds[u]), int(bounds[u + 1])
+        if b <= a:
+            continue
+        d = np.moveaxis(g[a:b] - r[a:b], keep_axis, 0).reshape(g.shape[keep_axis], -1)
+        n = np.moveaxis(r[a:b], keep_axis, 0).reshape(r.shape[keep_axis], -1)
+        num, den = np.linalg.norm(d, axis=1), np.linalg.norm(n, axis=1)
+        e = num / np.where(den > 0, den, 1.0)
+        h = int(np.argmax(e))
+        if e[h] > worst:
+            worst, where = float(e[h]), (u, h)
+    return worst, where
+
+
 class Guarded:
     """A device tensor with sentinel-filled guard bands on both sides."""
 

@@ -15,7 +15,7 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import TOL, TOL_CAPTURE, Guarded, check_capture as _check_capture, rel, to_dev
+from helpers import TOL, TOL_CAPTURE, Guarded, check_capture as _check_capture, rel, rel_per_unit, to_dev
 
 pytestmark = pytest.mark.gpu
 THREADS = min(32, os.cpu_count() or 4)
@@ -172,9 +172,18 @@ def test_prefill_T4100_bf16(gdn, W, oracle_mod):
     assert e_o < TOL[torch.bfloat16] and e_S < TOL[torch.bfloat16], (e_o, e_S)
     # the per-token path on the same inputs
     assert rel(o2, ro) < TOL[torch.bfloat16] and rel(S2, rS) < TOL[torch.bfloat16]
-    # per-chunk check of the ragged tail (last 4 tokens) and the first chunk
-    assert rel(out.t[-4:], ro[-4:]) < TOL[torch.bfloat16]
-    assert rel(out.t[:64], ro[:64]) < TOL[torch.bfloat16]
+    # Per unit: the bound holds for every (64-token chunk, value head) of the
+    # output, the 4-token tail included, and for every value head of the final
+    # state, so that one wrong tile cannot hide in the global norm.  Seen on
+    # GB300: worst (chunk, head) 4.5e-3, worst head state 3.5e-3.
+    tol = TOL[torch.bfloat16]
+    bounds = list(range(0, 4100, 64)) + [4100]
+    e_chunk, at = rel_per_unit(out.t, ro, bounds)
+    assert e_chunk < tol, (e_chunk, at)
+    e_head, at_h = rel_per_unit(fs.t[0], rS[0], [0, x.Hv], keep_axis=0)
+    assert e_head < tol, (e_head, at_h)
+    print(f"T=4100 worst per (chunk, head) output {e_chunk:.2e} at {at}, "
+          f"worst per head state {e_head:.2e}")
 
 
 # ------------------------------------------------ prefix snapshot reuse
@@ -420,5 +429,13 @@ def test_many_packed_rows_tensor_core_prefill(gdn, oracle_mod):
     tol = TOL[torch.bfloat16]
     assert rel(o, ro) < tol
     assert rel(fs, rS) < tol
+    # per (row, value head): outputs over the row's tokens, and final states
+    # (seen on GB300: worst 4.1e-3 and 2.7e-3)
+    e_o, at_o = rel_per_unit(o, ro, [int(c) for c in x.cu_seqlens])
+    assert e_o < tol, (e_o, at_o)
+    e_s, at_s = rel_per_unit(fs, rS, list(range(B + 1)))
+    assert e_s < tol, (e_s, at_s)
+    print(f"300 packed rows: worst per (row, head) output {e_o:.2e} at {at_o}, "
+          f"state {e_s:.2e} at {at_s}")
     empty = [b for b, L in enumerate(lengths) if L == 0]
     assert empty and all(torch.equal(fs[b], g["initial_state"][b]) for b in empty)

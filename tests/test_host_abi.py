@@ -255,6 +255,20 @@ def test_workspace_size_query(L):
     assert L.gdn_prefill_workspace_size(-1, 4100, 16, 32, 128, 128, 64, 2, 0) == ctypes.c_size_t(-1).value
 
 
+def test_workspace_size_accepts_the_prefill_dtype_code(L):
+    """The dtype code a caller passes to the prefill (storage type plus the
+    GDN_QK_L2NORM bit) gives the same workspace size as the bare type; a gate
+    bit or an unknown bit in dtype_qkv is rejected."""
+    QK, ALOG = 0x100, 0x200
+    for B, T, varlen in ((1, 4100, 0), (300, 6000, 1), (2, 100, 0)):
+        bare = L.gdn_prefill_workspace_size(B, T, 16, 32, 128, 128, 64, 2, varlen)
+        assert L.gdn_prefill_workspace_size(B, T, 16, 32, 128, 128, 64, 2 | QK, varlen) == bare
+    assert L.gdn_prefill_workspace_size(2, 100, 1, 2, 32, 32, 16, 0 | QK, 0) == 0
+    bad = ctypes.c_size_t(-1).value
+    assert L.gdn_prefill_workspace_size(1, 4100, 16, 32, 128, 128, 64, 2 | ALOG, 0) == bad
+    assert L.gdn_prefill_workspace_size(1, 4100, 16, 32, 128, 128, 64, 2 | 0x800, 0) == bad
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     from gated_deltanet_recurrence_02_gb300 import build, gdn
     monkeypatch.setattr(build, "LIB", str(tmp_path / "missing.so"))
