@@ -14,15 +14,14 @@
 //                                           P' and into the gamma of the output)
 //   S_end = gamma_last S0 + Delta^T diag(w) K
 //
-// Phase A (prefill_intra_kernel, one CTA per (chunk, value head), all chunks in
-// parallel): [K;Q] K^T on the tensor cores, A and P' from it, T by a blocked
-// (16 x 16 tiles) unit-lower-triangular inverse in fp32, then U and W on the
-// tensor cores with T rounded to the 16-bit input type (its rounding is of
-// the same size as the rounding of U and W themselves).  V is loaded into
-// Q's shared-memory slot once [K;Q]K^T has consumed Q; 71 KB of shared
-// memory and 128 TMEM columns per CTA let three CTAs share an SM.  Writes W,
-// P' and U as ready-made shared-memory operand images plus gamma / w into
-// the workspace.
+// Phase A (prefill_intra_kernel, persistent: two CTAs per SM walk the
+// (chunk, value head) units, the next unit's tiles in flight while the
+// current one is solved): [K;Q] K^T on the tensor cores, A and P' from it,
+// then [U | W] = (I + A)^{-1} [diag(beta) V | diag(beta gamma) K] by block
+// forward substitution over four 16-token blocks on warp-level MMAs (the
+// 16 x 16 diagonal blocks inverted in fp32 by substitution); U, W and P'
+// leave as ready-made operand images, staged in shared memory and
+// bulk-stored to the workspace with gamma / w.
 //
 // Phase B (prefill_carry_kernel, one CTA per (value head, 32-row dv tile,
 // row), serial over chunks; a 64-row-tile instance with a two-stage ring
@@ -90,6 +89,7 @@ struct Elem<__nv_bfloat16> {
         return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&u));
     }
     __device__ static float round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+    __device__ static __nv_bfloat16 from(float x) { return __float2bfloat16_rn(x); }
 };
 template <>
 struct Elem<__half> {
@@ -100,6 +100,7 @@ struct Elem<__half> {
     }
     __device__ static float2 unpack2(uint32_t u) { return __half22float2(*reinterpret_cast<__half2 *>(&u)); }
     __device__ static float round(float x) { return __half2float(__float2half_rn(x)); }
+    __device__ static __half from(float x) { return __float2half_rn(x); }
 };
 
 // Eight fp32 values -> eight 16-bit elements in one 16-byte vector.
@@ -147,8 +148,14 @@ __device__ __forceinline__ bool chunk_of(const PrefillParams &p, long gc, int &b
     if (p.chunk_table == nullptr) {
         const int nc = n_chunks(p.T);
         if (nc == 0) return false;
-        b = (int)(gc / nc);
-        c = (int)(gc % nc);
+        if (gc < 0x7fffffffL) {  // 32-bit division (the common case)
+            const unsigned q = (unsigned)gc / (unsigned)nc;
+            b = (int)q;
+            c = (int)((unsigned)gc - q * (unsigned)nc);
+        } else {
+            b = (int)(gc / nc);
+            c = (int)(gc % nc);
+        }
         return b < p.B;
     }
     const int32_t *tbl = p.chunk_table;
@@ -218,156 +225,156 @@ struct TcMaps {
 };
 
 // ============================================================ phase A ====
+//
+// Persistent: a grid of up to two CTAs per SM (256 threads each) walks the
+// (chunk, value head) units u = blockIdx.x, blockIdx.x + gridDim.x, ...; unit
+// u is global chunk u / Hv of value head u % Hv.  The next unit's K, Q and V
+// tiles are issued as soon as the current ones have been read (its load then
+// overlaps the solve below), its gates are loaded into registers one unit
+// ahead, and the unit after it is prefetched into L2.
+//
+// Per unit:
+//  1. [K;Q] K^T: one tcgen05 MMA group (M = 128) into TMEM.
+//  2. From TMEM: -A (16-bit, row-major) and its four 16 x 16 diagonal blocks
+//     (fp32); P' as its operand image, staged and bulk-stored to the record.
+//  3. D_J = (I + A_JJ)^{-1} for the diagonal blocks (fp32 substitution, one
+//     column per thread), stored 16-bit.
+//  4. [U | W] = (I + A)^{-1} [diag(beta) V | diag(beta gamma) K] by block
+//     forward substitution over the four 16-token blocks, on warp-level MMAs
+//     in registers: each warp owns 32 of the 256 right-hand-side columns and
+//     computes, transposed, X_J^T = (R_J^T - sum_{K<J} X_K^T A_JK^T) D_J^T.
+//     Operands are 16-bit (the inputs' type) with fp32 accumulation, as the
+//     carry phase's own MMAs use.  X_J leaves through stmatrix (transposed)
+//     in the record's U tile / W image layout, and is bulk-stored.
 
-constexpr uint32_t A_KQ = 0;          // [K;Q] image, 2 K-blocks of 128 rows (32 KB); V replaces Q
-constexpr uint32_t A_V0 = 8192;       //   V dv 0-63 (rows of the first K-block's Q half)
-constexpr uint32_t A_V1 = 24576;      //   V dv 64-127 (second K-block's Q half)
-constexpr uint32_t A_IMG = 32768;     // [T*beta ; T*beta*gamma] bf16 image (16 KB) ...
-constexpr uint32_t A_AT = A_IMG;      //   ... aliasing, before it exists, A^T fp32 [64][68]
-constexpr uint32_t A_X = A_IMG + 64 * 68 * 4;  //   and the blocked-inverse scratch, 3 x 16 x 16 fp32
-constexpr uint32_t A_T = A_X + 3 * 256 * 4;    // T fp32 [64][68]
-constexpr uint32_t A_VEC = A_T + 64 * 68 * 4;  // g, beta, gamma, 1/|k|, 1/|q|: 5 x 64 floats
-constexpr uint32_t A_BAR = A_VEC + 1536;
-constexpr uint32_t A_SMEM = A_BAR + 64 + 1024;  // + alignment slack
-constexpr uint32_t A_TMEM_COLS = 128;
-constexpr int LD = 68;                           // fp32 row stride of A^T and T
-
-// T = (I + A)^{-1} for the strictly lower 64 x 64 matrix A (A[r][c] = At[c*LD + r]),
-// blocked in 16 x 16 tiles: the four diagonal tiles D_J = (I + A_JJ)^{-1} by
-// forward substitution, then the off-diagonal tiles by increasing distance,
-// T_JI = -D_J (sum_{I <= K < J} A_JK T_KI).  In the level stages each thread
-// computes a 1 x 4 piece of a tile (row r, columns c0 .. c0 + 3), fed by one
-// float4 of T per step, with four partial sums; the diagonal solves load each
-// row of A one step ahead.  256 threads; T written to sT.
+constexpr uint32_t A_KQ = 0;        // [K;Q] image: K-block 0 (K rows 0-63 | Q rows 64-127), K-block 1 at 16384
+constexpr uint32_t A_V = 32768;     // V image: dv 0-63 | 64-127, 8 KB each
+constexpr uint32_t A_NA = 49152;    // -A, 16-bit, 64 rows of 128 B, 16-byte chunks swizzled by row % 8
+constexpr uint32_t A_AD = A_NA + 8192;            // diagonal blocks, fp32, transposed: [J][col][row], J stride 272
+constexpr uint32_t A_D = A_AD + 4 * 272 * 4;      // D_J, 16-bit row-major, 32 B rows (chunks swizzled), 512 B each
+constexpr uint32_t A_VEC = A_D + 4 * 512;         // g, beta, beta gamma (r), 1/|k|, 1/|q|: 5 x 64 floats
+constexpr uint32_t A_PS = 65536;                  // P' image on its way out (8 KB)
+constexpr uint32_t A_US = A_PS + 8192;            // U tiles on their way out (16 KB)
+constexpr uint32_t A_WS = A_US + 16384;           // W image on its way out (16 KB)
+constexpr uint32_t A_BAR = A_WS + 16384;
+constexpr uint32_t A_SMEM = A_BAR + 64 + 1024;    // + alignment slack
+constexpr uint32_t A_TMEM_COLS = 64;
 constexpr int kIntraThreads = 256;
-__device__ __forceinline__ void blocked_unit_lower_inverse(const float *At, float *sT, float *X, int tid) {
-    if (tid < 64) {
-        const int bb = tid >> 4, cl = tid & 15, o = 16 * bb;
-        float acc[16], row[16];  // row: A[o+t][o+r], loaded one step ahead
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            acc[r] = 0.f;
-            row[r] = At[o * LD + o + r];
-        }
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-            float nxt[16];
-            if (t + 1 < 16) {
-#pragma unroll
-                for (int r = 0; r < 16; ++r) nxt[r] = (r > t + 1) ? At[(o + t + 1) * LD + o + r] : 0.f;
-            }
-            const float x = (t < cl) ? 0.f : ((t == cl) ? 1.f : -acc[t]);
-            sT[(o + t) * LD + o + cl] = x;
-#pragma unroll
-            for (int r = t + 1; r < 16; ++r) acc[r] = fmaf(row[r], x, acc[r]);
-            if (t + 1 < 16) {
-#pragma unroll
-                for (int r = 0; r < 16; ++r) row[r] = nxt[r];
-            }
-        }
-    } else {
-        // zero the tiles above the diagonal
-        for (int e = tid - 64; e < 6 * 64; e += kIntraThreads - 64) {
-            const int blk = e >> 6, r = (e >> 2) & 15, c4 = (e & 3) * 4;
-            const int I = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-            const int J = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-            *reinterpret_cast<float4 *>(sT + (16 * I + r) * LD + 16 * J + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    }
-    __syncthreads();
-    // four partial sums per dot product (independent chains hide the
-    // shared-memory latency), added at the end
-    auto sum4 = [](const float4 (&a)[4]) {
-        return make_float4((a[0].x + a[1].x) + (a[2].x + a[3].x), (a[0].y + a[1].y) + (a[2].y + a[3].y),
-                           (a[0].z + a[1].z) + (a[2].z + a[3].z), (a[0].w + a[1].w) + (a[2].w + a[3].w));
-    };
-    const int q = tid & 63, r = q >> 2, c0 = (q & 3) * 4;
-#pragma unroll
-    for (int d = 1; d < 4; ++d) {
-        const int nb = 4 - d;
-        const int blk = tid >> 6, I = blk, J = blk + d;
-        if (blk < nb) {
-            float4 a[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) a[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int kk = 0; kk < d; ++kk) {
-                const int K = I + kk;
-#pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    const float x = At[(16 * K + m) * LD + 16 * J + r];
-                    const float4 t4 = *reinterpret_cast<const float4 *>(sT + (16 * K + m) * LD + 16 * I + c0);
-                    float4 &acc = a[m & 3];
-                    acc.x = fmaf(x, t4.x, acc.x); acc.y = fmaf(x, t4.y, acc.y);
-                    acc.z = fmaf(x, t4.z, acc.z); acc.w = fmaf(x, t4.w, acc.w);
-                }
-            }
-            *reinterpret_cast<float4 *>(X + blk * 256 + r * 16 + c0) = sum4(a);
-        }
-        __syncthreads();
-        if (blk < nb) {
-            float4 a[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) a[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const float dd = sT[(16 * J + r) * LD + 16 * J + m];
-                const float4 x4 = *reinterpret_cast<const float4 *>(X + blk * 256 + m * 16 + c0);
-                float4 &acc = a[m & 3];
-                acc.x = fmaf(dd, x4.x, acc.x); acc.y = fmaf(dd, x4.y, acc.y);
-                acc.z = fmaf(dd, x4.z, acc.z); acc.w = fmaf(dd, x4.w, acc.w);
-            }
-            const float4 s4 = sum4(a);
-            *reinterpret_cast<float4 *>(sT + (16 * J + r) * LD + 16 * I + c0) = make_float4(-s4.x, -s4.y, -s4.z, -s4.w);
-        }
-        __syncthreads();
-    }
-}
+constexpr int kIntraCtasPerSm = 2;
+static_assert(A_VEC + 5 * 256 <= A_PS, "phase A shared-memory layout overlaps");
+static_assert(A_SMEM * kIntraCtasPerSm + 2048 <= 232448, "two chunk-parallel CTAs must fit an SM");
+
+// Row r, 16-byte chunk q of -A (rows of 128 B).
+__device__ __forceinline__ uint32_t na_off(int r, int q) { return (uint32_t)(r * 128 + (((q ^ r) & 7) << 4)); }
+// Row r, 16-byte chunk q (0, 1) of D_J (rows of 32 B).
+__device__ __forceinline__ uint32_t d_off(int r, int q) { return (uint32_t)(r * 32 + ((q ^ (r >> 2)) & 1) * 16); }
 
 // XO: the call also writes capture or checkpoints; NORM: q and k are
 // L2-normalised in the kernel.  Separate instances, so that the plain prefill
 // carries none of that code.  The norms enter as per-token scalars:
-// A gets r_t r_i, P' rq_t r_i, the W image beta gamma r, and the record's
-// gamma (output) and w (state update) rq_t and r_t, with r = 1/|k|, rq = 1/|q|.
+// A gets r_t r_i, P' rq_t r_i, W's right-hand side beta gamma r, and the
+// record's gamma (output) and w (state update) rq_t and r_t, with r = 1/|k|,
+// rq = 1/|q|.
 template <typename E, bool XO, bool NORM>
-__global__ void __launch_bounds__(kIntraThreads, 3)
-prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap mq,
+__global__ void __launch_bounds__(kIntraThreads, kIntraCtasPerSm)
+prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_constant__ CUtensorMap mq,
                      const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sKQ = sm + A_KQ;
-    uint8_t *sImg = sm + A_IMG;
-    float *At = reinterpret_cast<float *>(sm + A_AT);
-    float *X = reinterpret_cast<float *>(sm + A_X);
-    float *sT = reinterpret_cast<float *>(sm + A_T);
+    uint8_t *sNA = sm + A_NA;
+    float *Adt = reinterpret_cast<float *>(sm + A_AD);
+    uint8_t *sD = sm + A_D;
     float *vg = reinterpret_cast<float *>(sm + A_VEC);
-    float *vbeta = vg + 64, *vgam = vg + 128, *vkn = vg + 192, *vqn = vg + 256;
-    uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + A_BAR);
-    uint64_t *bar_mma = bar_ld + 1;
-    uint64_t *bar_v = bar_ld + 2;
-    uint32_t *slot = reinterpret_cast<uint32_t *>(bar_ld + 3);
+    float *vbeta = vg + 64, *vbw = vg + 128, *vkn = vg + 192, *vqn = vg + 256;
+    uint64_t *bar_kq = reinterpret_cast<uint64_t *>(sm + A_BAR);
+    uint64_t *bar_v = bar_kq + 1;
+    uint64_t *bar_mma = bar_kq + 2;
+    uint32_t *slot = reinterpret_cast<uint32_t *>(bar_kq + 3);
 
     // the carry kernel may start its prologue once every CTA here has started
     grid_launch_dependents();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.y, Hv = p.Hv, Hk = p.Hk;
-    const int hk = h / (Hv / Hk);
-    int b, c;
-    if (!chunk_of(p, blockIdx.x, b, c)) return;
-    long rtok0;
-    int len;
-    row_range(p.cu_seqlens, b, p.T, rtok0, len);
-    const long tok0 = rtok0 + (long)c * C;
-    const int n = min(C, len - c * C);
-    uint8_t *rec = records(p) + ((size_t)(chunk_base(p, b) + c) * Hv + h) * REC_BYTES;
+    const int Hv = p.Hv, Hk = p.Hk, G = Hv / Hk;
+    const long su_slot = (long)Hv + (long)Hk * D + (long)Hv * D;
+    constexpr bool kbf = Elem<E>::kBf16;
+
+    // Units are (global chunk gc, value head h), unit index gc * Hv + h; this
+    // CTA's units advance by gridDim.x, i.e. by (gridDim.x / Hv) chunks and
+    // (gridDim.x % Hv) heads (no division inside the loop).
+    struct Unit {
+        long gc;
+        int h;
+        bool valid;
+        int b, c, n, len;
+        long tok0;
+    };
+    const int step_gc = (int)(gridDim.x / Hv), step_h = (int)(gridDim.x % Hv);
+    auto unit_at = [&](long gc, int h) {
+        Unit x;
+        x.gc = gc;
+        x.h = h;
+        x.valid = gc < max_chunks && chunk_of(p, gc, x.b, x.c);
+        if (x.valid) {
+            long rtok0;
+            row_range(p.cu_seqlens, x.b, p.T, rtok0, x.len);
+            x.tok0 = rtok0 + (long)x.c * C;
+            x.n = min(C, x.len - x.c * C);
+        }
+        return x;
+    };
+    auto next_unit = [&](const Unit &x) {
+        int h = x.h + step_h;
+        long gc = x.gc + step_gc;
+        if (h >= Hv) {
+            h -= Hv;
+            gc += 1;
+        }
+        return unit_at(gc, h);
+    };
+    auto issue_loads = [&](const Unit &x) {  // thread 0: K, Q and V tiles of unit x
+        if (!x.valid) return false;
+        const int h = x.h, hk = h / G;
+        const long tok0 = x.tok0;
+        mbar_arrive_expect_tx(bar_kq, 32768);
+        tma_load_3d(sKQ, &mk, 0, hk, (int)tok0, bar_kq);
+        tma_load_3d(sKQ + 16384, &mk, 64, hk, (int)tok0, bar_kq);
+        tma_load_3d(sKQ + 8192, &mq, 0, hk, (int)tok0, bar_kq);
+        tma_load_3d(sKQ + 24576, &mq, 64, hk, (int)tok0, bar_kq);
+        mbar_arrive_expect_tx(bar_v, 16384);
+        tma_load_3d(sm + A_V, &mv, 0, h, (int)tok0, bar_v);
+        tma_load_3d(sm + A_V + 8192, &mv, 64, h, (int)tok0, bar_v);
+        return true;
+    };
+    auto prefetch_l2 = [&](const Unit &x) {  // thread 0: the same tiles into L2
+        if (!x.valid) return;
+        const int h = x.h, hk = h / G;
+        const long tok0 = x.tok0;
+        tma_prefetch_l2_3d(&mk, 0, hk, (int)tok0);
+        tma_prefetch_l2_3d(&mk, 64, hk, (int)tok0);
+        tma_prefetch_l2_3d(&mq, 0, hk, (int)tok0);
+        tma_prefetch_l2_3d(&mq, 64, hk, (int)tok0);
+        tma_prefetch_l2_3d(&mv, 0, h, (int)tok0);
+        tma_prefetch_l2_3d(&mv, 64, h, (int)tok0);
+    };
+    // gates of unit x for token `tid` (threads < C); identity past the chunk's end
+    auto load_gates = [&](const Unit &x, float &ga, float &gb) {
+        ga = 1.f;
+        gb = 0.f;
+        if (tid < C && x.valid && tid < x.n) {
+            const long gi = (x.tok0 + tid) * Hv + x.h;
+            ga = ld_gate(p.alpha, gi, p.dt_gate);
+            gb = ld_gate(p.beta, gi, p.dt_gate);
+        }
+    };
 
     if (tid == 0) {
         prefetch_tensormap(&mq);
         prefetch_tensormap(&mk);
         prefetch_tensormap(&mv);
-        mbar_init(bar_ld, 1);
-        mbar_init(bar_mma, 1);
+        mbar_init(bar_kq, 1);
         mbar_init(bar_v, 1);
+        mbar_init(bar_mma, 1);
         fence_mbar_init();
     }
     __syncthreads();
@@ -375,243 +382,337 @@ prefill_intra_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
         tmem_alloc(slot, A_TMEM_COLS);
         tmem_relinquish();
     }
+    // thread 0's view of its copies and MMAs in flight, for the drain on timeout
+    bool kq_pending = false, v_pending = false, mma_pending = false;
+    Unit cur = unit_at(blockIdx.x / Hv, blockIdx.x % Hv);
+    Unit nxt = next_unit(cur);
     if (tid == 0) {
-        mbar_arrive_expect_tx(bar_ld, 32768);
-        tma_load_3d(sKQ, &mk, 0, hk, (int)tok0, bar_ld);
-        tma_load_3d(sKQ + 16384, &mk, 64, hk, (int)tok0, bar_ld);
-        tma_load_3d(sKQ + 8192, &mq, 0, hk, (int)tok0, bar_ld);
-        tma_load_3d(sKQ + 24576, &mq, 64, hk, (int)tok0, bar_ld);
+        kq_pending = v_pending = issue_loads(cur);
+        prefetch_l2(nxt);
     }
-    // capture: clear the whole buffer when inactive (every CTA a share), else
-    // this chunk's captured tokens' decay and (once per key head) shared key;
-    // their deltas come from the carry phase
-    const long su_slot = (long)Hv + (long)Hk * D + (long)Hv * D;
-    int ncap = 0;
-    float *su0 = nullptr;
     if constexpr (XO) {
-        prefill_capture_clear(p, su_slot, (long)blockIdx.y * gridDim.x + blockIdx.x,
-                              (long)gridDim.x * gridDim.y, tid, kIntraThreads);
-        ncap = prefill_ncap(p, b, len) - c * C;
-        if (ncap > 0) su0 = p.su + ((long)b * p.capacity + (long)c * C) * su_slot;
+        // inactive capture: every CTA clears a share of the whole buffer
+        prefill_capture_clear(p, su_slot, blockIdx.x, gridDim.x, tid, kIntraThreads);
     }
-    if (tid < C) {
-        const long gi = (tok0 + tid) * Hv + h;
-        const float a = (tid < n) ? ld_gate(p.alpha, gi, p.dt_gate) : 0.f;
-        vg[tid] = (tid < n) ? conv_log_alpha(a, p.conv) : 0.f;
-        vbeta[tid] = (tid < n) ? conv_beta(ld_gate(p.beta, gi, p.dt_gate), p.conv) : 0.f;
-        if (tid < ncap) su0[tid * su_slot + h] = conv_alpha(a, p.conv);
-    }
+    float ga, gb;
+    load_gates(cur, ga, gb);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tbase = *slot;
     const uint32_t lane_base = tbase + ((uint32_t)(32 * (warp & 3)) << 16);
-    const bool kbf = Elem<E>::kBf16;
-    bool ok = true;
-    if (tid == 0) {
-        // [K; Q] K^T -> TMEM cols [0, 64): rows 0-63 K K^T, rows 64-127 Q K^T
-        ok = mbar_wait(bar_ld, 0, p.wait_ns);
-        if (ok) {
-            fence_after_sync();
-            const uint64_t d0 = desc_sw128(smem_u32(sKQ), 16, 1024);
-            const uint32_t id = idesc_f16(128, 64, false, false, kbf);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const uint64_t d = desc_add(d0, (k >> 2) * 16384 + (k & 3) * 32);
-                mma_f16(tbase, d, d, id, k > 0);
-            }
-            mma_commit(bar_mma);
+    const int quarter = warp & 3, half = warp >> 2;
+    // this warp's 32 right-hand-side columns: V columns (U) for warps 0-3, K columns (W) for 4-7
+    const bool isW = warp >= 4;
+    const int cc0 = 32 * (warp & 3);                    // first column within V or K
+    const int t4 = lane & 3;                            // fragment column-pair index
+    bool failed = false;
+
+    int it = 0;
+    // (packed rows: every unit after an invalid one is past the end too)
+    for (; cur.valid; cur = nxt, nxt = next_unit(nxt), ++it) {
+        const int b = cur.b, c = cur.c, h = cur.h, n = cur.n, len = cur.len;
+        const long tok0 = cur.tok0;
+        const int hk = h / G;
+        const uint32_t ph = (uint32_t)it & 1u;
+        uint8_t *rec = records(p) + ((size_t)cur.gc * Hv + h) * REC_BYTES;
+        int ncap = 0;
+        float *su0 = nullptr;
+        if constexpr (XO) {
+            ncap = prefill_ncap(p, b, len) - c * C;
+            if (ncap > 0) su0 = p.su + ((long)b * p.capacity + (long)c * C) * su_slot;
         }
-    }
-    // warp 1: cumulative log-decay g, gamma, w while the MMA runs
-    float g0 = 0.f, g1 = 0.f, w0 = 0.f, w1 = 0.f, glast = 0.f;
-    if (warp == 1) {
-        float x0 = vg[lane], x1 = vg[lane + 32];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            float y0 = __shfl_up_sync(0xffffffffu, x0, o);
-            float y1 = __shfl_up_sync(0xffffffffu, x1, o);
-            if (lane >= o) { x0 += y0; x1 += y1; }
+        // ---- gates (loaded one unit ahead); start the next unit's gate loads
+        if (tid < C) {
+            vg[tid] = (tid < n) ? conv_log_alpha(ga, p.conv) : 0.f;
+            vbeta[tid] = (tid < n) ? conv_beta(gb, p.conv) : 0.f;
+            if (tid < ncap) su0[tid * su_slot + h] = conv_alpha(ga, p.conv);
         }
-        x1 += __shfl_sync(0xffffffffu, x0, 31);
-        glast = __shfl_sync(0xffffffffu, x1, 31);
-        g0 = expf(x0); g1 = expf(x1); w0 = expf(glast - x0); w1 = expf(glast - x1);
-        vg[lane] = x0;
-        vg[lane + 32] = x1;
-        vgam[lane] = g0; vgam[lane + 32] = g1;
-    }
-    // record: gamma for the output gamma (scale q) S^T, w for the state update
-    float *rv = reinterpret_cast<float *>(rec + REC_VEC);
-    if constexpr (NORM) {
-        // 1/|k_t| and 1/|q_t| from the staged tiles (rows 0-63 K, 64-127 Q;
-        // two threads per row, one per 64-column block), before V replaces Q
-        if (!mbar_wait(bar_ld, 0, p.wait_ns)) ok = false;
-        const int r = tid >> 1, kb = tid & 1;
-        float ss = 0.f;
+        load_gates(nxt, ga, gb);
+        if (tid == 0) prefetch_l2(next_unit(nxt));
+        bool ok = true;
+        if (tid == 0) {
+            // [K; Q] K^T -> TMEM cols [0, 64): rows 0-63 K K^T, rows 64-127 Q K^T
+            ok = mbar_wait(bar_kq, ph, p.wait_ns);
+            if (ok) {
+                fence_after_sync();
+                const uint64_t d0 = desc_sw128(smem_u32(sKQ), 16, 1024);
+                const uint32_t id = idesc_f16(128, 64, false, false, kbf);
 #pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8) {
-            float x[8];
-            unpack8<E>(*reinterpret_cast<const uint4 *>(sKQ + kb * 16384 + sw128_chunk(r, q8)), x);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
-        }
-        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-        if (kb == 0) (r < C ? vkn[r] : vqn[r - C]) = l2norm_factor(ss);
-        __syncthreads();
-        if (warp == 1) {
-            rv[lane] = p.scale * g0 * vqn[lane]; rv[lane + 32] = p.scale * g1 * vqn[lane + 32];
-            rv[64 + lane] = w0 * vkn[lane]; rv[96 + lane] = w1 * vkn[lane + 32];
-            if (lane == 0) rv[128] = expf(glast);
-        }
-    } else {
-        if (warp == 1) {
-            rv[lane] = p.scale * g0; rv[lane + 32] = p.scale * g1; rv[64 + lane] = w0; rv[96 + lane] = w1;
-            if (lane == 0) rv[128] = expf(glast);
-        }
-    }
-    __syncthreads();
-    if (ncap > 0 && h % (Hv / Hk) == 0) {
-        // captured keys: the (normalised) key the recurrence used
-        const E *kg = reinterpret_cast<const E *>(p.k);
-        const int nk = ncap < n ? ncap : n;
-        for (int e = tid; e < nk * D; e += kIntraThreads) {
-            const int t = e / D, j = e % D;
-            su0[t * su_slot + Hv + (long)hk * D + j] =
-                ld_f(kg + ((tok0 + t) * Hk + hk) * D + j) * (NORM ? vkn[t] : 1.f);
-        }
-    }
-    ok = ok && mbar_wait(bar_mma, 0, p.wait_ns);
-    fence_after_sync();
-    const bool v_issued = ok;  // the same for every thread (ok is uniform after the wait)
-    if (ok && tid == 0) {
-        // Q has been consumed: V takes its place (the load overlaps A, P' and T)
-        mbar_arrive_expect_tx(bar_v, 16384);
-        tma_load_3d(sm + A_V0, &mv, 0, h, (int)tok0, bar_v);
-        tma_load_3d(sm + A_V1, &mv, 64, h, (int)tok0, bar_v);
-    }
-    if (ok) {
-        // warp w reads TMEM lane quarter (w % 4); warps w and w + 4 split the 64 columns
-        const int quarter = warp & 3, half = warp >> 2;
-        if (quarter < 2) {
-            // A, stored transposed: At[i][t] = A[t][i] = beta_t e^{g_t - g_i} k_t.k_i  (i < t)
-            const int t = 32 * quarter + lane;
-            const float gt = vg[t], bt = vbeta[t] * (NORM ? vkn[t] : 1.f);
-            float v[32];
-            tmem_ld32(lane_base + 32 * half, v);
-#pragma unroll
-            for (int ii = 0; ii < 32; ++ii) {
-                const int i = 32 * half + ii;
-                At[i * LD + t] = (i < t) ? bt * __expf(gt - vg[i]) * (NORM ? v[ii] * vkn[i] : v[ii]) : 0.f;
-            }
-        } else {
-            // P'[t][i] = e^{g_t - g_i} (scale q_t).k_i (i <= t), image straight to the workspace
-            const int t = 32 * (quarter - 2) + lane;
-            const float gt = vg[t], sc = p.scale * (NORM ? vqn[t] : 1.f);
-            uint8_t *dst = rec + REC_P;
-            float v[32];
-            tmem_ld32(lane_base + 32 * half, v);
-#pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8) {
-                float pv[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int i = 32 * half + 8 * q8 + e;
-                    pv[e] = (i <= t) ? __expf(gt - vg[i]) * (sc * (NORM ? v[8 * q8 + e] * vkn[i] : v[8 * q8 + e]))
-                                     : 0.f;
+                for (int k = 0; k < 8; ++k) {
+                    const uint64_t d = desc_add(d0, (k >> 2) * 16384 + (k & 3) * 32);
+                    mma_f16(tbase, d, d, id, k > 0);
                 }
-                *reinterpret_cast<uint4 *>(dst + sw128_chunk(t, 4 * half + q8)) = pack8<E>(pv);
+                mma_commit(bar_mma);
+                mma_pending = true;
             }
         }
-    }
-    __syncthreads();
-
-    // ---- T = (I + A)^{-1}
-    if (ok) blocked_unit_lower_inverse(At, sT, X, tid);
-    else {
-        __syncthreads(); __syncthreads(); __syncthreads(); __syncthreads(); __syncthreads(); __syncthreads();
+        if constexpr (NORM) {
+            // 1/|k_t| and 1/|q_t| from the staged tiles (rows 0-63 K, 64-127 Q;
+            // two threads per row, one per 64-column block)
+            if (!mbar_wait(bar_kq, ph, p.wait_ns)) ok = false;
+            const int r = tid >> 1, kb = tid & 1;
+            float ss = 0.f;
+#pragma unroll
+            for (int q8 = 0; q8 < 8; ++q8) {
+                float x[8];
+                unpack8<E>(*reinterpret_cast<const uint4 *>(sKQ + kb * 16384 + sw128_chunk(r, q8)), x);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+            }
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            if (kb == 0) (r < C ? vkn[r] : vqn[r - C]) = l2norm_factor(ss);
+        }
+        if (__syncthreads_or(!ok)) { failed = true; break; }
+        if (tid == 0) kq_pending = false;
+        // warp 1: cumulative log-decay g, gamma, w; W's right-hand-side scale; the record's vectors
+        if (warp == 1) {
+            float x0 = vg[lane], x1 = vg[lane + 32];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                float y0 = __shfl_up_sync(0xffffffffu, x0, o);
+                float y1 = __shfl_up_sync(0xffffffffu, x1, o);
+                if (lane >= o) { x0 += y0; x1 += y1; }
+            }
+            x1 += __shfl_sync(0xffffffffu, x0, 31);
+            const float glast = __shfl_sync(0xffffffffu, x1, 31);
+            const float g0 = expf(x0), g1 = expf(x1), w0 = expf(glast - x0), w1 = expf(glast - x1);
+            vg[lane] = x0;
+            vg[lane + 32] = x1;
+            const float rk0 = NORM ? vkn[lane] : 1.f, rk1 = NORM ? vkn[lane + 32] : 1.f;
+            const float rq0 = NORM ? vqn[lane] : 1.f, rq1 = NORM ? vqn[lane + 32] : 1.f;
+            vbw[lane] = vbeta[lane] * g0 * rk0;
+            vbw[lane + 32] = vbeta[lane + 32] * g1 * rk1;
+            float *rv = reinterpret_cast<float *>(rec + REC_VEC);
+            rv[lane] = p.scale * g0 * rq0;
+            rv[lane + 32] = p.scale * g1 * rq1;
+            rv[64 + lane] = w0 * rk0;
+            rv[96 + lane] = w1 * rk1;
+            if (lane == 0) rv[128] = expf(glast);
+        }
+        if (ncap > 0 && h % G == 0) {
+            // captured keys: the (normalised) key the recurrence used
+            const E *kg = reinterpret_cast<const E *>(p.k);
+            const int nk = ncap < n ? ncap : n;
+            for (int e = tid; e < nk * D; e += kIntraThreads) {
+                const int t = e / D, j = e % D;
+                su0[t * su_slot + Hv + (long)hk * D + j] =
+                    ld_f(kg + ((tok0 + t) * Hk + hk) * D + j) * (NORM ? vkn[t] : 1.f);
+            }
+        }
+        ok = mbar_wait(bar_mma, ph, p.wait_ns);
+        if (tid == 0) bulk_wait_read_all();  // the last unit's staged images have been read
+        if (__syncthreads_or(!ok)) { failed = true; break; }
+        fence_after_sync();
+        if (tid == 0) mma_pending = false;
+        // ---- -A (16-bit) and its diagonal blocks (fp32), P' (image, staged) from TMEM.
+        // Warp w reads TMEM lane quarter w % 4 (rows 0-63: K K^T, 64-127: Q K^T);
+        // warps w and w + 4 split the columns a quarter's rows need: rows 0-31
+        // of A / P' have nothing right of column 31 (16 columns each), rows
+        // 32-63 use all 64 (32 each).
+        {
+            const bool aside = quarter < 2;  // A (K rows) or P' (Q rows)
+            const int t = 32 * (quarter & 1) + lane;
+            const int c_lo = (quarter & 1) ? 32 * half : 16 * half;
+            const float gt = vg[t];
+            if (aside) {
+                // A[t][i] = beta_t e^{g_t - g_i} k_t.k_i  (i < t), stored negated;
+                // the diagonal block (J, J), J = t / 16, also in fp32 for D_J
+                const float bt = vbeta[t] * (NORM ? vkn[t] : 1.f);
+                const int J = t >> 4;
+                auto emit = [&](const float *v, int nc) {
+                    for (int q8 = 0; q8 < nc / 8; ++q8) {
+                        float a[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int i = c_lo + 8 * q8 + e;
+                            const float kk = NORM ? v[8 * q8 + e] * vkn[i] : v[8 * q8 + e];
+                            a[e] = (i < t) ? bt * __expf(gt - vg[i]) * kk : 0.f;
+                        }
+                        if (((c_lo + 8 * q8) >> 4) == J) {
+                            float *dst = Adt + J * 272 + ((c_lo + 8 * q8) & 15) * 16 + (t & 15);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) dst[e * 16] = a[e];
+                        }
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) a[e] = -a[e];
+                        *reinterpret_cast<uint4 *>(sNA + na_off(t, (c_lo >> 3) + q8)) = pack8<E>(a);
+                    }
+                };
+                if (quarter == 0) {
+                    float v[16];
+                    tmem_ld16(lane_base + c_lo, v);
+                    emit(v, 16);
+                } else {
+                    float v[32];
+                    tmem_ld32(lane_base + c_lo, v);
+                    emit(v, 32);
+                }
+            } else {
+                // P'[t][i] = e^{g_t - g_i} (scale q_t).k_i (i <= t), image staged for a bulk store
+                const float sc = p.scale * (NORM ? vqn[t] : 1.f);
+                uint8_t *dst = sm + A_PS;
+                auto emit = [&](const float *v, int nc) {
+                    for (int q8 = 0; q8 < nc / 8; ++q8) {
+                        float pv[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int i = c_lo + 8 * q8 + e;
+                            const float qk = NORM ? v[8 * q8 + e] * vkn[i] : v[8 * q8 + e];
+                            pv[e] = (i <= t) ? __expf(gt - vg[i]) * (sc * qk) : 0.f;
+                        }
+                        *reinterpret_cast<uint4 *>(dst + sw128_chunk(t, (c_lo >> 3) + q8)) = pack8<E>(pv);
+                    }
+                };
+                if (quarter == 2) {
+                    float v[16];
+                    tmem_ld16(lane_base + c_lo, v);
+                    emit(v, 16);
+                    // columns 32-63 of rows 0-31 are zero: 2 chunks per thread
+#pragma unroll
+                    for (int q8 = 0; q8 < 2; ++q8)
+                        *reinterpret_cast<uint4 *>(dst + sw128_chunk(t, 4 + 2 * half + q8)) = make_uint4(0u, 0u, 0u, 0u);
+                } else {
+                    float v[32];
+                    tmem_ld32(lane_base + c_lo, v);
+                    emit(v, 32);
+                }
+            }
+        }
+        fence_proxy_async();
+        fence_before_sync();
         __syncthreads();
-    }
-
-    // ---- operand image [T diag(beta) ; T diag(beta gamma)] in the 16-bit input type
-    if (ok) {
-        const int t = tid & 63, which = (tid >> 6) & 1, part = tid >> 7, r = which * 64 + t;
+        if (tid == 0) {
+            bulk_store(rec + REC_P, sm + A_PS, 8192);
+            bulk_commit();
+        }
+        // ---- D_J = (I + A_JJ)^{-1} by forward substitution: four threads per
+        // column cl of block J (consecutive lanes), thread p holding rows 4p .. 4p+3
+        {
+            const int J = tid >> 6, cl = (tid >> 2) & 15, pr = tid & 3;
+            const float *Aj = Adt + J * 272;  // Aj[l * 16 + r] = A_JJ[r][l]
+            E *Dj = reinterpret_cast<E *>(sD + J * 512);
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            float4 col = *reinterpret_cast<const float4 *>(Aj + 4 * pr);  // column 0, rows 4p ..
 #pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-            const int q8 = 4 * part + qq;
-            float val[8];
+            for (int l = 0; l < 16; ++l) {
+                const int owner = l >> 2;
+                float4 nxt = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (l + 1 < 16) nxt = *reinterpret_cast<const float4 *>(Aj + (l + 1) * 16 + 4 * pr);
+                float mine = 0.f;
+                if (pr == owner) mine = (l < cl) ? 0.f : ((l == cl) ? 1.f : -acc[l & 3]);
+                const float x = __shfl_sync(0xffffffffu, mine, (lane & ~3) | owner);  // D_J[l][cl]
+                if (pr == owner) Dj[(d_off(l, cl >> 3) >> 1) + (cl & 7)] = Elem<E>::from(x);
+                const float cv[4] = {col.x, col.y, col.z, col.w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int s = 8 * q8 + e;
-                val[e] = sT[t * LD + s] * (which ? vbeta[s] * vgam[s] * (NORM ? vkn[s] : 1.f) : vbeta[s]);
+                for (int j = 0; j < 4; ++j)
+                    if (4 * pr + j > l) acc[j] = fmaf(cv[j], x, acc[j]);
+                col = nxt;
             }
-            *reinterpret_cast<uint4 *>(sImg + sw128_chunk(r, q8)) = pack8<E>(val);
         }
-    }
-    fence_proxy_async();
-    fence_before_sync();
-    __syncthreads();
-
-    // ---- U = [T b ; T b g] V (rows 0-63 used) -> TMEM cols [0, 128)
-    if (ok && tid == 0) {
-        fence_after_sync();
-        ok = mbar_wait(bar_v, 0, p.wait_ns);
+        // every warp: its right-hand-side columns, transposed, for all four token blocks
+        // (fragment of R^T, rows = its columns, cols = tokens; scaled when used)
+        ok = mbar_wait(bar_v, ph, p.wait_ns);
+        uint32_t rf[4][2][4];
         if (ok) {
-            const uint64_t a0 = desc_sw128(smem_u32(sImg), 16, 1024), b0 = desc_sw128(smem_u32(sm + A_V0), 16384, 1024);
-            const uint32_t id = idesc_f16(128, 128, false, true, kbf);
+            const uint8_t *srcb = isW ? sKQ + 16384 * (cc0 >> 6) : sm + A_V + 8192 * (cc0 >> 6);
+            const int mi_l = (lane >> 3) & 1, ti_l = lane >> 4, r8 = lane & 7;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) mma_f16(tbase, desc_add(a0, k * 32), desc_add(b0, k * 2048), id, k > 0);
-            mma_commit(bar_mma);
+            for (int J = 0; J < 4; ++J)
+#pragma unroll
+                for (int mi = 0; mi < 2; ++mi) {
+                    const int t = 16 * J + 8 * ti_l + r8;
+                    const int q = ((cc0 & 63) + 16 * mi + 8 * mi_l) >> 3;
+                    ldsm_x4_trans(rf[J][mi], srcb + sw128_chunk(t, q));
+                }
+        }
+        if (__syncthreads_or(!ok)) { failed = true; break; }
+        if (tid == 0) {
+            // K, Q and V have been read: the next unit's copies may land
+            kq_pending = v_pending = issue_loads(nxt);
+        }
+        // ---- block substitution: X_J^T = (R_J^T - sum_{K<J} X_K^T A_JK^T) D_J^T
+        {
+            const float *scl = isW ? vbw : vbeta;
+            uint32_t xa[4][2][4];  // X_K^T as A fragments, per block K and m-tile
+#pragma unroll
+            for (int J = 0; J < 4; ++J) {
+                float acc[2][2][4];
+#pragma unroll
+                for (int ni = 0; ni < 2; ++ni) {
+                    const float2 s0 = *reinterpret_cast<const float2 *>(scl + 16 * J + 8 * ni + 2 * t4);
+#pragma unroll
+                    for (int mi = 0; mi < 2; ++mi) {
+                        const float2 lo = Elem<E>::unpack2(rf[J][mi][2 * ni]);      // row g
+                        const float2 hi = Elem<E>::unpack2(rf[J][mi][2 * ni + 1]);  // row g + 8
+                        acc[mi][ni][0] = lo.x * s0.x;
+                        acc[mi][ni][1] = lo.y * s0.y;
+                        acc[mi][ni][2] = hi.x * s0.x;
+                        acc[mi][ni][3] = hi.y * s0.y;
+                    }
+                }
+#pragma unroll
+                for (int K = 0; K < J; ++K) {
+                    uint32_t bq[4];  // (-A_JK)^T as B fragments: n-tile 0 (b0, b1), n-tile 1 (b0, b1)
+                    const int row = 16 * J + (lane & 7) + 8 * (lane >> 4);
+                    ldsm_x4(bq, sNA + na_off(row, 2 * K + ((lane >> 3) & 1)));
+#pragma unroll
+                    for (int mi = 0; mi < 2; ++mi) {
+                        mma16816<kbf>(acc[mi][0], xa[K][mi], bq[0], bq[1]);
+                        mma16816<kbf>(acc[mi][1], xa[K][mi], bq[2], bq[3]);
+                    }
+                }
+                uint32_t ya[2][4];
+#pragma unroll
+                for (int mi = 0; mi < 2; ++mi) {
+                    ya[mi][0] = Elem<E>::pack2(acc[mi][0][0], acc[mi][0][1]);
+                    ya[mi][1] = Elem<E>::pack2(acc[mi][0][2], acc[mi][0][3]);
+                    ya[mi][2] = Elem<E>::pack2(acc[mi][1][0], acc[mi][1][1]);
+                    ya[mi][3] = Elem<E>::pack2(acc[mi][1][2], acc[mi][1][3]);
+                }
+                uint32_t bd[4];  // D_J^T as B fragments
+                {
+                    const int row = (lane & 7) + 8 * (lane >> 4);
+                    ldsm_x4(bd, sD + J * 512 + d_off(row, (lane >> 3) & 1));
+                }
+#pragma unroll
+                for (int mi = 0; mi < 2; ++mi) {
+                    float o0[4] = {0.f, 0.f, 0.f, 0.f}, o1[4] = {0.f, 0.f, 0.f, 0.f};
+                    mma16816<kbf>(o0, ya[mi], bd[0], bd[1]);
+                    mma16816<kbf>(o1, ya[mi], bd[2], bd[3]);
+                    xa[J][mi][0] = Elem<E>::pack2(o0[0], o0[1]);
+                    xa[J][mi][1] = Elem<E>::pack2(o0[2], o0[3]);
+                    xa[J][mi][2] = Elem<E>::pack2(o1[0], o1[1]);
+                    xa[J][mi][3] = Elem<E>::pack2(o1[2], o1[3]);
+                    // X_J rows (tokens) 16J .. 16J+15, this m-tile's 16 columns, to the staged record
+                    const int t = 16 * J + 8 * (lane >> 4) + (lane & 7);
+                    const int ccol = cc0 + 16 * mi + 8 * ((lane >> 3) & 1);
+                    uint8_t *dst = isW ? sm + A_WS + (ccol >> 6) * 8192 + sw128_chunk(t, (ccol & 63) >> 3)
+                                       : sm + A_US + (ccol >> 5) * 4096 + u32_chunk(t, (ccol & 31) >> 3);
+                    stsm_x4_trans(dst, xa[J][mi]);
+                }
+            }
+        }
+        fence_proxy_async();
+        __syncthreads();
+        if (tid == 0) {
+            bulk_store(rec + REC_U, sm + A_US, 16384);
+            bulk_store(rec + REC_W, sm + A_WS, 16384);
+            bulk_commit();
         }
     }
-    ok = ok && mbar_wait(bar_mma, 1, p.wait_ns);
-    fence_after_sync();
-    if (ok && (warp & 3) < 2) {
-        // U as four thread-read tiles of 32 dv columns: [64 t][32 i], 16-byte chunks swizzled by t
-        const int t = 32 * (warp & 3) + lane, half = warp >> 2;
-#pragma unroll
-        for (int qq = 0; qq < 2; ++qq) {
-            const int q4 = 2 * half + qq;
-            float v[32];
-            tmem_ld32(lane_base + 32 * q4, v);
-            uint8_t *dst = rec + REC_U + q4 * 4096;
-#pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8)
-                *reinterpret_cast<uint4 *>(dst + u32_chunk(t, q8)) = pack8<E>(v + 8 * q8);
+    if (failed) {
+        if (tid == 0) {
+            atomicOr(p.err, (uint32_t)GDN_DEVERR_TIMEOUT);
+            // copies and MMAs in flight must finish before the CTA exits
+            const uint32_t ph = (uint32_t)it & 1u;
+            if (kq_pending) mbar_wait(bar_kq, ph, kWaitNs);
+            if (v_pending) mbar_wait(bar_v, ph, kWaitNs);
+            if (mma_pending) mbar_wait(bar_mma, ph, kWaitNs);
         }
     }
-    fence_before_sync();
-    __syncthreads();
-
-    // ---- W = [T b ; T b g] K (rows 64-127 used) -> TMEM cols [0, 128)
-    if (ok && tid == 0) {
-        fence_after_sync();
-        const uint64_t a0 = desc_sw128(smem_u32(sImg), 16, 1024), b0 = desc_sw128(smem_u32(sKQ), 16384, 1024);
-        const uint32_t id = idesc_f16(128, 128, false, true, kbf);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) mma_f16(tbase, desc_add(a0, k * 32), desc_add(b0, k * 2048), id, k > 0);
-        mma_commit(bar_mma);
-    }
-    ok = ok && mbar_wait(bar_mma, 0, p.wait_ns);
-    fence_after_sync();
-    if (ok && (warp & 3) >= 2) {
-        const int t = 32 * ((warp & 3) - 2) + lane, half = warp >> 2;
-#pragma unroll
-        for (int qq = 0; qq < 2; ++qq) {
-            const int q4 = 2 * half + qq;
-            float v[32];
-            tmem_ld32(lane_base + 32 * q4, v);
-            uint8_t *dst = rec + REC_W + (q4 >> 1) * 8192;
-#pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8)
-                *reinterpret_cast<uint4 *>(dst + sw128_chunk(t, (q4 & 1) * 4 + q8)) = pack8<E>(v + 8 * q8);
-        }
-    }
-    if (!ok) {
-        if (tid == 0) atomicOr(p.err, (uint32_t)GDN_DEVERR_TIMEOUT);
-        // copies in flight must land before the CTA exits
-        mbar_wait(bar_ld, 0, kWaitNs);
-        if (v_issued) mbar_wait(bar_v, 0, kWaitNs);
-    }
+    // (without a timeout nothing is in flight here: issue_loads issues nothing past the last unit)
+    if (tid == 0) bulk_wait_all();  // the records have been written
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, A_TMEM_COLS);
@@ -1004,8 +1105,11 @@ cudaError_t launch_e(const PrefillParams &p, long total_T, long max_chunks, cuda
              : set_smem_once<prefill_carry_kernel<E, XO, 32>>((int)CarryCfg<32>::B_SMEM);
     if (e != cudaSuccess) return e;
     if (max_chunks > 0) {
-        dim3 ga((unsigned)max_chunks, p.Hv);
-        intra<<<ga, kIntraThreads, A_SMEM, stream>>>(p, mq, mk, mv);
+        // persistent: at most two CTAs per SM walk the (chunk, value head) units
+        const long n_units = max_chunks * p.Hv;
+        const long cap = (long)kIntraCtasPerSm * sm_count_of_current_device();
+        const unsigned grid = (unsigned)(n_units < cap ? n_units : cap);
+        intra<<<grid, kIntraThreads, A_SMEM, stream>>>(p, max_chunks, mq, mk, mv);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
