@@ -195,6 +195,20 @@ __device__ __forceinline__ void st_out(float *p, float x) { *p = x; }
 __device__ __forceinline__ void st_out(__half *p, float x) { *p = __float2half_rn(x); }
 __device__ __forceinline__ void st_out(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
 
+// The same, as a volatile read-only load: it is issued where it is written,
+// so that a load meant to run ahead of its use is not moved next to it.
+__device__ __forceinline__ float ld_gate_early(const void *p, long idx, int dt) {
+    if (dt == GDN_F32) {
+        float x;
+        asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(x) : "l"(reinterpret_cast<const float *>(p) + idx));
+        return x;
+    }
+    unsigned short u;
+    asm volatile("ld.global.nc.b16 %0, [%1];" : "=h"(u) : "l"(reinterpret_cast<const unsigned short *>(p) + idx));
+    if (dt == GDN_F16) return __half2float(__ushort_as_half(u));
+    return __bfloat162float(__ushort_as_bfloat16(u));
+}
+
 // Gate value (alpha / beta) of runtime dtype `dt` at element `idx`.
 __device__ __forceinline__ float ld_gate(const void *p, long idx, int dt) {
     if (dt == GDN_F32) return reinterpret_cast<const float *>(p)[idx];

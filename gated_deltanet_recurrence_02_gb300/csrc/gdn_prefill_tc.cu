@@ -258,7 +258,7 @@ constexpr uint32_t A_US = A_PS + 8192;            // U tiles on their way out (1
 constexpr uint32_t A_WS = A_US + 16384;           // W image on its way out (16 KB)
 constexpr uint32_t A_BAR = A_WS + 16384;
 constexpr uint32_t A_SMEM = A_BAR + 64 + 1024;    // + alignment slack
-constexpr uint32_t A_TMEM_COLS = 64;
+constexpr uint32_t A_TMEM_COLS = 128;  // [K;Q] K^T of this unit and of the next, by unit parity
 constexpr int kIntraThreads = 256;
 constexpr int kIntraCtasPerSm = 2;
 static_assert(A_VEC + 5 * 256 <= A_PS, "phase A shared-memory layout overlaps");
@@ -346,6 +346,21 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
         tma_load_3d(sm + A_V + 8192, &mv, 64, h, (int)tok0, bar_v);
         return true;
     };
+    // thread 0: [K; Q] K^T of the unit with loop index `ui` into TMEM buffer ui % 2
+    // (rows 0-63 K K^T, rows 64-127 Q K^T), once its tiles have landed
+    auto issue_kq_mma = [&](int ui, uint32_t tb) -> bool {
+        if (!mbar_wait(bar_kq, (uint32_t)ui & 1u, p.wait_ns)) return false;
+        fence_after_sync();
+        const uint64_t d0 = desc_sw128(smem_u32(sKQ), 16, 1024);
+        const uint32_t id = idesc_f16(128, 64, false, false, kbf);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint64_t d = desc_add(d0, (k >> 2) * 16384 + (k & 3) * 32);
+            mma_f16(tb + (ui & 1) * 64, d, d, id, k > 0);
+        }
+        mma_commit(bar_mma);
+        return true;
+    };
     auto prefetch_l2 = [&](const Unit &x) {  // thread 0: the same tiles into L2
         if (!x.valid) return;
         const int h = x.h, hk = h / G;
@@ -357,14 +372,15 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
         tma_prefetch_l2_3d(&mv, 0, h, (int)tok0);
         tma_prefetch_l2_3d(&mv, 64, h, (int)tok0);
     };
-    // gates of unit x for token `tid` (threads < C); identity past the chunk's end
+    // gates of unit x for token `tid` (threads < C); identity past the chunk's end.
+    // Issued as volatile loads so that they stay a unit ahead of their use.
     auto load_gates = [&](const Unit &x, float &ga, float &gb) {
         ga = 1.f;
         gb = 0.f;
         if (tid < C && x.valid && tid < x.n) {
             const long gi = (x.tok0 + tid) * Hv + x.h;
-            ga = ld_gate(p.alpha, gi, p.dt_gate);
-            gb = ld_gate(p.beta, gi, p.dt_gate);
+            ga = ld_gate_early(p.alpha, gi, p.dt_gate);
+            gb = ld_gate_early(p.beta, gi, p.dt_gate);
         }
     };
 
@@ -383,7 +399,7 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
         tmem_relinquish();
     }
     // thread 0's view of its copies and MMAs in flight, for the drain on timeout
-    bool kq_pending = false, v_pending = false, mma_pending = false;
+    bool kq_pending = false, v_pending = false, mma_pending = false, kq_pending_fail = false;
     Unit cur = unit_at(blockIdx.x / Hv, blockIdx.x % Hv);
     Unit nxt = next_unit(cur);
     if (tid == 0) {
@@ -402,6 +418,12 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
     const uint32_t tbase = *slot;
     const uint32_t lane_base = tbase + ((uint32_t)(32 * (warp & 3)) << 16);
     const int quarter = warp & 3, half = warp >> 2;
+    // the first unit's [K; Q] K^T (later units': issued by the unit before)
+    if (tid == 0 && cur.valid) {
+        const bool ok0 = issue_kq_mma(0, tbase);
+        kq_pending = !ok0;
+        mma_pending = ok0;
+    }
     // this warp's 32 right-hand-side columns: V columns (U) for warps 0-3, K columns (W) for 4-7
     const bool isW = warp >= 4;
     const int cc0 = 32 * (warp & 3);                    // first column within V or K
@@ -430,23 +452,7 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
         }
         load_gates(nxt, ga, gb);
         if (tid == 0) prefetch_l2(next_unit(nxt));
-        bool ok = true;
-        if (tid == 0) {
-            // [K; Q] K^T -> TMEM cols [0, 64): rows 0-63 K K^T, rows 64-127 Q K^T
-            ok = mbar_wait(bar_kq, ph, p.wait_ns);
-            if (ok) {
-                fence_after_sync();
-                const uint64_t d0 = desc_sw128(smem_u32(sKQ), 16, 1024);
-                const uint32_t id = idesc_f16(128, 64, false, false, kbf);
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint64_t d = desc_add(d0, (k >> 2) * 16384 + (k & 3) * 32);
-                    mma_f16(tbase, d, d, id, k > 0);
-                }
-                mma_commit(bar_mma);
-                mma_pending = true;
-            }
-        }
+        bool ok = !(tid == 0 && (kq_pending_fail || (it == 0 && kq_pending)));  // this unit's [K; Q] K^T issued
         if constexpr (NORM) {
             // 1/|k_t| and 1/|q_t| from the staged tiles (rows 0-63 K, 64-127 Q;
             // two threads per row, one per 64-column block)
@@ -464,7 +470,6 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
             if (kb == 0) (r < C ? vkn[r] : vqn[r - C]) = l2norm_factor(ss);
         }
         if (__syncthreads_or(!ok)) { failed = true; break; }
-        if (tid == 0) kq_pending = false;
         // warp 1: cumulative log-decay g, gamma, w; W's right-hand-side scale; the record's vectors
         if (warp == 1) {
             float x0 = vg[lane], x1 = vg[lane + 32];
@@ -500,11 +505,12 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
                     ld_f(kg + ((tok0 + t) * Hk + hk) * D + j) * (NORM ? vkn[t] : 1.f);
             }
         }
-        ok = mbar_wait(bar_mma, ph, p.wait_ns);
+        ok = mbar_wait(bar_mma, ph, p.wait_ns);  // this unit's [K; Q] K^T
         if (tid == 0) bulk_wait_read_all();  // the last unit's staged images have been read
         if (__syncthreads_or(!ok)) { failed = true; break; }
         fence_after_sync();
         if (tid == 0) mma_pending = false;
+        const uint32_t lane_buf = lane_base + (uint32_t)(it & 1) * 64;  // this unit's [K; Q] K^T
         // ---- -A (16-bit) and its diagonal blocks (fp32), P' (image, staged) from TMEM.
         // Warp w reads TMEM lane quarter w % 4 (rows 0-63: K K^T, 64-127: Q K^T);
         // warps w and w + 4 split the columns a quarter's rows need: rows 0-31
@@ -541,11 +547,11 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
                 };
                 if (quarter == 0) {
                     float v[16];
-                    tmem_ld16(lane_base + c_lo, v);
+                    tmem_ld16(lane_buf + c_lo, v);
                     emit(v, 16);
                 } else {
                     float v[32];
-                    tmem_ld32(lane_base + c_lo, v);
+                    tmem_ld32(lane_buf + c_lo, v);
                     emit(v, 32);
                 }
             } else {
@@ -566,7 +572,7 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
                 };
                 if (quarter == 2) {
                     float v[16];
-                    tmem_ld16(lane_base + c_lo, v);
+                    tmem_ld16(lane_buf + c_lo, v);
                     emit(v, 16);
                     // columns 32-63 of rows 0-31 are zero: 2 chunks per thread
 #pragma unroll
@@ -574,7 +580,7 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
                         *reinterpret_cast<uint4 *>(dst + sw128_chunk(t, 4 + 2 * half + q8)) = make_uint4(0u, 0u, 0u, 0u);
                 } else {
                     float v[32];
-                    tmem_ld32(lane_base + c_lo, v);
+                    tmem_ld32(lane_buf + c_lo, v);
                     emit(v, 32);
                 }
             }
@@ -586,28 +592,33 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
             bulk_store(rec + REC_P, sm + A_PS, 8192);
             bulk_commit();
         }
-        // ---- D_J = (I + A_JJ)^{-1} by forward substitution: four threads per
-        // column cl of block J (consecutive lanes), thread p holding rows 4p .. 4p+3
-        {
-            const int J = tid >> 6, cl = (tid >> 2) & 15, pr = tid & 3;
+        // ---- D_J = (I + A_JJ)^{-1} by forward substitution: warp J (< 4), lane
+        // cl (< 16) computes column cl of D_J
+        if (warp < 4 && lane < 16) {
+            const int J = warp, cl = lane;
             const float *Aj = Adt + J * 272;  // Aj[l * 16 + r] = A_JJ[r][l]
             E *Dj = reinterpret_cast<E *>(sD + J * 512);
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            float4 col = *reinterpret_cast<const float4 *>(Aj + 4 * pr);  // column 0, rows 4p ..
+            float acc[16], col[16];  // col: column l of A_JJ, loaded one step ahead
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                acc[r] = 0.f;
+                col[r] = Aj[r];
+            }
 #pragma unroll
             for (int l = 0; l < 16; ++l) {
-                const int owner = l >> 2;
-                float4 nxt = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (l + 1 < 16) nxt = *reinterpret_cast<const float4 *>(Aj + (l + 1) * 16 + 4 * pr);
-                float mine = 0.f;
-                if (pr == owner) mine = (l < cl) ? 0.f : ((l == cl) ? 1.f : -acc[l & 3]);
-                const float x = __shfl_sync(0xffffffffu, mine, (lane & ~3) | owner);  // D_J[l][cl]
-                if (pr == owner) Dj[(d_off(l, cl >> 3) >> 1) + (cl & 7)] = Elem<E>::from(x);
-                const float cv[4] = {col.x, col.y, col.z, col.w};
+                float nxt[16];
+                if (l + 1 < 16) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (4 * pr + j > l) acc[j] = fmaf(cv[j], x, acc[j]);
-                col = nxt;
+                    for (int r = 0; r < 16; ++r) nxt[r] = (r > l + 1) ? Aj[(l + 1) * 16 + r] : 0.f;
+                }
+                const float x = (l < cl) ? 0.f : ((l == cl) ? 1.f : -acc[l]);  // D_J[l][cl]
+                Dj[(d_off(l, cl >> 3) >> 1) + (cl & 7)] = Elem<E>::from(x);
+#pragma unroll
+                for (int r = l + 1; r < 16; ++r) acc[r] = fmaf(col[r], x, acc[r]);
+                if (l + 1 < 16) {
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) col[r] = nxt[r];
+                }
             }
         }
         // every warp: its right-hand-side columns, transposed, for all four token blocks
@@ -629,7 +640,8 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
         if (__syncthreads_or(!ok)) { failed = true; break; }
         if (tid == 0) {
             // K, Q and V have been read: the next unit's copies may land
-            kq_pending = v_pending = issue_loads(nxt);
+            v_pending = issue_loads(nxt);
+            kq_pending = v_pending;
         }
         // ---- block substitution: X_J^T = (R_J^T - sum_{K<J} X_K^T A_JK^T) D_J^T
         {
@@ -694,21 +706,33 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
             }
         }
         fence_proxy_async();
+        fence_before_sync();
         __syncthreads();
         if (tid == 0) {
             bulk_store(rec + REC_U, sm + A_US, 16384);
             bulk_store(rec + REC_W, sm + A_WS, 16384);
             bulk_commit();
+            // the next unit's [K; Q] K^T, into the other TMEM buffer
+            if (nxt.valid && !kq_pending_fail) {
+                if (issue_kq_mma(it + 1, tbase)) {
+                    kq_pending = false;
+                    mma_pending = true;
+                } else {
+                    kq_pending_fail = true;  // reported at the next unit's first check
+                }
+            }
         }
     }
     if (failed) {
         if (tid == 0) {
             atomicOr(p.err, (uint32_t)GDN_DEVERR_TIMEOUT);
             // copies and MMAs in flight must finish before the CTA exits
-            const uint32_t ph = (uint32_t)it & 1u;
-            if (kq_pending) mbar_wait(bar_kq, ph, kWaitNs);
-            if (v_pending) mbar_wait(bar_v, ph, kWaitNs);
-            if (mma_pending) mbar_wait(bar_mma, ph, kWaitNs);
+            // (copies of this unit or of the next, whichever were issued last)
+            for (uint32_t ph = 0; ph < 2; ++ph) {
+                if (kq_pending) mbar_wait(bar_kq, ph, kWaitNs / 4);
+                if (v_pending) mbar_wait(bar_v, ph, kWaitNs / 4);
+                if (mma_pending) mbar_wait(bar_mma, ph, kWaitNs / 4);
+            }
         }
     }
     // (without a timeout nothing is in flight here: issue_loads issues nothing past the last unit)
