@@ -261,6 +261,9 @@ constexpr uint32_t A_SMEM = A_BAR + 64 + 1024;    // + alignment slack
 constexpr uint32_t A_TMEM_COLS = 128;  // [K;Q] K^T of this unit and of the next, by unit parity
 constexpr int kIntraThreads = 256;
 constexpr int kIntraCtasPerSm = 2;
+constexpr uint32_t kBarAWritten = 1;  // named barrier of the A warps (0, 1, 4, 5)
+constexpr uint32_t kBarPImage = 2;    // named barrier of the P' warps (2, 3, 6, 7)
+constexpr int kPStoreThread = 64;     // issues (and drains) the P' image stores
 static_assert(A_VEC + 5 * 256 <= A_PS, "phase A shared-memory layout overlaps");
 static_assert(A_SMEM * kIntraCtasPerSm + 2048 <= 232448, "two chunk-parallel CTAs must fit an SM");
 
@@ -506,7 +509,7 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
             }
         }
         ok = mbar_wait(bar_mma, ph, p.wait_ns);  // this unit's [K; Q] K^T
-        if (tid == 0) bulk_wait_read_all();  // the last unit's staged images have been read
+        if (tid == 0 || tid == kPStoreThread) bulk_wait_read_all();  // the last unit's staged images have been read
         if (__syncthreads_or(!ok)) { failed = true; break; }
         fence_after_sync();
         if (tid == 0) mma_pending = false;
@@ -585,17 +588,23 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
                 }
             }
         }
-        fence_proxy_async();
         fence_before_sync();
-        __syncthreads();
-        if (tid == 0) {
-            bulk_store(rec + REC_P, sm + A_PS, 8192);
-            bulk_commit();
+        if (quarter >= 2) {
+            // P' warps: the image is staged; one of them stores it
+            fence_proxy_async();
+            named_bar(kBarPImage, 128);
+            if (tid == kPStoreThread) {
+                bulk_store(rec + REC_P, sm + A_PS, 8192);
+                bulk_commit();
+            }
+        } else {
+            named_bar(kBarAWritten, 128);  // -A and the diagonal blocks written (A warps)
         }
-        // ---- D_J = (I + A_JJ)^{-1} by forward substitution: warp J (< 4), lane
-        // cl (< 16) computes column cl of D_J
-        if (warp < 4 && lane < 16) {
-            const int J = warp, cl = lane;
+        // ---- D_J = (I + A_JJ)^{-1} by forward substitution, while the P' warps
+        // finish: warp 0 (J = 0, 1) and warp 4 (J = 2, 3), lane cl % 16 computes
+        // column cl of D_J
+        if (warp == 0 || warp == 4) {
+            const int J = (warp >> 1) + (lane >> 4), cl = lane & 15;
             const float *Aj = Adt + J * 272;  // Aj[l * 16 + r] = A_JJ[r][l]
             E *Dj = reinterpret_cast<E *>(sD + J * 512);
             float acc[16], col[16];  // col: column l of A_JJ, loaded one step ahead
@@ -736,7 +745,7 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
         }
     }
     // (without a timeout nothing is in flight here: issue_loads issues nothing past the last unit)
-    if (tid == 0) bulk_wait_all();  // the records have been written
+    if (tid == 0 || tid == kPStoreThread) bulk_wait_all();  // the records have been written
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, A_TMEM_COLS);
@@ -974,6 +983,15 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
                 // Delta = U - W S^T for token t, NC of the TV columns
                 const int t = 32 * (quarter - 2) + lane;
                 const float wt = ok ? vec[64 + t] : 0.f;
+                // this row's U chunks, read while D1 runs
+                uint4 uraw[Q8];
+#pragma unroll
+                for (int q8 = 0; q8 < Q8; ++q8) {
+                    const int c = c0 + 8 * q8;  // column of the tile: U tile (c / 32), chunk (c % 32) / 8
+                    uraw[q8] = ok ? *reinterpret_cast<const uint4 *>(st + Cfg::ST_U + (c >> 5) * 4096 +
+                                                                      u32_chunk(t, (c & 31) >> 3))
+                                  : make_uint4(0u, 0u, 0u, 0u);
+                }
                 if (ok) ok = mbar_wait(bar1, cc & 1, p.wait_ns);
                 if (ok) {
                     fence_after_sync();
@@ -986,11 +1004,9 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
                                      : nullptr;
 #pragma unroll
                     for (int q8 = 0; q8 < Q8; ++q8) {
-                        // column c0 + 8 q8 of the tile: U tile (c / 32), chunk (c % 32) / 8
                         const int c = c0 + 8 * q8;
-                        const uint8_t *su = st + Cfg::ST_U + (c >> 5) * 4096;
                         float u[8], dd[8], dw[8];
-                        unpack8<E>(*reinterpret_cast<const uint4 *>(su + u32_chunk(t, (c & 31) >> 3)), u);
+                        unpack8<E>(uraw[q8], u);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             dd[e] = u[e] - ws[8 * q8 + e];
