@@ -429,7 +429,7 @@ def run_ours(args, rank, world, local_rank):
                     "frac": round(pb / pre_avg_s / 1e9 / hbm_peak, 4),
                     "algorithmic_bytes_per_launch": pb,
                     "tensor_frac": round(pf / pre_avg_s / 1e12 / tf_peak, 4),
-                    "algorithmic_flops_per_launch": pf, "traffic": None,
+                    "algorithmic_flops_per_launch": pf, "traffic": PREFILL_TRAFFIC_BYTES,
                 },
                 "e2e": e2e_pre,
                 "checkpoints": {
@@ -699,10 +699,12 @@ def run_front_end(gdn, stream, q, k, v, a, bt, S, out, cc, su, gp, p_out, p_fs, 
 
 PREFILL_LAUNCHES = 2  # kernels one gdn_prefill_chunked call launches on this workload (tensor-core path)
 # DRAM bytes (read + write) of one launch of the current kernels, each from one
-# ncu capture of that kernel on this workload: decode at B=256 and the fused
-# replay + verify step.  Reset to None whenever the kernel changes.
+# ncu capture of that kernel on this workload: decode at B=256, the fused
+# replay + verify step, and one prefill call (its two kernels, chunk-parallel
+# then carry).  Reset to None whenever the kernel changes.
 DECODE_TRAFFIC_BYTES = 541_250_304 + 483_723_776
 VERIFY_TRAFFIC_BYTES = 567_168_768 + 391_290_624
+PREFILL_TRAFFIC_BYTES = (68_461_824 + 31_582_208) + (123_141_376 + 16_210_432)
 
 
 E2E_GROUPS = 8       # decode e2e: row groups pipelined on their own streams
