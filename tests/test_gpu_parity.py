@@ -408,6 +408,35 @@ def test_query_scale_every_path(gdn, oracle_mod, path):
     assert rel(fs, rS) < tol
 
 
+def test_uniform_rows_tensor_core_prefill_units_span_rows(gdn, oracle_mod):
+    """Two rows of equal length (no cu_seqlens) on the tensor-core prefill,
+    with more (chunk, value head) units than chunk-parallel CTAs, so every
+    CTA walks several units across both rows, and few enough tiles for the
+    32-row carry.  Checked per (64-token chunk, value head) of the output,
+    the ragged 12-token tail of each row included, and per (row, head) of
+    the final state."""
+    from gated_deltanet_recurrence_02_gb300.inputs import make_inputs
+    T, B, Hk, Hv = 1100, 2, 8, 16  # 18 chunks per row: 2 x 18 x 16 = 576 units
+    x = make_inputs(2101, lengths=[T] * B, Hk=Hk, Hv=Hv, dk=128, dv=128, dtype_qkv="bf16",
+                    dtype_gate="f32")
+    g = to_dev(x)
+    o, fs = gdn.gdn_prefill_chunked(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=B, T=T,
+                                    initial_state=g["initial_state"], chunk=64)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_errors() == 0
+    ro, rS, _ = oracle_mod.recurrent(x.q, x.k, x.v, x.alpha, x.beta, B=B, Hk=Hk, Hv=Hv, dk=128,
+                                     dv=128, T=T, initial_state=x.initial_state, threads=THREADS)
+    tol = TOL[torch.bfloat16]
+    assert rel(o, ro) < tol and rel(fs, rS) < tol
+    bounds = sorted({min(r * T + c, (r + 1) * T) for r in range(B) for c in range(0, T + 64, 64)})
+    e_o, at_o = rel_per_unit(o, ro, bounds)
+    assert e_o < tol, (e_o, at_o)
+    e_s, at_s = rel_per_unit(fs, rS, list(range(B + 1)))
+    assert e_s < tol, (e_s, at_s)
+    print(f"2 x {T} tokens: worst per (chunk, head) output {e_o:.2e} at {at_o}, "
+          f"state {e_s:.2e} at {at_s}")
+
+
 def test_many_packed_rows_tensor_core_prefill(gdn, oracle_mod):
     """300 packed rows of 0 .. 40 tokens (many empty or shorter than a chunk)
     through the tensor-core prefill: every row's output and final state
