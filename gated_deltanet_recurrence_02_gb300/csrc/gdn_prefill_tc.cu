@@ -55,6 +55,7 @@
 // GDN_DEVERR_TIMEOUT, waits (bounded) for its copies in flight, releases its
 // TMEM and exits.
 #include <cstring>
+#include <type_traits>
 #include <mutex>
 
 #include "gdn_internal.cuh"
@@ -115,6 +116,14 @@ __device__ __forceinline__ void unpack8(uint4 u, float *v) {
            d = Elem<E>::unpack2(u.w);
     v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y; v[4] = c.x; v[5] = c.y; v[6] = d.x; v[7] = d.y;
 }
+
+// 2^x on the special-function unit (base-2 exponential; e^x = 2^(x log2 e)).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;
 
 // Byte offset of the 16-byte chunk holding elements [8*q, 8*q+8) of row r.
 __device__ __forceinline__ uint32_t sw128_chunk(int r, int q) {
@@ -252,7 +261,7 @@ constexpr uint32_t A_V = 32768;     // V image: dv 0-63 | 64-127, 8 KB each
 constexpr uint32_t A_NA = 49152;    // -A, 16-bit, 64 rows of 128 B, 16-byte chunks swizzled by row % 8
 constexpr uint32_t A_AD = A_NA + 8192;            // diagonal blocks, fp32, transposed: [J][col][row], J stride 272
 constexpr uint32_t A_D = A_AD + 4 * 272 * 4;      // D_J, 16-bit row-major, 32 B rows (chunks swizzled), 512 B each
-constexpr uint32_t A_VEC = A_D + 4 * 512;         // g, beta, beta gamma (r), 1/|k|, 1/|q|: 5 x 64 floats
+constexpr uint32_t A_VEC = A_D + 4 * 512;         // g, beta, beta gamma (r), 1/|k|, 1/|q|, g log2(e): 6 x 64 floats
 constexpr uint32_t A_PS = 65536;                  // P' image on its way out (8 KB)
 constexpr uint32_t A_US = A_PS + 8192;            // U tiles on their way out (16 KB)
 constexpr uint32_t A_WS = A_US + 16384;           // W image on its way out (16 KB)
@@ -264,7 +273,7 @@ constexpr int kIntraCtasPerSm = 2;
 constexpr uint32_t kBarAWritten = 1;  // named barrier of the A warps (0, 1, 4, 5)
 constexpr uint32_t kBarPImage = 2;    // named barrier of the P' warps (2, 3, 6, 7)
 constexpr int kPStoreThread = 64;     // issues (and drains) the P' image stores
-static_assert(A_VEC + 5 * 256 <= A_PS, "phase A shared-memory layout overlaps");
+static_assert(A_VEC + 6 * 256 <= A_PS, "phase A shared-memory layout overlaps");
 static_assert(A_SMEM * kIntraCtasPerSm + 2048 <= 232448, "two chunk-parallel CTAs must fit an SM");
 
 // Row r, 16-byte chunk q of -A (rows of 128 B).
@@ -290,6 +299,7 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
     uint8_t *sD = sm + A_D;
     float *vg = reinterpret_cast<float *>(sm + A_VEC);
     float *vbeta = vg + 64, *vbw = vg + 128, *vkn = vg + 192, *vqn = vg + 256;
+    float *vgl = vg + 320;  // g log2(e): e^{g_t - g_i} = 2^{vgl_t - vgl_i}
     uint64_t *bar_kq = reinterpret_cast<uint64_t *>(sm + A_BAR);
     uint64_t *bar_v = bar_kq + 1;
     uint64_t *bar_mma = bar_kq + 2;
@@ -487,6 +497,8 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
             const float g0 = expf(x0), g1 = expf(x1), w0 = expf(glast - x0), w1 = expf(glast - x1);
             vg[lane] = x0;
             vg[lane + 32] = x1;
+            vgl[lane] = x0 * kLog2e;
+            vgl[lane + 32] = x1 * kLog2e;
             const float rk0 = NORM ? vkn[lane] : 1.f, rk1 = NORM ? vkn[lane + 32] : 1.f;
             const float rq0 = NORM ? vqn[lane] : 1.f, rq1 = NORM ? vqn[lane + 32] : 1.f;
             vbw[lane] = vbeta[lane] * g0 * rk0;
@@ -523,60 +535,69 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
             const bool aside = quarter < 2;  // A (K rows) or P' (Q rows)
             const int t = 32 * (quarter & 1) + lane;
             const int c_lo = (quarter & 1) ? 32 * half : 16 * half;
-            const float gt = vg[t];
+            const float gtl = vgl[t];
             if (aside) {
                 // A[t][i] = beta_t e^{g_t - g_i} k_t.k_i  (i < t), stored negated;
                 // the diagonal block (J, J), J = t / 16, also in fp32 for D_J
                 const float bt = vbeta[t] * (NORM ? vkn[t] : 1.f);
                 const int J = t >> 4;
-                auto emit = [&](const float *v, int nc) {
-                    for (int q8 = 0; q8 < nc / 8; ++q8) {
-                        float a[8];
+                // every column first (broadcast reads of their g), then every
+                // store, so that no shared-memory read waits behind a store
+                auto emit = [&](const float *v, auto ncols) {
+                    constexpr int NCOL = decltype(ncols)::value;
+                    float a[NCOL];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int i = c_lo + 8 * q8 + e;
-                            const float kk = NORM ? v[8 * q8 + e] * vkn[i] : v[8 * q8 + e];
-                            a[e] = (i < t) ? bt * __expf(gt - vg[i]) * kk : 0.f;
+                    for (int e = 0; e < NCOL; ++e) {
+                        const int i = c_lo + e;
+                        const float kk = NORM ? v[e] * vkn[i] : v[e];
+                        a[e] = (i < t) ? bt * ex2_approx(gtl - vgl[i]) * kk : 0.f;
+                    }
+#pragma unroll
+                    for (int blk = 0; blk < NCOL / 16; ++blk) {
+                        if ((c_lo >> 4) + blk == J) {
+                            float *dst = Adt + J * 272 + (t & 15);  // column e of the block at e * 16
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) dst[e * 16] = a[16 * blk + e];
                         }
-                        if (((c_lo + 8 * q8) >> 4) == J) {
-                            float *dst = Adt + J * 272 + ((c_lo + 8 * q8) & 15) * 16 + (t & 15);
+                    }
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) dst[e * 16] = a[e];
-                        }
+                    for (int q8 = 0; q8 < NCOL / 8; ++q8) {
+                        float na[8];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) a[e] = -a[e];
-                        *reinterpret_cast<uint4 *>(sNA + na_off(t, (c_lo >> 3) + q8)) = pack8<E>(a);
+                        for (int e = 0; e < 8; ++e) na[e] = -a[8 * q8 + e];
+                        *reinterpret_cast<uint4 *>(sNA + na_off(t, (c_lo >> 3) + q8)) = pack8<E>(na);
                     }
                 };
                 if (quarter == 0) {
                     float v[16];
                     tmem_ld16(lane_buf + c_lo, v);
-                    emit(v, 16);
+                    emit(v, std::integral_constant<int, 16>{});
                 } else {
                     float v[32];
                     tmem_ld32(lane_buf + c_lo, v);
-                    emit(v, 32);
+                    emit(v, std::integral_constant<int, 32>{});
                 }
             } else {
                 // P'[t][i] = e^{g_t - g_i} (scale q_t).k_i (i <= t), image staged for a bulk store
                 const float sc = p.scale * (NORM ? vqn[t] : 1.f);
                 uint8_t *dst = sm + A_PS;
-                auto emit = [&](const float *v, int nc) {
-                    for (int q8 = 0; q8 < nc / 8; ++q8) {
-                        float pv[8];
+                auto emit = [&](const float *v, auto ncols) {
+                    constexpr int NCOL = decltype(ncols)::value;
+                    float pv[NCOL];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int i = c_lo + 8 * q8 + e;
-                            const float qk = NORM ? v[8 * q8 + e] * vkn[i] : v[8 * q8 + e];
-                            pv[e] = (i <= t) ? __expf(gt - vg[i]) * (sc * qk) : 0.f;
-                        }
-                        *reinterpret_cast<uint4 *>(dst + sw128_chunk(t, (c_lo >> 3) + q8)) = pack8<E>(pv);
+                    for (int e = 0; e < NCOL; ++e) {
+                        const int i = c_lo + e;
+                        const float qk = NORM ? v[e] * vkn[i] : v[e];
+                        pv[e] = (i <= t) ? ex2_approx(gtl - vgl[i]) * (sc * qk) : 0.f;
                     }
+#pragma unroll
+                    for (int q8 = 0; q8 < NCOL / 8; ++q8)
+                        *reinterpret_cast<uint4 *>(dst + sw128_chunk(t, (c_lo >> 3) + q8)) = pack8<E>(pv + 8 * q8);
                 };
                 if (quarter == 2) {
                     float v[16];
                     tmem_ld16(lane_buf + c_lo, v);
-                    emit(v, 16);
+                    emit(v, std::integral_constant<int, 16>{});
                     // columns 32-63 of rows 0-31 are zero: 2 chunks per thread
 #pragma unroll
                     for (int q8 = 0; q8 < 2; ++q8)
@@ -584,7 +605,7 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
                 } else {
                     float v[32];
                     tmem_ld32(lane_buf + c_lo, v);
-                    emit(v, 32);
+                    emit(v, std::integral_constant<int, 32>{});
                 }
             }
         }
