@@ -704,7 +704,7 @@ PREFILL_LAUNCHES = 2  # kernels one gdn_prefill_chunked call launches on this wo
 # then carry).  Reset to None whenever the kernel changes.
 DECODE_TRAFFIC_BYTES = 541_250_304 + 483_723_776
 VERIFY_TRAFFIC_BYTES = 567_168_768 + 391_290_624
-PREFILL_TRAFFIC_BYTES = (68_461_824 + 31_582_208) + (123_141_376 + 16_210_432)
+PREFILL_TRAFFIC_BYTES = (68_439_552 + 31_748_352) + (123_136_768 + 16_706_560)
 
 
 E2E_GROUPS = 8       # decode e2e: row groups pipelined on their own streams
