@@ -701,10 +701,13 @@ PREFILL_LAUNCHES = 2  # kernels one gdn_prefill_chunked call launches on this wo
 # DRAM bytes (read + write) of one launch of the current kernels, each from one
 # ncu capture of that kernel on this workload: decode at B=256, the fused
 # replay + verify step, and one prefill call (its two kernels, chunk-parallel
-# then carry).  Reset to None whenever the kernel changes.
+# then carry, captured back to back without ncu's cache flushing, after a
+# read-only pass over a buffer larger than L2, so that the carry meets the
+# chunk-parallel kernel's records where they are).  Reset to None whenever the
+# kernel changes.
 DECODE_TRAFFIC_BYTES = 541_250_304 + 483_723_776
 VERIFY_TRAFFIC_BYTES = 567_168_768 + 391_290_624
-PREFILL_TRAFFIC_BYTES = (68_439_552 + 31_748_352) + (123_136_768 + 16_706_560)
+PREFILL_TRAFFIC_BYTES = (68_728_320 + 21_744_384) + (84_232_192 + 43_203_840)
 
 
 E2E_GROUPS = 8       # decode e2e: row groups pipelined on their own streams

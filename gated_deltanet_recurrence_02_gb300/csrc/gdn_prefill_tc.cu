@@ -311,6 +311,9 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
     const int Hv = p.Hv, Hk = p.Hk, G = Hv / Hk;
     const long su_slot = (long)Hv + (long)Hk * D + (long)Hv * D;
     constexpr bool kbf = Elem<E>::kBf16;
+    // L2 priorities: V is read here only; the records are read by the carry
+    // kernel next, and the footprint of one call's inputs and records exceeds L2
+    const uint64_t pol_read_once = l2_evict_first_policy(), pol_keep = l2_evict_last_policy();
 
     // Units are (global chunk gc, value head h), unit index gc * Hv + h; this
     // CTA's units advance by gridDim.x, i.e. by (gridDim.x / Hv) chunks and
@@ -355,8 +358,8 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
         tma_load_3d(sKQ + 8192, &mq, 0, hk, (int)tok0, bar_kq);
         tma_load_3d(sKQ + 24576, &mq, 64, hk, (int)tok0, bar_kq);
         mbar_arrive_expect_tx(bar_v, 16384);
-        tma_load_3d(sm + A_V, &mv, 0, h, (int)tok0, bar_v);
-        tma_load_3d(sm + A_V + 8192, &mv, 64, h, (int)tok0, bar_v);
+        tma_load_3d_hint(sm + A_V, &mv, 0, h, (int)tok0, bar_v, pol_read_once);
+        tma_load_3d_hint(sm + A_V + 8192, &mv, 64, h, (int)tok0, bar_v, pol_read_once);
         return true;
     };
     // thread 0: [K; Q] K^T of the unit with loop index `ui` into TMEM buffer ui % 2
@@ -615,7 +618,7 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
             fence_proxy_async();
             named_bar(kBarPImage, 128);
             if (tid == kPStoreThread) {
-                bulk_store(rec + REC_P, sm + A_PS, 8192);
+                bulk_store_hint(rec + REC_P, sm + A_PS, 8192, pol_keep);
                 bulk_commit();
             }
         } else {
@@ -739,8 +742,8 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
         fence_before_sync();
         __syncthreads();
         if (tid == 0) {
-            bulk_store(rec + REC_U, sm + A_US, 16384);
-            bulk_store(rec + REC_W, sm + A_WS, 16384);
+            bulk_store_hint(rec + REC_U, sm + A_US, 16384, pol_keep);
+            bulk_store_hint(rec + REC_W, sm + A_WS, 16384, pol_keep);
             bulk_commit();
             // the next unit's [K; Q] K^T, into the other TMEM buffer
             if (nxt.valid && !kq_pending_fail) {
@@ -874,6 +877,7 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
 
     if (warp == kCopierWarp) {
         // ======================= copier warp ============================
+        const uint64_t pol_read_once = l2_evict_first_policy();  // the records are read once
         auto issue_stage = [&](int cc) {
             const int s = cc % NS;
             uint8_t *st = sm + s * Cfg::ST_BYTES;
@@ -882,13 +886,14 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
             mbar_arrive_expect_tx(&full[s], Cfg::STAGE_TX);
             tma_load_3d(st + Cfg::ST_A1, &mq, 0, hk, t0, &full[s]);
             tma_load_3d(st + Cfg::ST_A1 + 16384, &mq, 64, hk, t0, &full[s]);
-            bulk_load(st + Cfg::ST_A1 + 8192, rec + REC_W, 8192, &full[s]);
-            bulk_load(st + Cfg::ST_A1 + 24576, rec + REC_W + 8192, 8192, &full[s]);
+            bulk_load_hint(st + Cfg::ST_A1 + 8192, rec + REC_W, 8192, &full[s], pol_read_once);
+            bulk_load_hint(st + Cfg::ST_A1 + 24576, rec + REC_W + 8192, 8192, &full[s], pol_read_once);
             tma_load_3d(st + Cfg::ST_K, &mk, 0, hk, t0, &full[s]);
             tma_load_3d(st + Cfg::ST_K + 8192, &mk, 64, hk, t0, &full[s]);
-            bulk_load(st + Cfg::ST_P, rec + REC_P, 8192, &full[s]);
-            bulk_load(st + Cfg::ST_U, rec + REC_U + vt * Cfg::kUBytes, Cfg::kUBytes, &full[s]);
-            bulk_load(st + Cfg::ST_VEC, rec + REC_VEC, 1024, &full[s]);
+            bulk_load_hint(st + Cfg::ST_P, rec + REC_P, 8192, &full[s], pol_read_once);
+            bulk_load_hint(st + Cfg::ST_U, rec + REC_U + vt * Cfg::kUBytes, Cfg::kUBytes, &full[s],
+                           pol_read_once);
+            bulk_load_hint(st + Cfg::ST_VEC, rec + REC_VEC, 1024, &full[s], pol_read_once);
         };
         auto prefetch_chunk = [&](int cc) {
             const uint8_t *rec = rec0 + (size_t)cc * rec_stride;
