@@ -23,10 +23,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
-    return (uint32_t)(r * 128 + ((((c >> 3) ^ (r & 7)) & 7) << 4) + (c & 7) * 2);
-}
-
 // ------------------------------------------------------------ mbarrier ---
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
@@ -92,14 +88,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
 
 // ----------------------------------------------------------------- TMA ---
 
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1,
-                                            uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
-        : "memory");
-}
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int c0, int c1,
                                             int c2, uint64_t *bar) {
     asm volatile(
@@ -144,6 +132,8 @@ __device__ __forceinline__ void bulk_load_hint(void *dst, const void *src, uint3
         "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
         : "memory");
 }
+// Contiguous shared -> global copy by the async proxy (both addresses 16-byte
+// aligned, bytes % 16 == 0), tracked in the issuing thread's bulk group.
 __device__ __forceinline__ void bulk_store_hint(void *dst, const void *src, uint32_t bytes, uint64_t pol) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst),
                  "r"(smem_u32(src)), "r"(bytes), "l"(pol)
@@ -154,13 +144,6 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *map, int c
     asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
                      reinterpret_cast<uint64_t>(map)),
                  "r"(c0), "r"(c1), "r"(c2)
-                 : "memory");
-}
-// Contiguous shared -> global copy by the async proxy (both addresses 16-byte
-// aligned, bytes % 16 == 0), tracked in the issuing thread's bulk group.
-__device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
-                 "r"(bytes)
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
@@ -176,10 +159,6 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-// Arrive on a named barrier without waiting (producers of a bar.sync consumer).
-__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t count) {
-    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -317,13 +296,6 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], const void *row_
 // matrix l / 8.
 __device__ __forceinline__ void stsm_x4_trans(void *row_addr, const uint32_t (&r)[4]) {
     asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(row_addr)),
-                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
-                 : "memory");
-}
-// Non-transposing store: matrix i held as (row g, cols 2t..2t+1) in r[i] is
-// stored as is; lane l gives the address of row l % 8 of matrix l / 8.
-__device__ __forceinline__ void stsm_x4(void *row_addr, const uint32_t (&r)[4]) {
-    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(row_addr)),
                  "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
                  : "memory");
 }
