@@ -4,8 +4,8 @@
 // backend" (executorch issue 23097), work list: chunked GDN prefill with an
 // explicit initial and final state and an FP32 recurrence.  This is the
 // general-shape path (any dk, dv in {32, 64, 128}, chunk in {16, 32, 64}, any
-// storage dtype); the tensor-core kernel takes the dk = dv = 128, chunk = 64,
-// 16-bit case.
+// storage dtype); the tensor-core kernels take chunk 64 with 16-bit inputs,
+// so this one runs fp32 inputs and chunks of 16 and 32.
 //
 // One CTA (256 threads) carries a 32-row tile of one (row b, value head h)
 // state through all chunks of that row.  Inside a chunk of n tokens with start

@@ -1,6 +1,9 @@
 // gdn_prefill_tc.cu -- chunked prefill on the 5th-generation tensor cores
-// (tcgen05 MMA, TMEM accumulators, TMA), for dk = dv = 128, chunk 64, bf16 or
-// fp16 inputs.
+// (tcgen05 MMA, TMEM accumulators, TMA), for dk, dv in {32, 64, 128}, chunk
+// 64, bf16 or fp16 inputs.  The kernels work on 128-wide tiles: a smaller
+// head is read as zero-padded to 128 (the tensor maps' out-of-bounds fill),
+// which changes no product with the real features, and only its real rows
+// and columns are written.
 //
 // "Enable the native Kev example on NVIDIA GPUs through ExecuTorch's AOTI CUDA
 // backend" (executorch issue 23097), work list: a chunked GDN prefill with an
@@ -67,7 +70,7 @@ namespace {
 using namespace tc;
 
 constexpr int C = 64;    // chunk
-constexpr int D = 128;   // dk = dv
+constexpr int D = 128;   // tile width of dk and of dv (smaller heads are zero-padded to it)
 constexpr uint64_t kWaitNs = kDefaultWaitNs;  // drains of the CTA's own copies
 
 // Workspace record per (chunk, value head), bytes.
@@ -315,7 +318,7 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
     grid_launch_dependents();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int Hv = p.Hv, Hk = p.Hk, G = Hv / Hk;
-    const long su_slot = (long)Hv + (long)Hk * D + (long)Hv * D;
+    const long su_slot = (long)Hv + (long)Hk * p.dk + (long)Hv * p.dv;
     constexpr bool kbf = Elem<E>::kBf16;
     // L2 priorities: V is read here only; the records are read by the carry
     // kernel next, and the footprint of one call's inputs and records exceeds L2
@@ -523,10 +526,11 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
             // captured keys: the (normalised) key the recurrence used
             const E *kg = reinterpret_cast<const E *>(p.k);
             const int nk = ncap < n ? ncap : n;
-            for (int e = tid; e < nk * D; e += kIntraThreads) {
-                const int t = e / D, j = e % D;
-                su0[t * su_slot + Hv + (long)hk * D + j] =
-                    ld_f(kg + ((tok0 + t) * Hk + hk) * D + j) * (NORM ? vkn[t] : 1.f);
+            const int dk = p.dk;
+            for (int e = tid; e < nk * dk; e += kIntraThreads) {
+                const int t = e / dk, j = e % dk;
+                su0[t * su_slot + Hv + (long)hk * dk + j] =
+                    ld_f(kg + ((tok0 + t) * Hk + hk) * dk + j) * (NORM ? vkn[t] : 1.f);
             }
         }
         ok = mbar_wait(bar_mma, ph, p.wait_ns);  // this unit's [K; Q] K^T
@@ -853,7 +857,7 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     int len;
     row_range(p.cu_seqlens, b, p.T, rtok0, len);
     const int nc = n_chunks(len);
-    const long su_slot = (long)Hv + (long)Hk * D + (long)Hv * D;
+    const long su_slot = (long)Hv + (long)Hk * p.dk + (long)Hv * p.dv;
     const int ncap = XO ? prefill_ncap(p, b, len) : 0;
     const uint8_t *rec0 = records(p) + (size_t)chunk_base(p, b) * Hv * REC_BYTES +
                           (size_t)h * REC_BYTES;
@@ -987,9 +991,12 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
         const int j = 32 * quarter + lane;
         const int c0 = NC * half;
         float S[NC];
-        const float *s0 = initial_state_ptr(p.s0, p.s0_idx, p.n_s0, b, h, Hv, D, D, p.err);
+        // (columns j >= dk of a smaller head stay zero: so do K's and Q's there)
+        const int dk = p.dk, dv = p.dv;
+        const bool jin = j < dk;
+        const float *s0 = initial_state_ptr(p.s0, p.s0_idx, p.n_s0, b, h, Hv, dv, dk, p.err);
 #pragma unroll
-        for (int i = 0; i < NC; ++i) S[i] = s0 ? s0[(size_t)(i0 + c0 + i) * D + j] : 0.f;
+        for (int i = 0; i < NC; ++i) S[i] = (s0 && jin) ? s0[(size_t)(i0 + c0 + i) * dk + j] : 0.f;
 #pragma unroll
         for (int q8 = 0; q8 < Q8; ++q8)
             *reinterpret_cast<uint4 *>(sS + sw128_chunk(j, c0 / 8 + q8)) = pack8<E>(S + 8 * q8);
@@ -1031,8 +1038,8 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
                     tmem_ld_cols<NC>(lane_base + d1 + c0, ws);
                     // captured tokens: Delta's row t is token t's delta
                     float *cap = (cc * C + t < ncap)
-                                     ? p.su + ((size_t)b * p.capacity + cc * C + t) * su_slot + Hv + (size_t)Hk * D +
-                                           (size_t)h * D + i0 + c0
+                                     ? p.su + ((size_t)b * p.capacity + cc * C + t) * su_slot + Hv +
+                                           (size_t)Hk * p.dk + (size_t)h * p.dv + i0 + c0
                                      : nullptr;
 #pragma unroll
                     for (int q8 = 0; q8 < Q8; ++q8) {
@@ -1072,10 +1079,10 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
                 if constexpr (XO) {
                     // chunk-boundary checkpoint: the fp32 state after this chunk
                     const int ck = ckpt_slot(p, cc, len);
-                    if (ck >= 0) {
-                        float *dst = p.ckpt + ((((size_t)b * p.ckpt_cap + ck) * Hv + h) * D + i0 + c0) * D;
+                    if (ck >= 0 && jin) {
+                        float *dst = p.ckpt + ((((size_t)b * p.ckpt_cap + ck) * Hv + h) * dv + i0 + c0) * dk;
 #pragma unroll
-                        for (int i = 0; i < NC; ++i) __stcs(dst + (size_t)i * D + j, S[i]);
+                        for (int i = 0; i < NC; ++i) __stcs(dst + (size_t)i * dk + j, S[i]);
                     }
                 }
             }
@@ -1092,7 +1099,7 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
                     tmem_ld_cols<NC>(lane_base + d1 + c0, qs);
                     tmem_ld_cols<NC>(lane_base + d3 + c0, pd);
                     if (t < n) {
-                        E *dst = ob + ((rtok0 + (long)cc * C + t) * Hv + h) * (long)D + i0 + c0;
+                        E *dst = ob + ((rtok0 + (long)cc * C + t) * Hv + h) * (long)dv + i0 + c0;
 #pragma unroll
                         for (int q8 = 0; q8 < Q8; ++q8) {
                             float o[8];
@@ -1104,10 +1111,10 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
                 }
             }
         }
-        if (ok && p.s_final != nullptr) {
-            float *sf = p.s_final + (((size_t)b * Hv + h) * D + i0 + c0) * D;
+        if (ok && p.s_final != nullptr && jin) {
+            float *sf = p.s_final + (((size_t)b * Hv + h) * dv + i0 + c0) * dk;
 #pragma unroll
-            for (int i = 0; i < NC; ++i) sf[(size_t)i * D + j] = S[i];
+            for (int i = 0; i < NC; ++i) sf[(size_t)i * dk + j] = S[i];
         }
     }
     if (!ok && tid == 0) atomicOr(p.err, (uint32_t)GDN_DEVERR_TIMEOUT);
@@ -1140,12 +1147,14 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [total_T, H, 128] 16-bit tensor, box {64 features, 1 head, 64 tokens}, 128-byte swizzle.
-bool make_map(CUtensorMap *m, const void *ptr, int H, long total_T, bool bf16) {
+// [total_T, H, width] 16-bit tensor, box {64 features, 1 head, 64 tokens},
+// 128-byte swizzle.  A head narrower than 128 features reads as zero-padded
+// to 128: the box parts past `width` are out of bounds and come back as zeros.
+bool make_map(CUtensorMap *m, const void *ptr, int H, long total_T, bool bf16, int width) {
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)total_T};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+    cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)H, (cuuint64_t)total_T};
+    cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)H * width * 2};
     cuuint32_t box[3] = {64, 1, 64};
     cuuint32_t es[3] = {1, 1, 1};
     return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
@@ -1162,8 +1171,8 @@ cudaError_t launch_e(const PrefillParams &p, long total_T, long max_chunks, cuda
     memset(&mk, 0, sizeof(mk));
     memset(&mv, 0, sizeof(mv));
     // With no tokens at all no chunk exists and the maps are never used.
-    if (total_T > 0 && (!make_map(&mq, p.q, p.Hk, total_T, bf) || !make_map(&mk, p.k, p.Hk, total_T, bf) ||
-                        !make_map(&mv, p.v, p.Hv, total_T, bf)))
+    if (total_T > 0 && (!make_map(&mq, p.q, p.Hk, total_T, bf, p.dk) || !make_map(&mk, p.k, p.Hk, total_T, bf, p.dk) ||
+                        !make_map(&mv, p.v, p.Hv, total_T, bf, p.dv)))
         return cudaErrorInvalidValue;
     const bool norm = (p.conv & GDN_QK_L2NORM) != 0;
     auto intra = norm ? prefill_intra_kernel<E, XO, true> : prefill_intra_kernel<E, XO, false>;
@@ -1172,7 +1181,7 @@ cudaError_t launch_e(const PrefillParams &p, long total_T, long max_chunks, cuda
     if (e != cudaSuccess) return e;
     // carry instance: 32-row tiles while one wave of them fits the GPU (the
     // chain's latency decides), 64-row tiles for more rows (throughput decides)
-    const bool wide = (long)(D / 32) * p.Hv * p.B > (long)sm_count_of_current_device();
+    const bool wide = p.dv >= 64 && (long)(p.dv / 32) * p.Hv * p.B > (long)sm_count_of_current_device();
     e = wide ? set_smem_once<prefill_carry_kernel<E, XO, 64>>((int)CarryCfg<64>::B_SMEM)
              : set_smem_once<prefill_carry_kernel<E, XO, 32>>((int)CarryCfg<32>::B_SMEM);
     if (e != cudaSuccess) return e;
@@ -1189,7 +1198,7 @@ cudaError_t launch_e(const PrefillParams &p, long total_T, long max_chunks, cuda
     // its prologue (barriers, TMEM, the initial state) overlaps that kernel's
     // tail, and it waits for that kernel's records before reading them.
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(D / (wide ? 64 : 32), p.Hv, p.B);
+    cfg.gridDim = dim3(p.dv / (wide ? 64 : 32), p.Hv, p.B);
     cfg.blockDim = dim3(kCarryThreads);
     cfg.dynamicSmemBytes = wide ? CarryCfg<64>::B_SMEM : CarryCfg<32>::B_SMEM;
     cfg.stream = stream;
@@ -1209,7 +1218,8 @@ long max_chunks_of(int B, int T, bool varlen) {
 }  // namespace
 
 bool prefill_tc_supported(int dk, int dv, int chunk, int dt_qkv) {
-    return dk == D && dv == D && chunk == C && (dt_qkv == GDN_BF16 || dt_qkv == GDN_F16);
+    auto width_ok = [](int d) { return d == 32 || d == 64 || d == D; };
+    return width_ok(dk) && width_ok(dv) && chunk == C && (dt_qkv == GDN_BF16 || dt_qkv == GDN_F16);
 }
 
 size_t prefill_tc_workspace_bytes(int B, int T, int /*Hk*/, int Hv, bool varlen) {

@@ -1,7 +1,8 @@
 """GPU parity of gdn_prefill_chunked_checkpoints -- the chunked prefill that
 also writes the state at chunk boundaries -- against the fp64 oracle, on
 both prefill kernels (CUDA-core: fp32, d=32, chunk 16; tensor-core: bf16,
-d=128, chunk 64).
+d=128, chunk 64; smaller heads on the tensor-core path are covered in
+test_gpu_tc_head_sizes.py).
 
 Source: "Enable the native Kev example on the WebGPU backend" (executorch
 issue 23099): an immutable prefix snapshot reused later; here a snapshot is
