@@ -318,6 +318,7 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
     grid_launch_dependents();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int Hv = p.Hv, Hk = p.Hk, G = Hv / Hk;
+    const int ksteps = p.dk > 64 ? 8 : 4;  // K = 16 steps of the products over dk
     const long su_slot = (long)Hv + (long)Hk * p.dk + (long)Hv * p.dv;
     constexpr bool kbf = Elem<E>::kBf16;
     // L2 priorities: V is read here only; the records are read by the carry
@@ -380,6 +381,7 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
         const uint32_t id = idesc_f16(128, 64, false, false, kbf);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
+            if (k >= ksteps) break;  // a head of <= 64 features: its second K-block is all zeros
             const uint64_t d = desc_add(d0, (k >> 2) * 16384 + (k & 3) * 32);
             mma_f16(tb + (ui & 1) * 64, d, d, id, k > 0);
         }
@@ -851,6 +853,7 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     const int quarter = warp & 3, half = (warp >> 2) & 1;
     const int vt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int Hv = p.Hv, Hk = p.Hk;
+    const int ksteps = p.dk > 64 ? 8 : 4;  // K = 16 steps of D1 (over dk)
     const int hk = h / (Hv / Hk);
     const int i0 = vt * TV;
     long rtok0;
@@ -952,9 +955,11 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
                     const uint64_t a0 = desc_sw128(smem_u32(st + Cfg::ST_A1), 16, 1024);
                     const uint32_t d1 = (cc & 1) ? (uint32_t)TV : 0u;
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
+                    for (int k = 0; k < 8; ++k) {
+                        if (k >= ksteps) break;  // a head of <= 64 features: its second K-block is all zeros
                         mma_f16(tbase + d1, desc_add(a0, (k >> 2) * 16384 + (k & 3) * 32), desc_add(bS0, k * 2048),
                                 id1, k > 0);
+                    }
                     mma_commit(bar1);
                 }
             }
