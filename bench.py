@@ -285,6 +285,15 @@ def run_ours(args, rank, world, local_rank):
                                           p["chunk"], torch.bfloat16)
     ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    # --flush read: a read-only pass over 512 MiB instead, so that L2 holds only
+    # clean lines when the step starts (for DRAM-traffic captures of one step)
+    flush_r = torch.ones(512 << 20, dtype=torch.uint8, device=dev) if args.flush == "read" else None
+
+    def flush_l2():
+        if flush_r is None:
+            flush.fill_(1)
+        else:
+            flush_r.sum(dtype=torch.int64)
 
     def prefill():
         gdn.gdn_prefill_chunked(gp["q"], gp["k"], gp["v"], gp["alpha"], gp["beta"], B=1,
@@ -305,7 +314,7 @@ def run_ours(args, rank, world, local_rank):
     ev = [[E() for _ in range(n_ev)] for _ in range(args.steps)]
 
     def step(evs=None):
-        flush.fill_(1)
+        flush_l2()
         if evs: evs[0].record(stream)
         if do_pre:
             prefill()
@@ -707,7 +716,7 @@ PREFILL_LAUNCHES = 2  # kernels one gdn_prefill_chunked call launches on this wo
 # kernel changes.
 DECODE_TRAFFIC_BYTES = 541_250_304 + 483_723_776
 VERIFY_TRAFFIC_BYTES = 567_168_768 + 391_290_624
-PREFILL_TRAFFIC_BYTES = (68_728_320 + 21_744_384) + (84_232_192 + 43_203_840)
+PREFILL_TRAFFIC_BYTES = (68_817_664 + 22_300_160) + (86_523_648 + 44_048_896)
 
 
 E2E_GROUPS = 8       # decode e2e: row groups pipelined on their own streams
@@ -1040,6 +1049,9 @@ def main():
     ap.add_argument("--only", choices=["all", "prefill", "decode", "replay", "verify", "batch", "snapshot"],
                     default="all",
                     help="profiling aid: run one phase only (prints timings, not the contract line)")
+    ap.add_argument("--flush", choices=["write", "read"], default="write",
+                    help="profiling aid: L2 flush before each step (read: a read-only pass, "
+                         "no dirty lines for a traffic capture)")
     ap.add_argument("--decode-rows", type=int, default=DEC["B"],
                     help="profiling aid: rows of the decode / replay phases (default 256)")
     args = ap.parse_args()
