@@ -142,3 +142,28 @@ def test_capture_checkpoints_and_conventions(gdn, oracle_mod):
     for r, L in enumerate(LENGTHS):
         for j in range(min(ck_cap, L // 64)):
             assert rel(ck[r, j], cks[r, j]) < tol, (r, j)
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (32, 128)])
+def test_wide_carry_instance(gdn, oracle_mod, dk, dv):
+    """Enough (row, head) tiles that the launcher takes the 64-row carry
+    instance (dv / 32 x Hv x B above the SM count): one 64-row tile per head
+    at dv = 64, two at dv = 128 with a 32-feature key."""
+    from gated_deltanet_recurrence_02_gb300.inputs import make_inputs
+    Hk, Hv = 4, 16
+    lengths = [70, 130, 1, 64, 200, 90, 65, 33]
+    B = len(lengths)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if (dv // 32) * Hv * B <= sms:
+        pytest.skip("the 64-row carry instance needs more (row, head) tiles than SMs")
+    x = make_inputs(3190 + dk + dv, lengths=lengths, Hk=Hk, Hv=Hv, dk=dk, dv=dv, dtype_qkv="bf16",
+                    dtype_gate="f32")
+    g = _dev(x)
+    out, fs = gdn.gdn_prefill_chunked(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=B,
+                                      cu_seqlens=x.cu_seqlens.cuda(), initial_state=x.initial_state.cuda(),
+                                      chunk=64)
+    torch.cuda.synchronize()
+    ro, rS, _ = oracle_mod.recurrent(x.q, x.k, x.v, x.alpha, x.beta, B=B, Hk=Hk, Hv=Hv, dk=dk, dv=dv,
+                                     cu_seqlens=x.cu_seqlens, initial_state=x.initial_state,
+                                     threads=THREADS)
+    _per_row_head(out, fs, ro, rS, x.cu_seqlens.tolist(), Hv, TOL[torch.bfloat16])
