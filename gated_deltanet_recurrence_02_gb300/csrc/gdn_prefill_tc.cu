@@ -790,12 +790,15 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
 // ============================================================ phase B ====
 
 // One carry CTA owns TV rows of one (row, value head) state: TV = 32 (the
-// latency instance: the most CTAs, three stages) or TV = 64 (the throughput
-// instance, for grids of many rows: twice the work per MMA for about the same
-// issue time, two stages).
+// latency instance: the most CTAs, three stages) or TV = 64 / 128 (the
+// throughput instances, for grids of many rows: two and four times the work
+// per MMA for about the same issue time, two stages).  Operand images wider
+// than 64 columns are stored as 64-column blocks (N-blocks of the MN-major
+// 128-byte-swizzled layout, one after the other).
 template <int TV>
 struct CarryCfg {
     static constexpr int kCols = TV / 2;             // state columns per compute thread
+    static constexpr int kGroup = kCols < 32 ? kCols : 32;  // columns a thread handles at a time
     static constexpr int NS = TV == 32 ? 3 : 2;      // stages in the ring
     static constexpr uint32_t ST_A1 = 0;             // [Q ; W] image, 2 K-blocks of 128 rows
     static constexpr uint32_t ST_K = 32768;          // K image, 2 dk blocks of 64 rows
@@ -804,16 +807,23 @@ struct CarryCfg {
     static constexpr uint32_t kUBytes = TV * 128;
     static constexpr uint32_t ST_VEC = ST_U + kUBytes;  // gamma, w, gamma_last
     static constexpr uint32_t ST_BYTES = ST_VEC + 1024;
-    static constexpr uint32_t B_S = NS * ST_BYTES;   // S^T image (MN-major, 128 K-rows, TV N used)
-    static constexpr uint32_t B_DW = B_S + 16384;    // diag(w) Delta image (64 K-rows)
-    static constexpr uint32_t B_DD = B_DW + 8192;    // Delta image
-    static constexpr uint32_t B_BAR = B_DD + 8192;
+    static constexpr uint32_t kNBlocks = TV > 64 ? 2 : 1;  // 64-column blocks of the images
+    static constexpr uint32_t SIMG_BLOCK = 16384;    // S^T image block: 128 K-rows (dk)
+    static constexpr uint32_t DIMG_BLOCK = 8192;     // Delta image block: 64 K-rows (tokens)
+    static constexpr uint32_t B_S = NS * ST_BYTES;   // S^T image (MN-major, TV N used)
+    static constexpr uint32_t B_DW = B_S + kNBlocks * SIMG_BLOCK;  // diag(w) Delta image
+    static constexpr uint32_t B_DD = B_DW + kNBlocks * DIMG_BLOCK;  // Delta image
+    static constexpr uint32_t B_BAR = B_DD + kNBlocks * DIMG_BLOCK;
     static constexpr uint32_t B_SMEM = B_BAR + 128 + 1024;
     static constexpr uint32_t STAGE_TX = 16384 + 16384 + 16384 + 8192 + kUBytes + 1024;
     // TMEM columns: D1 = [Q; W] S^T at 0 / TV (by chunk parity), D2 = K^T w Delta
-    // at 2 TV, D3 = P' Delta at 3 TV / 4 TV (by chunk parity)
+    // at 2 TV, D3 = P' Delta at 3 TV / 4 TV (by chunk parity; one buffer at
+    // TV = 128, where the output warps read D3 of a chunk before they reach
+    // the next chunk's Delta barrier, after which its D3 is issued)
     static constexpr uint32_t T_D2 = 2 * TV, T_D3 = 3 * TV;
+    static constexpr uint32_t T_D3_ODD = TV == 128 ? 0u : (uint32_t)TV;
     static constexpr uint32_t T_COLS = TV == 32 ? 256 : 512;
+    static_assert(T_D3 + T_D3_ODD + TV <= T_COLS, "carry TMEM columns");
     static_assert(B_SMEM <= 232448, "carry CTA exceeds the shared memory of an SM");
 };
 // 8 compute warps: warp w reads TMEM lane quarter w % 4, warps w and w + 4
@@ -831,8 +841,14 @@ constexpr uint32_t kBarState = 2;  // named barrier: S image written (all warps)
 // The calling warp's N consecutive TMEM columns (N = 16 or 32), see tmem_ld16.
 template <int N>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[N]) {
+    static_assert(N == 16 || N == 32, "16 or 32 columns");
     if constexpr (N == 16) tmem_ld16(taddr, v);
     else tmem_ld32(taddr, v);
+}
+// Byte offset of the 16-byte chunk holding columns [c, c + 8) of row r of an
+// operand image stored as 64-column SW128 blocks `block` bytes apart.
+__device__ __forceinline__ uint32_t img_chunk(int r, int c, uint32_t block) {
+    return (uint32_t)(c >> 6) * block + sw128_chunk(r, (c & 63) >> 3);
 }
 
 template <typename E, bool XO, int TV>
@@ -840,7 +856,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
 prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap mq,
                      const __grid_constant__ CUtensorMap mk) {
     using Cfg = CarryCfg<TV>;
-    constexpr int NS = Cfg::NS, NC = Cfg::kCols, Q8 = NC / 8;
+    constexpr int NS = Cfg::NS, NC = Cfg::kCols, Q8 = NC / 8, CG = Cfg::kGroup;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sS = sm + Cfg::B_S, *sDw = sm + Cfg::B_DW, *sDd = sm + Cfg::B_DD;
@@ -942,7 +958,8 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
         const uint32_t id1 = idesc_f16(128, TV, false, true, kbf);
         const uint32_t id2 = idesc_f16(128, TV, true, true, kbf);
         const uint32_t id3 = idesc_f16(128, TV, false, true, kbf);
-        const uint64_t bS0 = desc_sw128(smem_u32(sS), 8192, 1024);
+        // (LBO: the distance between 64-column blocks of an MN-major operand)
+        const uint64_t bS0 = desc_sw128(smem_u32(sS), Cfg::kNBlocks > 1 ? Cfg::SIMG_BLOCK : 8192u, 1024);
         const uint64_t bDw0 = desc_sw128(smem_u32(sDw), 8192, 1024);
         const uint64_t bDd0 = desc_sw128(smem_u32(sDd), 8192, 1024);
         for (int cc = 0; cc < nc; ++cc) {
@@ -970,7 +987,7 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
             if (lane == 0 && ok) {
                 const uint64_t k0 = desc_sw128(smem_u32(st + Cfg::ST_K), 8192, 1024);
                 const uint64_t p0 = desc_sw128(smem_u32(st + Cfg::ST_P), 16, 1024);
-                const uint32_t d3 = Cfg::T_D3 + ((cc & 1) ? (uint32_t)TV : 0u);
+                const uint32_t d3 = Cfg::T_D3 + ((cc & 1) ? Cfg::T_D3_ODD : 0u);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     mma_f16(tbase + Cfg::T_D2, desc_add(k0, k * 2048), desc_add(bDw0, k * 2048), id2, k > 0);
@@ -1004,7 +1021,7 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
         for (int i = 0; i < NC; ++i) S[i] = (s0 && jin) ? s0[(size_t)(i0 + c0 + i) * dk + j] : 0.f;
 #pragma unroll
         for (int q8 = 0; q8 < Q8; ++q8)
-            *reinterpret_cast<uint4 *>(sS + sw128_chunk(j, c0 / 8 + q8)) = pack8<E>(S + 8 * q8);
+            *reinterpret_cast<uint4 *>(sS + img_chunk(j, c0 + 8 * q8, Cfg::SIMG_BLOCK)) = pack8<E>(S + 8 * q8);
         fence_proxy_async();
         grid_dependency_wait();  // global writes below follow the chunk-parallel kernel's
         fence_before_sync();
@@ -1018,7 +1035,7 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
             const int s = cc % NS;
             uint8_t *st = sm + s * Cfg::ST_BYTES;
             const uint32_t d1 = (cc & 1) ? (uint32_t)TV : 0u;
-            const uint32_t d3 = Cfg::T_D3 + ((cc & 1) ? (uint32_t)TV : 0u);
+            const uint32_t d3 = Cfg::T_D3 + ((cc & 1) ? Cfg::T_D3_ODD : 0u);
             const int n = min(C, len - cc * C);
             if (ok) ok = mbar_wait(&full[s], (cc / NS) & 1, p.wait_ns);
             const float *vec = reinterpret_cast<const float *>(st + Cfg::ST_VEC);
@@ -1039,28 +1056,32 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
                 if (ok) ok = mbar_wait(bar1, cc & 1, p.wait_ns);
                 if (ok) {
                     fence_after_sync();
-                    float ws[NC];
-                    tmem_ld_cols<NC>(lane_base + d1 + c0, ws);
                     // captured tokens: Delta's row t is token t's delta
                     float *cap = (cc * C + t < ncap)
                                      ? p.su + ((size_t)b * p.capacity + cc * C + t) * su_slot + Hv +
                                            (size_t)Hk * p.dk + (size_t)h * p.dv + i0 + c0
                                      : nullptr;
 #pragma unroll
-                    for (int q8 = 0; q8 < Q8; ++q8) {
-                        const int c = c0 + 8 * q8;
-                        float u[8], dd[8], dw[8];
-                        unpack8<E>(uraw[q8], u);
+                    for (int gq = 0; gq < NC / CG; ++gq) {
+                        float ws[CG];
+                        tmem_ld_cols<CG>(lane_base + d1 + c0 + gq * CG, ws);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            dd[e] = u[e] - ws[8 * q8 + e];
-                            dw[e] = wt * dd[e];
+                        for (int q8 = 0; q8 < CG / 8; ++q8) {
+                            const int qq = gq * (CG / 8) + q8;
+                            const int c = c0 + 8 * qq;
+                            float u[8], dd[8], dw[8];
+                            unpack8<E>(uraw[qq], u);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                dd[e] = u[e] - ws[8 * q8 + e];
+                                dw[e] = wt * dd[e];
+                            }
+                            *reinterpret_cast<uint4 *>(sDd + img_chunk(t, c, Cfg::DIMG_BLOCK)) = pack8<E>(dd);
+                            *reinterpret_cast<uint4 *>(sDw + img_chunk(t, c, Cfg::DIMG_BLOCK)) = pack8<E>(dw);
+                            if (cap != nullptr)
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) cap[8 * qq + e] = dd[e];
                         }
-                        *reinterpret_cast<uint4 *>(sDd + sw128_chunk(t, c >> 3)) = pack8<E>(dd);
-                        *reinterpret_cast<uint4 *>(sDw + sw128_chunk(t, c >> 3)) = pack8<E>(dw);
-                        if (cap != nullptr)
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) cap[8 * q8 + e] = dd[e];
                     }
                     fence_proxy_async();
                 }
@@ -1073,13 +1094,16 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
             if (ok) ok = mbar_wait(bar2, cc & 1, p.wait_ns);
             if (ok) {
                 fence_after_sync();
-                float v[NC];
-                tmem_ld_cols<NC>(lane_base + Cfg::T_D2 + c0, v);
 #pragma unroll
-                for (int i = 0; i < NC; ++i) S[i] = fmaf(gC, S[i], v[i]);
+                for (int gq = 0; gq < NC / CG; ++gq) {
+                    float v[CG];
+                    tmem_ld_cols<CG>(lane_base + Cfg::T_D2 + c0 + gq * CG, v);
+#pragma unroll
+                    for (int i = 0; i < CG; ++i) S[gq * CG + i] = fmaf(gC, S[gq * CG + i], v[i]);
+                }
 #pragma unroll
                 for (int q8 = 0; q8 < Q8; ++q8)
-                    *reinterpret_cast<uint4 *>(sS + sw128_chunk(j, c0 / 8 + q8)) = pack8<E>(S + 8 * q8);
+                    *reinterpret_cast<uint4 *>(sS + img_chunk(j, c0 + 8 * q8, Cfg::SIMG_BLOCK)) = pack8<E>(S + 8 * q8);
                 fence_proxy_async();
                 if constexpr (XO) {
                     // chunk-boundary checkpoint: the fp32 state after this chunk
@@ -1100,17 +1124,20 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
                 ok = mbar_wait(bar3, cc & 1, p.wait_ns);
                 if (ok) {
                     fence_after_sync();
-                    float qs[NC], pd[NC];
-                    tmem_ld_cols<NC>(lane_base + d1 + c0, qs);
-                    tmem_ld_cols<NC>(lane_base + d3 + c0, pd);
-                    if (t < n) {
-                        E *dst = ob + ((rtok0 + (long)cc * C + t) * Hv + h) * (long)dv + i0 + c0;
+                    E *dst = ob + ((rtok0 + (long)cc * C + t) * Hv + h) * (long)dv + i0 + c0;
 #pragma unroll
-                        for (int q8 = 0; q8 < Q8; ++q8) {
-                            float o[8];
+                    for (int gq = 0; gq < NC / CG; ++gq) {
+                        float qs[CG], pd[CG];
+                        tmem_ld_cols<CG>(lane_base + d1 + c0 + gq * CG, qs);
+                        tmem_ld_cols<CG>(lane_base + d3 + c0 + gq * CG, pd);
+                        if (t < n) {
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) o[e] = fmaf(gt, qs[8 * q8 + e], pd[8 * q8 + e]);
-                            *reinterpret_cast<uint4 *>(dst + 8 * q8) = pack8<E>(o);
+                            for (int q8 = 0; q8 < CG / 8; ++q8) {
+                                float o[8];
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) o[e] = fmaf(gt, qs[8 * q8 + e], pd[8 * q8 + e]);
+                                *reinterpret_cast<uint4 *>(dst + gq * CG + 8 * q8) = pack8<E>(o);
+                            }
                         }
                     }
                 }
@@ -1132,6 +1159,9 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
 }
 
 // ============================================================== host =====
+
+// Rows of the carry tiles for grids of many rows (64 or 128).
+constexpr int kWideRows = 128;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
@@ -1185,10 +1215,13 @@ cudaError_t launch_e(const PrefillParams &p, long total_T, long max_chunks, cuda
                          : set_smem_once<prefill_intra_kernel<E, XO, false>>((int)A_SMEM);
     if (e != cudaSuccess) return e;
     // carry instance: 32-row tiles while one wave of them fits the GPU (the
-    // chain's latency decides), 64-row tiles for more rows (throughput decides)
-    const bool wide = p.dv >= 64 && (long)(p.dv / 32) * p.Hv * p.B > (long)sm_count_of_current_device();
-    e = wide ? set_smem_once<prefill_carry_kernel<E, XO, 64>>((int)CarryCfg<64>::B_SMEM)
-             : set_smem_once<prefill_carry_kernel<E, XO, 32>>((int)CarryCfg<32>::B_SMEM);
+    // chain's latency decides), wider tiles for more rows (throughput decides)
+    int tv = 32;
+    if ((long)(p.dv / 32) * p.Hv * p.B > (long)sm_count_of_current_device() && p.dv >= 64)
+        tv = p.dv >= kWideRows ? kWideRows : 64;
+    e = tv == 32 ? set_smem_once<prefill_carry_kernel<E, XO, 32>>((int)CarryCfg<32>::B_SMEM)
+        : tv == 64 ? set_smem_once<prefill_carry_kernel<E, XO, 64>>((int)CarryCfg<64>::B_SMEM)
+                   : set_smem_once<prefill_carry_kernel<E, XO, 128>>((int)CarryCfg<128>::B_SMEM);
     if (e != cudaSuccess) return e;
     if (max_chunks > 0) {
         // persistent: at most two CTAs per SM walk the (chunk, value head) units
@@ -1203,17 +1236,18 @@ cudaError_t launch_e(const PrefillParams &p, long total_T, long max_chunks, cuda
     // its prologue (barriers, TMEM, the initial state) overlaps that kernel's
     // tail, and it waits for that kernel's records before reading them.
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.dv / (wide ? 64 : 32), p.Hv, p.B);
+    cfg.gridDim = dim3(p.dv / tv, p.Hv, p.B);
     cfg.blockDim = dim3(kCarryThreads);
-    cfg.dynamicSmemBytes = wide ? CarryCfg<64>::B_SMEM : CarryCfg<32>::B_SMEM;
+    cfg.dynamicSmemBytes = tv == 32 ? CarryCfg<32>::B_SMEM : tv == 64 ? CarryCfg<64>::B_SMEM : CarryCfg<128>::B_SMEM;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = max_chunks > 0 ? 1 : 0;
-    return wide ? cudaLaunchKernelEx(&cfg, prefill_carry_kernel<E, XO, 64>, p, mq, mk)
-                : cudaLaunchKernelEx(&cfg, prefill_carry_kernel<E, XO, 32>, p, mq, mk);
+    if (tv == 32) return cudaLaunchKernelEx(&cfg, prefill_carry_kernel<E, XO, 32>, p, mq, mk);
+    if (tv == 64) return cudaLaunchKernelEx(&cfg, prefill_carry_kernel<E, XO, 64>, p, mq, mk);
+    return cudaLaunchKernelEx(&cfg, prefill_carry_kernel<E, XO, 128>, p, mq, mk);
 }
 
 long max_chunks_of(int B, int T, bool varlen) {

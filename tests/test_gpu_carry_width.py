@@ -1,10 +1,11 @@
-"""GPU parity of the tensor-core prefill's 64-row carry tiles.
+"""GPU parity of the tensor-core prefill's wide carry tiles.
 
 The carry phase runs on 32-row state tiles while one wave of them fits the
-GPU and on 64-row tiles for more (row, value head) pairs.  These cases have
-4 Hv B > the SM count, so every call below takes the 64-row instance: plain,
-with capture, with checkpoints and with the in-kernel input conventions,
-against the fp64 oracle.
+GPU and on 128-row tiles (64-row ones when dv = 64) for more (row, value
+head) pairs.  These cases have 4 Hv B > the SM count, so every call below
+takes a wide instance (128 rows at d = 128): plain, with capture, with
+checkpoints and with the in-kernel input conventions, against the fp64
+oracle.
 
 Sources: the chunked form of the gated delta rule (the prefill path of
 "Enable the native Kev example on NVIDIA GPUs through ExecuTorch's AOTI CUDA
