@@ -27,11 +27,11 @@
 // bulk-stored to the workspace with gamma / w.
 //
 // Phase B (prefill_carry_kernel, one CTA per (value head, 32-row dv tile,
-// row), serial over chunks; a 64-row-tile instance with a two-stage ring
-// takes over when the 32-row grid is larger than the SM count, where
-// throughput rather than the chain's latency decides; it is launched as a
-// programmatic dependent of phase A): per chunk two dependent tensor-core
-// steps,
+// row), serial over chunks; 128-row-tile (64-row at dv = 64) instances with a
+// two-stage ring take over when the 32-row grid is larger than the SM count,
+// where throughput rather than the chain's latency decides; it is launched
+// as a programmatic dependent of phase A): per chunk two dependent
+// tensor-core steps,
 //   D1 = [Q; W] S^T                       (M=128: Q S^T and W S^T at once)
 //   Delta = U - (W S^T)                   (threads, fp32)
 //   D2 = K^T diag(w) Delta,  D3 = P' Delta (tensor cores)
