@@ -86,33 +86,66 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(const Prefill
         *reinterpret_cast<float4 *>(Ss + i * KS + j) = x;
     }
 
+    // The next chunk's k, q, v and gates are loaded into registers while the
+    // current chunk is computed, and written to shared memory at the start of
+    // the next iteration (identity tokens past the row's end).
+    constexpr int NKQ = (C * DK / 4 + kThreads - 1) / kThreads;  // float4 of k (and of q) per thread
+    constexpr int NV = (C * kDVT + kThreads - 1) / kThreads;      // v elements per thread
+    float4 kr[NKQ], qr[NKQ];
+    float vr[NV], ga = 1.f, gb = 0.f;
+    auto load_chunk = [&](int cs) {
+        const int nn = (Tb - cs < C) ? (Tb - cs) : C;
+#pragma unroll
+        for (int u = 0; u < NKQ; ++u) {
+            const int e = tid + u * kThreads, t = e / (DK / 4), j = (e % (DK / 4)) * 4;
+            kr[u] = qr[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (e < C * DK / 4 && t < nn) {
+                const long off = ((tok0 + cs + t) * Hk + hk) * DK + j;
+                kr[u] = ld4(kb + off);
+                qr[u] = ld4(qb + off);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < NV; ++u) {
+            const int e = tid + u * kThreads, t = e / kDVT, i = e % kDVT;
+            vr[u] = (e < C * kDVT && t < nn) ? ld_f(vb + ((tok0 + cs + t) * Hv + h) * (long)dv + row0 + i) : 0.f;
+        }
+        ga = 1.f;
+        gb = 0.f;
+        if (tid < nn) {
+            const long g = (tok0 + cs + tid) * Hv + h;
+            ga = ld_gate(p.alpha, g, p.dt_gate);
+            gb = ld_gate(p.beta, g, p.dt_gate);
+        }
+    };
+    if (Tb > 0) load_chunk(0);
+
     for (int c0 = 0; c0 < Tb; c0 += C) {
         const int n = (Tb - c0 < C) ? (Tb - c0) : C;
         // ---- 1. stage the chunk (identity tokens past n) -------------------
-        for (int e = tid; e < C * DK / 4; e += kThreads) {
-            const int t = e / (DK / 4), j = (e % (DK / 4)) * 4;
-            float4 kk = make_float4(0.f, 0.f, 0.f, 0.f), qq = kk;
-            if (t < n) {
-                const long off = ((tok0 + c0 + t) * Hk + hk) * DK + j;
-                kk = ld4(kb + off);
-                qq = ld4(qb + off);
+#pragma unroll
+        for (int u = 0; u < NKQ; ++u) {
+            const int e = tid + u * kThreads, t = e / (DK / 4), j = (e % (DK / 4)) * 4;
+            if (e < C * DK / 4) {
+                float4 qq = qr[u];
                 if (!(p.conv & GDN_QK_L2NORM)) {
                     qq.x *= scale; qq.y *= scale; qq.z *= scale; qq.w *= scale;
                 }
+                *reinterpret_cast<float4 *>(Ks + t * KS + j) = kr[u];
+                *reinterpret_cast<float4 *>(Qs + t * KS + j) = qq;
             }
-            *reinterpret_cast<float4 *>(Ks + t * KS + j) = kk;
-            *reinterpret_cast<float4 *>(Qs + t * KS + j) = qq;
         }
-        for (int e = tid; e < C * kDVT; e += kThreads) {
-            const int t = e / kDVT, i = e % kDVT;
-            Vs[t * DS + i] = (t < n) ? ld_f(vb + ((tok0 + c0 + t) * Hv + h) * (long)dv + row0 + i) : 0.f;
+#pragma unroll
+        for (int u = 0; u < NV; ++u) {
+            const int e = tid + u * kThreads, t = e / kDVT, i = e % kDVT;
+            if (e < C * kDVT) Vs[t * DS + i] = vr[u];
         }
-        for (int t = tid; t < C; t += kThreads) {
-            const long g = (tok0 + c0 + t) * Hv + h;
-            lg[t] = (t < n) ? conv_log_alpha(ld_gate(p.alpha, g, p.dt_gate), p.conv) : 0.f;
-            bt[t] = (t < n) ? conv_beta(ld_gate(p.beta, g, p.dt_gate), p.conv) : 0.f;
+        if (tid < C) {
+            lg[tid] = (tid < n) ? conv_log_alpha(ga, p.conv) : 0.f;
+            bt[tid] = (tid < n) ? conv_beta(gb, p.conv) : 0.f;
         }
         __syncthreads();
+        if (c0 + C < Tb) load_chunk(c0 + C);  // in flight while this chunk is computed
         if (p.conv & GDN_QK_L2NORM) {
             // q and k normalised in the kernel, one warp per row; q then scaled
             for (int r = warp; r < 2 * C; r += kThreads / 32) {
@@ -243,13 +276,32 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(const Prefill
             }
         }
 
-        // ---- 5a. outputs O = Os + P Delta -----------------------------------
-        for (int e = tid; e < C * kDVT; e += kThreads) {
-            const int t = e / kDVT, i = e % kDVT;
-            if (t < n) {
-                float acc = Os[t * DS + i];
-                for (int s = 0; s <= t; ++s) acc += Ps[t * AS + s] * Vs[s * DS + i];
-                st_out(ob + ((tok0 + c0 + t) * Hv + h) * (long)dv + row0 + i, acc);
+        // ---- 5a. outputs O = Os + P Delta: 2 tokens x 4 columns per thread ---
+        for (int blk = tid; blk < (C / 2) * (kDVT / 4); blk += kThreads) {
+            const int t0 = (blk / (kDVT / 4)) * 2, i0 = (blk % (kDVT / 4)) * 4;
+            float4 acc[2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) acc[r] = *reinterpret_cast<const float4 *>(Os + (t0 + r) * DS + i0);
+            for (int s = 0; s <= t0 + 1; ++s) {  // P[t][s] = 0 for s > t
+                const float4 d = *reinterpret_cast<const float4 *>(Vs + s * DS + i0);
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const float pr = Ps[(t0 + r) * AS + s];
+                    acc[r].x += pr * d.x;
+                    acc[r].y += pr * d.y;
+                    acc[r].z += pr * d.z;
+                    acc[r].w += pr * d.w;
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                if (t0 + r < n) {
+                    TQ *o = ob + ((tok0 + c0 + t0 + r) * Hv + h) * (long)dv + row0 + i0;
+                    st_out(o, acc[r].x);
+                    st_out(o + 1, acc[r].y);
+                    st_out(o + 2, acc[r].z);
+                    st_out(o + 3, acc[r].w);
+                }
             }
         }
         // ---- 5b. S <- e^{g_last} S + Delta^T diag(e^{g_last - g}) K ----------
