@@ -32,6 +32,61 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kDVT = 32;  // state rows per CTA
 
+// fp32 products on the warp-level tensor cores at fp32 accuracy: each operand
+// x is split into two tf32 parts x = big + small (big = x rounded to tf32,
+// small = the rest rounded to tf32), and a b is taken as
+// a_small b_big + a_big b_small + a_big b_big, dropping a_small b_small
+// (relative size ~2^-22); products accumulate in fp32.
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void split_tf32(float x, uint32_t &big, uint32_t &small) {
+    big = to_tf32(x);
+    small = to_tf32(x - __uint_as_float(big));
+}
+// m16n8k8, tf32 inputs, fp32 accumulate.  Fragments (g = lane / 4, t = lane % 4):
+// A a0 = (g, t), a1 = (g + 8, t), a2 = (g, t + 4), a3 = (g + 8, t + 4);
+// B b0 = (k = t, n = g), b1 = (k = t + 4, n = g);
+// C c0, c1 = (g, 2t), (g, 2t + 1); c2, c3 = (g + 8, 2t), (g + 8, 2t + 1).
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+struct SplitA {
+    uint32_t big[4], small[4];
+};
+struct SplitB {
+    uint32_t big[2], small[2];
+};
+__device__ __forceinline__ void mma_3xtf32(float (&d)[4], const SplitA &a, const SplitB &b) {
+    mma_tf32(d, a.small, b.big[0], b.big[1]);
+    mma_tf32(d, a.big, b.small[0], b.small[1]);
+    mma_tf32(d, a.big, b.big[0], b.big[1]);
+}
+// A fragment of rows r0 .. r0 + 15, columns k0 .. k0 + 7 of a row-major fp32
+// matrix with row stride `ld` (floats).
+__device__ __forceinline__ SplitA load_a(const float *m, int ld, int r0, int k0, int g, int t) {
+    SplitA a;
+    split_tf32(m[(r0 + g) * ld + k0 + t], a.big[0], a.small[0]);
+    split_tf32(m[(r0 + g + 8) * ld + k0 + t], a.big[1], a.small[1]);
+    split_tf32(m[(r0 + g) * ld + k0 + t + 4], a.big[2], a.small[2]);
+    split_tf32(m[(r0 + g + 8) * ld + k0 + t + 4], a.big[3], a.small[3]);
+    return a;
+}
+// B fragment (k = k0 .. k0 + 7, n = n0 .. n0 + 7) of B = M^T for a row-major
+// M with rows n and row stride `ld`: B[k][n] = M[n][k].
+__device__ __forceinline__ SplitB load_bt(const float *m, int ld, int n0, int k0, int g, int t) {
+    SplitB b;
+    split_tf32(m[(n0 + g) * ld + k0 + t], b.big[0], b.small[0]);
+    split_tf32(m[(n0 + g) * ld + k0 + t + 4], b.big[1], b.small[1]);
+    return b;
+}
+
 template <int DK, int C>
 struct SimtSmem {
     static constexpr int KS = DK + 4;   // row stride of S, K, Q
@@ -177,69 +232,45 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(const Prefill
         }
         __syncthreads();
 
-        // ---- 3a. A and P, 4x4 register blocks -------------------------------
-        constexpr int NB = C / 4;
-        for (int blk = tid; blk < NB * NB; blk += kThreads) {
-            const int t0 = (blk / NB) * 4, i0 = (blk % NB) * 4;
-            float kk[4][4] = {}, qk[4][4] = {};
-            if (i0 <= t0 + 3) {
-                for (int j = 0; j < DK; j += 4) {
-                    float4 kt[4], qt[4], ki[4];
+        // ---- 3. [K; Q] [K^T | S^T] on the warp-level tensor cores (3 x tf32):
+        // warp w < C / 8 takes rows 16w .. 16w + 15 of [K; Q] (K rows, then Q
+        // rows); its fragments give A or P (decay and mask applied) and R (in
+        // place over V) or the readout from the chunk's start state.
+        if (warp < C / 8) {
+            const int g = lane >> 2, t4 = lane & 3;
+            const bool krows = 16 * warp < C;
+            const int r0 = krows ? 16 * warp : 16 * warp - C;  // first row within K or Q
+            const float *M = krows ? Ks : Qs;
+            constexpr int NA = C / 8, NS8 = kDVT / 8;  // n-tiles of K^T and of S^T
+            float acc[NA + NS8][4];
 #pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        kt[r] = *reinterpret_cast<const float4 *>(Ks + (t0 + r) * KS + j);
-                        qt[r] = *reinterpret_cast<const float4 *>(Qs + (t0 + r) * KS + j);
-                        ki[r] = *reinterpret_cast<const float4 *>(Ks + (i0 + r) * KS + j);
-                    }
+            for (int n = 0; n < NA + NS8; ++n)
 #pragma unroll
-                    for (int r = 0; r < 4; ++r)
+                for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
+            for (int k0 = 0; k0 < DK; k0 += 8) {
+                const SplitA a = load_a(M, KS, r0, k0, g, t4);
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            kk[r][c] += kt[r].x * ki[c].x + kt[r].y * ki[c].y + kt[r].z * ki[c].z + kt[r].w * ki[c].w;
-                            qk[r][c] += qt[r].x * ki[c].x + qt[r].y * ki[c].y + qt[r].z * ki[c].z + qt[r].w * ki[c].w;
-                        }
-                }
+                for (int n = 0; n < NA; ++n) mma_3xtf32(acc[n], a, load_bt(Ks, KS, 8 * n, k0, g, t4));
+#pragma unroll
+                for (int n = 0; n < NS8; ++n) mma_3xtf32(acc[NA + n], a, load_bt(Ss, KS, 8 * n, k0, g, t4));
             }
+            // element e of a fragment: row r0 + g + 8 (e / 2), column 8 n + 2 t4 + e % 2
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
+            for (int n = 0; n < NA; ++n)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int t = t0 + r, i = i0 + c;
+                for (int e = 0; e < 4; ++e) {
+                    const int t = r0 + g + 8 * (e >> 1), i = 8 * n + 2 * t4 + (e & 1);
                     const float decay = (i <= t) ? expf(lg[t] - lg[i]) : 0.f;
-                    As[t * AS + i] = (i < t) ? bt[t] * decay * kk[r][c] : 0.f;
-                    Ps[t * AS + i] = (i <= t) ? decay * qk[r][c] : 0.f;
-                }
-        }
-
-        // ---- 3b. R (in place over V) and the inter-chunk readout ------------
-        constexpr int NB2 = (C / 4) * (kDVT / 4);
-        for (int w = tid; w < 2 * NB2; w += kThreads) {
-            const int kind = w / NB2, blk = w % NB2;
-            const int t0 = (blk / (kDVT / 4)) * 4, i0 = (blk % (kDVT / 4)) * 4;
-            const float *src = kind == 0 ? Ks : Qs;
-            float acc[4][4] = {};
-            for (int j = 0; j < DK; j += 4) {
-                float4 x[4], s[4];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    x[r] = *reinterpret_cast<const float4 *>(src + (t0 + r) * KS + j);
-                    s[r] = *reinterpret_cast<const float4 *>(Ss + (i0 + r) * KS + j);
+                    if (krows) As[t * AS + i] = (i < t) ? bt[t] * decay * acc[n][e] : 0.f;
+                    else Ps[t * AS + i] = (i <= t) ? decay * acc[n][e] : 0.f;
                 }
 #pragma unroll
-                for (int r = 0; r < 4; ++r)
+            for (int n = 0; n < NS8; ++n)
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        acc[r][c] += x[r].x * s[c].x + x[r].y * s[c].y + x[r].z * s[c].z + x[r].w * s[c].w;
-            }
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int t = t0 + r, i = i0 + c;
-                    if (kind == 0)
-                        Vs[t * DS + i] = bt[t] * (Vs[t * DS + i] - eg[t] * acc[r][c]);
-                    else
-                        Os[t * DS + i] = eg[t] * acc[r][c];
+                for (int e = 0; e < 4; ++e) {
+                    const int t = r0 + g + 8 * (e >> 1), i = 8 * n + 2 * t4 + (e & 1);
+                    if (krows) Vs[t * DS + i] = bt[t] * (Vs[t * DS + i] - eg[t] * acc[NA + n][e]);
+                    else Os[t * DS + i] = eg[t] * acc[NA + n][e];
                 }
         }
         __syncthreads();
@@ -304,33 +335,34 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(const Prefill
                 }
             }
         }
-        // ---- 5b. S <- e^{g_last} S + Delta^T diag(e^{g_last - g}) K ----------
+        // ---- 5b. S <- e^{g_last} S + Delta^T diag(e^{g_last - g}) K (3 x tf32):
+        // the 32 x DK state as 2 x DK / 8 fragment tiles, DK / 32 per warp
         {
+            const int g = lane >> 2, t4 = lane & 3;
             const float glast = eg[C - 1];
-            for (int blk = tid; blk < kDVT * DK / 16; blk += kThreads) {
-                const int i0 = (blk / (DK / 4)) * 4, j0 = (blk % (DK / 4)) * 4;
-                float4 acc[4];
+            constexpr int NP = DK / 32;
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    float4 s = *reinterpret_cast<const float4 *>(Ss + (i0 + r) * KS + j0);
-                    acc[r] = make_float4(glast * s.x, glast * s.y, glast * s.z, glast * s.w);
-                }
-                for (int s = 0; s < C; ++s) {
-                    const float4 d = *reinterpret_cast<const float4 *>(Vs + s * DS + i0);
-                    const float4 kk = *reinterpret_cast<const float4 *>(Ks + s * KS + j0);
-                    const float w = wg[s];
-                    const float dd[4] = {w * d.x, w * d.y, w * d.z, w * d.w};
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        acc[r].x += dd[r] * kk.x;
-                        acc[r].y += dd[r] * kk.y;
-                        acc[r].z += dd[r] * kk.z;
-                        acc[r].w += dd[r] * kk.w;
-                    }
+            for (int pi = 0; pi < NP; ++pi) {
+                const int pair = warp * NP + pi;
+                const int m = pair / (DK / 8), n = pair % (DK / 8);  // state rows 16 m .., columns 8 n ..
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int k0 = 0; k0 < C; k0 += 8) {
+                    // A = (diag(w) Delta)^T: A[i][s] = w_s Delta[s][i]; B = K: B[s][j] = K[s][j]
+                    SplitA a;
+                    split_tf32(wg[k0 + t4] * Vs[(k0 + t4) * DS + 16 * m + g], a.big[0], a.small[0]);
+                    split_tf32(wg[k0 + t4] * Vs[(k0 + t4) * DS + 16 * m + g + 8], a.big[1], a.small[1]);
+                    split_tf32(wg[k0 + t4 + 4] * Vs[(k0 + t4 + 4) * DS + 16 * m + g], a.big[2], a.small[2]);
+                    split_tf32(wg[k0 + t4 + 4] * Vs[(k0 + t4 + 4) * DS + 16 * m + g + 8], a.big[3], a.small[3]);
+                    SplitB bk;
+                    split_tf32(Ks[(k0 + t4) * KS + 8 * n + g], bk.big[0], bk.small[0]);
+                    split_tf32(Ks[(k0 + t4 + 4) * KS + 8 * n + g], bk.big[1], bk.small[1]);
+                    mma_3xtf32(acc, a, bk);
                 }
 #pragma unroll
-                for (int r = 0; r < 4; ++r)
-                    *reinterpret_cast<float4 *>(Ss + (i0 + r) * KS + j0) = acc[r];
+                for (int e = 0; e < 4; ++e) {
+                    float *sp = Ss + (16 * m + g + 8 * (e >> 1)) * KS + 8 * n + 2 * t4 + (e & 1);
+                    *sp = fmaf(glast, *sp, acc[e]);
+                }
             }
         }
         __syncthreads();
