@@ -63,10 +63,16 @@ struct SplitA {
 struct SplitB {
     uint32_t big[2], small[2];
 };
-__device__ __forceinline__ void mma_3xtf32(float (&d)[4], const SplitA &a, const SplitB &b) {
-    mma_tf32(d, a.small, b.big[0], b.big[1]);
-    mma_tf32(d, a.big, b.small[0], b.small[1]);
-    mma_tf32(d, a.big, b.big[0], b.big[1]);
+// d[n] += a b[n] for N fragments, each of the three terms issued for all N
+// before the next (consecutive MMAs then go to different accumulators)
+template <int N>
+__device__ __forceinline__ void mma_3xtf32_n(float (&d)[N][4], const SplitA &a, const SplitB (&b)[N]) {
+#pragma unroll
+    for (int n = 0; n < N; ++n) mma_tf32(d[n], a.small, b[n].big[0], b[n].big[1]);
+#pragma unroll
+    for (int n = 0; n < N; ++n) mma_tf32(d[n], a.big, b[n].small[0], b[n].small[1]);
+#pragma unroll
+    for (int n = 0; n < N; ++n) mma_tf32(d[n], a.big, b[n].big[0], b[n].big[1]);
 }
 // A fragment of rows r0 .. r0 + 15, columns k0 .. k0 + 7 of a row-major fp32
 // matrix with row stride `ld` (floats).
@@ -249,10 +255,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(const Prefill
                 for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
             for (int k0 = 0; k0 < DK; k0 += 8) {
                 const SplitA a = load_a(M, KS, r0, k0, g, t4);
+                SplitB bf[NA + NS8];
 #pragma unroll
-                for (int n = 0; n < NA; ++n) mma_3xtf32(acc[n], a, load_bt(Ks, KS, 8 * n, k0, g, t4));
+                for (int n = 0; n < NA; ++n) bf[n] = load_bt(Ks, KS, 8 * n, k0, g, t4);
 #pragma unroll
-                for (int n = 0; n < NS8; ++n) mma_3xtf32(acc[NA + n], a, load_bt(Ss, KS, 8 * n, k0, g, t4));
+                for (int n = 0; n < NS8; ++n) bf[NA + n] = load_bt(Ss, KS, 8 * n, k0, g, t4);
+                mma_3xtf32_n<NA + NS8>(acc, a, bf);
             }
             // element e of a fragment: row r0 + g + 8 (e / 2), column 8 n + 2 t4 + e % 2
 #pragma unroll
@@ -275,16 +283,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(const Prefill
         }
         __syncthreads();
 
-        // ---- 4. Delta = (I + A)^{-1} R: warp w owns columns 4w .. 4w+3 ------
+        // ---- 4. Delta = (I + A)^{-1} R by forward substitution in registers:
+        // warp w owns columns 4w .. 4w+3, lane 8 ci + rg rows rg, rg + 8, ... of
+        // column 4w + ci.  Row s is final once the rows above it have been
+        // folded in; its owner broadcasts it to the column's 8 lanes, which
+        // subtract A[t][s] x_s from their rows (A[t][s] = 0 for t <= s).
         {
-            const int part = lane & 7, i = warp * 4 + (lane >> 3);
-            for (int t = 0; t < C; ++t) {
-                float acc = 0.f;
-                for (int s = part; s < t; s += 8) acc += As[t * AS + s] * Vs[s * DS + i];
-                acc = group_sum<8>(acc);
-                if (part == 0) Vs[t * DS + i] -= acc;
-                __syncwarp();
+            constexpr int RPL = C / 8;  // rows per lane
+            const int rg = lane & 7, i = warp * 4 + (lane >> 3);
+            float x[RPL];
+#pragma unroll
+            for (int k = 0; k < RPL; ++k) x[k] = Vs[(rg + 8 * k) * DS + i];
+#pragma unroll
+            for (int s = 0; s < C - 1; ++s) {
+                const float xs = __shfl_sync(0xffffffffu, x[s >> 3], (lane & ~7) | (s & 7));
+#pragma unroll
+                for (int k = s >> 3; k < RPL; ++k) x[k] = fmaf(-As[(rg + 8 * k) * AS + s], xs, x[k]);
             }
+#pragma unroll
+            for (int k = 0; k < RPL; ++k) Vs[(rg + 8 * k) * DS + i] = x[k];
         }
         __syncthreads();
 
@@ -340,30 +357,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(const Prefill
         {
             const int g = lane >> 2, t4 = lane & 3;
             const float glast = eg[C - 1];
+            // warp w: state rows 16 m .. (m = w / 4), columns 8 n .. for its NP n-tiles
             constexpr int NP = DK / 32;
+            const int m = warp >> 2, nb = (warp & 3) * NP;
+            float acc[NP][4];
 #pragma unroll
-            for (int pi = 0; pi < NP; ++pi) {
-                const int pair = warp * NP + pi;
-                const int m = pair / (DK / 8), n = pair % (DK / 8);  // state rows 16 m .., columns 8 n ..
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int k0 = 0; k0 < C; k0 += 8) {
-                    // A = (diag(w) Delta)^T: A[i][s] = w_s Delta[s][i]; B = K: B[s][j] = K[s][j]
-                    SplitA a;
-                    split_tf32(wg[k0 + t4] * Vs[(k0 + t4) * DS + 16 * m + g], a.big[0], a.small[0]);
-                    split_tf32(wg[k0 + t4] * Vs[(k0 + t4) * DS + 16 * m + g + 8], a.big[1], a.small[1]);
-                    split_tf32(wg[k0 + t4 + 4] * Vs[(k0 + t4 + 4) * DS + 16 * m + g], a.big[2], a.small[2]);
-                    split_tf32(wg[k0 + t4 + 4] * Vs[(k0 + t4 + 4) * DS + 16 * m + g + 8], a.big[3], a.small[3]);
-                    SplitB bk;
-                    split_tf32(Ks[(k0 + t4) * KS + 8 * n + g], bk.big[0], bk.small[0]);
-                    split_tf32(Ks[(k0 + t4 + 4) * KS + 8 * n + g], bk.big[1], bk.small[1]);
-                    mma_3xtf32(acc, a, bk);
+            for (int pi = 0; pi < NP; ++pi)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[pi][e] = 0.f;
+            for (int k0 = 0; k0 < C; k0 += 8) {
+                // A = (diag(w) Delta)^T: A[i][s] = w_s Delta[s][i]; B = K: B[s][j] = K[s][j]
+                SplitA a;
+                split_tf32(wg[k0 + t4] * Vs[(k0 + t4) * DS + 16 * m + g], a.big[0], a.small[0]);
+                split_tf32(wg[k0 + t4] * Vs[(k0 + t4) * DS + 16 * m + g + 8], a.big[1], a.small[1]);
+                split_tf32(wg[k0 + t4 + 4] * Vs[(k0 + t4 + 4) * DS + 16 * m + g], a.big[2], a.small[2]);
+                split_tf32(wg[k0 + t4 + 4] * Vs[(k0 + t4 + 4) * DS + 16 * m + g + 8], a.big[3], a.small[3]);
+                SplitB bk[NP];
+#pragma unroll
+                for (int pi = 0; pi < NP; ++pi) {
+                    split_tf32(Ks[(k0 + t4) * KS + 8 * (nb + pi) + g], bk[pi].big[0], bk[pi].small[0]);
+                    split_tf32(Ks[(k0 + t4 + 4) * KS + 8 * (nb + pi) + g], bk[pi].big[1], bk[pi].small[1]);
                 }
+                mma_3xtf32_n<NP>(acc, a, bk);
+            }
+#pragma unroll
+            for (int pi = 0; pi < NP; ++pi)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    float *sp = Ss + (16 * m + g + 8 * (e >> 1)) * KS + 8 * n + 2 * t4 + (e & 1);
-                    *sp = fmaf(glast, *sp, acc[e]);
+                    float *sp = Ss + (16 * m + g + 8 * (e >> 1)) * KS + 8 * (nb + pi) + 2 * t4 + (e & 1);
+                    *sp = fmaf(glast, *sp, acc[pi][e]);
                 }
-            }
         }
         __syncthreads();
         // ---- 6. chunk-boundary checkpoint ------------------------------------
