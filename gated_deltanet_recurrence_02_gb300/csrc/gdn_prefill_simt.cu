@@ -1,4 +1,7 @@
-// gdn_prefill_simt.cu -- chunked prefill on CUDA cores, fp32 throughout.
+// gdn_prefill_simt.cu -- chunked prefill for the general shapes, fp32
+// arithmetic throughout: CUDA cores, with the two large products on the
+// warp-level tensor cores at fp32 accuracy (each operand split into two tf32
+// parts, three products).
 //
 // "Enable the native Kev example on NVIDIA GPUs through ExecuTorch's AOTI CUDA
 // backend" (executorch issue 23097), work list: chunked GDN prefill with an
