@@ -468,3 +468,35 @@ def test_many_packed_rows_tensor_core_prefill(gdn, oracle_mod):
           f"state {e_s:.2e} at {at_s}")
     empty = [b for b, L in enumerate(lengths) if L == 0]
     assert empty and all(torch.equal(fs[b], g["initial_state"][b]) for b in empty)
+
+
+@pytest.mark.parametrize("case", ["ties_and_empty", "over_1024_rows"])
+def test_packed_rows_mixed_lengths(gdn, oracle_mod, case):
+    """Packed rows through the tensor-core prefill: rows of equal, empty and
+    sub-chunk lengths mixed with multi-chunk ones, and a batch of 1100 rows
+    (more than the prologue's one-CTA scan takes in one pass, the longest row
+    last); each row's output and final state against the oracle."""
+    from gated_deltanet_recurrence_02_gb300.inputs import make_inputs, ragged_lengths
+    if case == "ties_and_empty":
+        lengths = [70, 300, 0, 300, 129, 1, 64]
+        dims = dict(Hk=2, Hv=4, dk=128, dv=128)
+    else:
+        lengths = ragged_lengths(2002, 1100, 0, 12)
+        lengths[1099] = 140  # the longest row last
+        dims = dict(Hk=1, Hv=2, dk=32, dv=32)
+    x = make_inputs(2003, lengths=lengths, dtype_qkv="bf16", dtype_gate="f32", **dims)
+    g = to_dev(x)
+    B = len(lengths)
+    o, fs = gdn.gdn_prefill_chunked(g["q"], g["k"], g["v"], g["alpha"], g["beta"], B=B,
+                                    cu_seqlens=g["cu_seqlens"], initial_state=g["initial_state"],
+                                    chunk=64)
+    torch.cuda.synchronize()
+    ro, rS, _ = oracle_mod.recurrent(x.q, x.k, x.v, x.alpha, x.beta, B=B, cu_seqlens=x.cu_seqlens,
+                                     initial_state=x.initial_state, threads=THREADS, **dims)
+    tol = TOL[torch.bfloat16]
+    e_o, at_o = rel_per_unit(o, ro, [int(c) for c in x.cu_seqlens])
+    assert e_o < tol, (e_o, at_o)
+    e_s, at_s = rel_per_unit(fs, rS, list(range(B + 1)))
+    assert e_s < tol, (e_s, at_s)
+    empty = [b for b, L in enumerate(lengths) if L == 0]
+    assert empty and all(torch.equal(fs[b], g["initial_state"][b]) for b in empty)
