@@ -166,14 +166,10 @@ __device__ __forceinline__ bool chunk_of(const PrefillParams &p, long gc, int &b
     if (p.chunk_table == nullptr) {
         const int nc = n_chunks(p.T);
         if (nc == 0) return false;
-        if (gc < 0x7fffffffL) {  // 32-bit division (the common case)
-            const unsigned q = (unsigned)gc / (unsigned)nc;
-            b = (int)q;
-            c = (int)((unsigned)gc - q * (unsigned)nc);
-        } else {
-            b = (int)(gc / nc);
-            c = (int)(gc % nc);
-        }
+        // 32-bit division: the launcher keeps every chunk index below 2^31
+        const unsigned q = (unsigned)gc / (unsigned)nc;
+        b = (int)q;
+        c = (int)((unsigned)gc - q * (unsigned)nc);
         return b < p.B;
     }
     const int32_t *tbl = p.chunk_table;
@@ -429,6 +425,7 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
     bool kq_pending = false, v_pending = false, mma_pending = false, kq_pending_fail = false;
     Unit cur = unit_at(blockIdx.x / Hv, blockIdx.x % Hv);
     Unit nxt = next_unit(cur);
+    Unit nxt2;  // the unit after nxt (set in each iteration)
     if (tid == 0) {
         kq_pending = v_pending = issue_loads(cur);
         prefetch_l2(nxt);
@@ -459,7 +456,7 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
 
     int it = 0;
     // (packed rows: every unit after an invalid one is past the end too)
-    for (; cur.valid; cur = nxt, nxt = next_unit(nxt), ++it) {
+    for (; cur.valid; cur = nxt, nxt = nxt2, ++it) {
         const int b = cur.b, c = cur.c, h = cur.h, n = cur.n, len = cur.len;
         const long tok0 = cur.tok0;
         const int hk = h / G;
@@ -478,7 +475,8 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
             if (tid < ncap) su0[tid * su_slot + h] = conv_alpha(ga, p.conv);
         }
         load_gates(nxt, ga, gb);
-        if (tid == 0) prefetch_l2(next_unit(nxt));
+        nxt2 = next_unit(nxt);
+        if (tid == 0) prefetch_l2(nxt2);
         bool ok = !(tid == 0 && (kq_pending_fail || (it == 0 && kq_pending)));  // this unit's [K; Q] K^T issued
         if constexpr (NORM) {
             // 1/|k_t| and 1/|q_t| from the staged tiles (rows 0-63 K, 64-127 Q;
@@ -547,81 +545,62 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
         // of A / P' have nothing right of column 31 (16 columns each), rows
         // 32-63 use all 64 (32 each).
         {
+            // A[t][i] = beta_t e^{g_t - g_i} k_t.k_i (i < t), stored negated, and
+            // P'[t][i] = e^{g_t - g_i} (scale q_t).k_i (i <= t) take the same steps
+            // with their own row factor (-beta_t, or the query scale), last column
+            // (t - 1 or t) and image (-A, or P' staged for a bulk store; both of
+            // 128-byte rows, 16-byte chunks swizzled by row % 8); A's diagonal
+            // block (J, J), J = t / 16, also goes out in fp32 for D_J.  One code
+            // path for both halves keeps the kernel's instruction footprint small.
             const bool aside = quarter < 2;  // A (K rows) or P' (Q rows)
             const int t = 32 * (quarter & 1) + lane;
             const int c_lo = (quarter & 1) ? 32 * half : 16 * half;
             const float gtl = vgl[t];
-            if (aside) {
-                // A[t][i] = beta_t e^{g_t - g_i} k_t.k_i  (i < t), stored negated;
-                // the diagonal block (J, J), J = t / 16, also in fp32 for D_J
-                const float bt = vbeta[t] * (NORM ? vkn[t] : 1.f);
-                const int J = t >> 4;
-                // every column first (broadcast reads of their g), then every
-                // store, so that no shared-memory read waits behind a store
-                auto emit = [&](const float *v, auto ncols) {
-                    constexpr int NCOL = decltype(ncols)::value;
-                    float a[NCOL];
+            const float f = aside ? -vbeta[t] * (NORM ? vkn[t] : 1.f) : p.scale * (NORM ? vqn[t] : 1.f);
+            const int ilast = aside ? t - 1 : t;
+            uint8_t *img = aside ? sNA : sm + A_PS;
+            const int J = t >> 4;
+            // every column first (broadcast reads of their g), then every
+            // store, so that no shared-memory read waits behind a store
+            auto emit = [&](const float *v, auto ncols) {
+                constexpr int NCOL = decltype(ncols)::value;
+                float a[NCOL];
 #pragma unroll
-                    for (int e = 0; e < NCOL; ++e) {
-                        const int i = c_lo + e;
-                        const float kk = NORM ? v[e] * vkn[i] : v[e];
-                        a[e] = (i < t) ? bt * ex2_approx(gtl - vgl[i]) * kk : 0.f;
-                    }
+                for (int e = 0; e < NCOL; ++e) {
+                    const int i = c_lo + e;
+                    const float kk = NORM ? v[e] * vkn[i] : v[e];
+                    a[e] = (i <= ilast) ? ex2_approx(gtl - vgl[i]) * (f * kk) : 0.f;
+                }
+                if (aside) {
 #pragma unroll
                     for (int blk = 0; blk < NCOL / 16; ++blk) {
                         if ((c_lo >> 4) + blk == J) {
                             float *dst = Adt + J * 272 + (t & 15);  // column e of the block at e * 16
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) dst[e * 16] = a[16 * blk + e];
+                            for (int e = 0; e < 16; ++e) dst[e * 16] = -a[16 * blk + e];
                         }
                     }
-#pragma unroll
-                    for (int q8 = 0; q8 < NCOL / 8; ++q8) {
-                        float na[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) na[e] = -a[8 * q8 + e];
-                        *reinterpret_cast<uint4 *>(sNA + na_off(t, (c_lo >> 3) + q8)) = pack8<E>(na);
-                    }
-                };
-                if (quarter == 0) {
-                    float v[16];
-                    tmem_ld16(lane_buf + c_lo, v);
-                    emit(v, std::integral_constant<int, 16>{});
-                } else {
-                    float v[32];
-                    tmem_ld32(lane_buf + c_lo, v);
-                    emit(v, std::integral_constant<int, 32>{});
                 }
-            } else {
-                // P'[t][i] = e^{g_t - g_i} (scale q_t).k_i (i <= t), image staged for a bulk store
-                const float sc = p.scale * (NORM ? vqn[t] : 1.f);
-                uint8_t *dst = sm + A_PS;
-                auto emit = [&](const float *v, auto ncols) {
-                    constexpr int NCOL = decltype(ncols)::value;
-                    float pv[NCOL];
 #pragma unroll
-                    for (int e = 0; e < NCOL; ++e) {
-                        const int i = c_lo + e;
-                        const float qk = NORM ? v[e] * vkn[i] : v[e];
-                        pv[e] = (i <= t) ? ex2_approx(gtl - vgl[i]) * (sc * qk) : 0.f;
-                    }
-#pragma unroll
-                    for (int q8 = 0; q8 < NCOL / 8; ++q8)
-                        *reinterpret_cast<uint4 *>(dst + sw128_chunk(t, (c_lo >> 3) + q8)) = pack8<E>(pv + 8 * q8);
-                };
-                if (quarter == 2) {
-                    float v[16];
-                    tmem_ld16(lane_buf + c_lo, v);
-                    emit(v, std::integral_constant<int, 16>{});
-                    // columns 32-63 of rows 0-31 are zero: 2 chunks per thread
+                for (int q8 = 0; q8 < NCOL / 8; ++q8)
+                    *reinterpret_cast<uint4 *>(img + sw128_chunk(t, (c_lo >> 3) + q8)) = pack8<E>(a + 8 * q8);
+            };
+            if ((quarter & 1) == 0) {
+                // rows 0-31: columns 0-31 in two halves of 16
+                float v[16];
+                tmem_ld16(lane_buf + c_lo, v);
+                emit(v, std::integral_constant<int, 16>{});
+                if (!aside) {
+                    // columns 32-63 of P' rows 0-31 are zero: 2 chunks per thread
 #pragma unroll
                     for (int q8 = 0; q8 < 2; ++q8)
-                        *reinterpret_cast<uint4 *>(dst + sw128_chunk(t, 4 + 2 * half + q8)) = make_uint4(0u, 0u, 0u, 0u);
-                } else {
-                    float v[32];
-                    tmem_ld32(lane_buf + c_lo, v);
-                    emit(v, std::integral_constant<int, 32>{});
+                        *reinterpret_cast<uint4 *>(img + sw128_chunk(t, 4 + 2 * half + q8)) = make_uint4(0u, 0u, 0u, 0u);
                 }
+            } else {
+                // rows 32-63: columns 0-63 in two halves of 32
+                float v[32];
+                tmem_ld32(lane_buf + c_lo, v);
+                emit(v, std::integral_constant<int, 32>{});
             }
         }
         fence_before_sync();
@@ -1270,6 +1249,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &p_in, cudaStream_t stream) {
     const bool varlen = p.cu_seqlens != nullptr;
     const long total_T = varlen ? (long)p.T : (long)p.B * p.T;
     const long mc = max_chunks_of(p.B, p.T, varlen);
+    if (mc >= 0x7fffffffL) return cudaErrorInvalidValue;  // chunk indices stay 32-bit
     const bool xo = p.ckpt != nullptr || p.capacity > 0;
     p.chunk_table = nullptr;
     if (varlen && p.B > 0) {
