@@ -436,6 +436,13 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
     }
     float ga, gb;
     load_gates(cur, ga, gb);
+    {
+        // columns 32-63 of P' rows 0-31 are zero in every unit: written once into
+        // the staging image (four threads per row, one of its chunks 4-7 each)
+        const int r = tid >> 2, q = 4 + (tid & 3);
+        if (r < 32) *reinterpret_cast<uint4 *>(sm + A_PS + sw128_chunk(r, q)) = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async();  // (read by the bulk stores)
+    }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -540,10 +547,9 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
         if (tid == 0) mma_pending = false;
         const uint32_t lane_buf = lane_base + (uint32_t)(it & 1) * 64;  // this unit's [K; Q] K^T
         // ---- -A (16-bit) and its diagonal blocks (fp32), P' (image, staged) from TMEM.
-        // Warp w reads TMEM lane quarter w % 4 (rows 0-63: K K^T, 64-127: Q K^T);
-        // warps w and w + 4 split the columns a quarter's rows need: rows 0-31
-        // of A / P' have nothing right of column 31 (16 columns each), rows
-        // 32-63 use all 64 (32 each).
+        // Warp w reads TMEM lane quarter w % 4 (rows 0-63: K K^T, 64-127: Q K^T):
+        // rows 0-31 of A / P' have nothing right of column 31 and go to warp w
+        // alone (w < 4); rows 32-63 use all 64 columns, 32 to each of w and w + 4.
         {
             // A[t][i] = beta_t e^{g_t - g_i} k_t.k_i (i < t), stored negated, and
             // P'[t][i] = e^{g_t - g_i} (scale q_t).k_i (i <= t) take the same steps
@@ -554,7 +560,7 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
             // path for both halves keeps the kernel's instruction footprint small.
             const bool aside = quarter < 2;  // A (K rows) or P' (Q rows)
             const int t = 32 * (quarter & 1) + lane;
-            const int c_lo = (quarter & 1) ? 32 * half : 16 * half;
+            const int c_lo = (quarter & 1) ? 32 * half : 0;
             const float gtl = vgl[t];
             const float f = aside ? -vbeta[t] * (NORM ? vkn[t] : 1.f) : p.scale * (NORM ? vqn[t] : 1.f);
             const int ilast = aside ? t - 1 : t;
@@ -585,19 +591,9 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
                 for (int q8 = 0; q8 < NCOL / 8; ++q8)
                     *reinterpret_cast<uint4 *>(img + sw128_chunk(t, (c_lo >> 3) + q8)) = pack8<E>(a + 8 * q8);
             };
-            if ((quarter & 1) == 0) {
-                // rows 0-31: columns 0-31 in two halves of 16
-                float v[16];
-                tmem_ld16(lane_buf + c_lo, v);
-                emit(v, std::integral_constant<int, 16>{});
-                if (!aside) {
-                    // columns 32-63 of P' rows 0-31 are zero: 2 chunks per thread
-#pragma unroll
-                    for (int q8 = 0; q8 < 2; ++q8)
-                        *reinterpret_cast<uint4 *>(img + sw128_chunk(t, 4 + 2 * half + q8)) = make_uint4(0u, 0u, 0u, 0u);
-                }
-            } else {
-                // rows 32-63: columns 0-63 in two halves of 32
+            // rows 0-31 need columns 0-31 (warp half 0; half 1 has nothing to
+            // build), rows 32-63 columns 0-63 in two halves of 32
+            if ((quarter & 1) != 0 || half == 0) {
                 float v[32];
                 tmem_ld32(lane_buf + c_lo, v);
                 emit(v, std::integral_constant<int, 32>{});
