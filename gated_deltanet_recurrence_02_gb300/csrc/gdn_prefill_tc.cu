@@ -275,7 +275,8 @@ constexpr uint32_t A_SMEM = A_BAR + 64 + 1024;    // + alignment slack
 constexpr uint32_t A_TMEM_COLS = 128;  // [K;Q] K^T of this unit and of the next, by unit parity
 constexpr int kIntraThreads = 256;
 constexpr int kIntraCtasPerSm = 2;
-constexpr uint32_t kBarAWritten = 1;  // named barrier of the A warps (0, 1, 4, 5)
+constexpr uint32_t kBarDiag01 = 1;    // named barrier: diagonal blocks 0, 1 written (warps 0, 4)
+constexpr uint32_t kBarDiag23 = 3;    // named barrier: diagonal blocks 2, 3 written (warps 2, 5, 6)
 constexpr uint32_t kBarPImage = 2;    // named barrier of the P' warps (2, 3, 6, 7)
 constexpr int kPStoreThread = 64;     // issues (and drains) the P' image stores
 static_assert(A_VEC + 6 * 256 <= A_PS, "phase A shared-memory layout overlaps");
@@ -285,6 +286,39 @@ static_assert(A_SMEM * kIntraCtasPerSm + 2048 <= 232448, "two chunk-parallel CTA
 __device__ __forceinline__ uint32_t na_off(int r, int q) { return (uint32_t)(r * 128 + (((q ^ r) & 7) << 4)); }
 // Row r, 16-byte chunk q (0, 1) of D_J (rows of 32 B).
 __device__ __forceinline__ uint32_t d_off(int r, int q) { return (uint32_t)(r * 32 + ((q ^ (r >> 2)) & 1) * 16); }
+
+// D = (I + A_JJ)^{-1} for one 16 x 16 diagonal block (A_JJ strictly lower
+// triangular) by forward substitution, (I + A_JJ) x = e_c column by column,
+// on one warp: lane (c = lane % 16, h = lane / 16) keeps the partial sums of
+// rows 8h .. 8h + 7 of column c, and each x_l of rows 0-7 reaches the lanes
+// of rows 8-15 by a shuffle.  Aj[l * 16 + r] = A_JJ[r][l] in fp32, zero for
+// r <= l, so every lane adds every column's term.  Each lane's eight values
+// of D leave 16-bit, in the D_J layout, once the column is solved.
+template <typename E>
+__device__ __forceinline__ void solve_diag_block(const float *Aj, uint8_t *Dj, int lane) {
+    const int c = lane & 15, h = lane >> 4;
+    float acc[8], xs[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int l = 0; l < 16; ++l) {
+        const float own = (l < c) ? 0.f : ((l == c) ? 1.f : -acc[l & 7]);  // D[l][c] in the lanes of row l's half
+        const float x = (l < 8) ? __shfl_sync(0xffffffffu, own, c) : own;
+        if ((l >> 3) == h) xs[l & 7] = x;
+        // (loads in step order, so that the sixteen columns are never all held
+        // in registers at once)
+        float av[8];
+        const uint32_t src = smem_u32(Aj + l * 16 + 8 * h);
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(av[0]), "=f"(av[1]), "=f"(av[2]), "=f"(av[3]) : "r"(src) : "memory");
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(av[4]), "=f"(av[5]), "=f"(av[6]), "=f"(av[7]) : "r"(src + 16) : "memory");
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(av[i], x, acc[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) reinterpret_cast<E *>(Dj + d_off(8 * h + i, c >> 3))[c & 7] = Elem<E>::from(xs[i]);
+}
 
 // XO: the call also writes capture or checkpoints; NORM: q and k are
 // L2-normalised in the kernel.  Separate instances, so that the plain prefill
@@ -608,38 +642,26 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
                 bulk_store_hint(rec + REC_P, sm + A_PS, 8192, pol_keep);
                 bulk_commit();
             }
-        } else {
-            named_bar(kBarAWritten, 128);  // -A and the diagonal blocks written (A warps)
         }
-        // ---- D_J = (I + A_JJ)^{-1} by forward substitution, while the P' warps
-        // finish: warp 0 (J = 0, 1) and warp 4 (J = 2, 3), lane cl % 16 computes
-        // column cl of D_J
-        if (warp == 0 || warp == 4) {
-            const int J = (warp >> 1) + (lane >> 4), cl = lane & 15;
-            const float *Aj = Adt + J * 272;  // Aj[l * 16 + r] = A_JJ[r][l]
-            E *Dj = reinterpret_cast<E *>(sD + J * 512);
-            float acc[16], col[16];  // col: column l of A_JJ, loaded one step ahead
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                acc[r] = 0.f;
-                col[r] = Aj[r];
+        // ---- D_J = (I + A_JJ)^{-1}, one warp per block: warp 0 built blocks 0
+        // and 1 and solves block 0, warp 4 solves block 1 behind a named barrier
+        // with it; blocks 2 and 3 (built by warp 5) go to P' warps 2 and 6
+        {
+            int J = -1;
+            if (warp == 0) {
+                named_bar_arrive(kBarDiag01, 64);
+                __syncwarp();  // (its own lanes wrote block 0)
+                J = 0;
+            } else if (warp == 5) {
+                named_bar_arrive(kBarDiag23, 96);
+            } else if (warp == 4) {
+                named_bar(kBarDiag01, 64);
+                J = 1;
+            } else if (quarter == 2) {
+                named_bar(kBarDiag23, 96);
+                J = 2 + half;
             }
-#pragma unroll
-            for (int l = 0; l < 16; ++l) {
-                float nxt[16];
-                if (l + 1 < 16) {
-#pragma unroll
-                    for (int r = 0; r < 16; ++r) nxt[r] = (r > l + 1) ? Aj[(l + 1) * 16 + r] : 0.f;
-                }
-                const float x = (l < cl) ? 0.f : ((l == cl) ? 1.f : -acc[l]);  // D_J[l][cl]
-                Dj[(d_off(l, cl >> 3) >> 1) + (cl & 7)] = Elem<E>::from(x);
-#pragma unroll
-                for (int r = l + 1; r < 16; ++r) acc[r] = fmaf(col[r], x, acc[r]);
-                if (l + 1 < 16) {
-#pragma unroll
-                    for (int r = 0; r < 16; ++r) col[r] = nxt[r];
-                }
-            }
+            if (J >= 0) solve_diag_block<E>(Adt + J * 272, sD + J * 512, lane);
         }
         // every warp: its right-hand-side columns, transposed, for all four token blocks
         // (fragment of R^T, rows = its columns, cols = tokens; scaled when used)
