@@ -244,8 +244,9 @@ struct TcMaps {
 // (chunk, value head) units u = blockIdx.x, blockIdx.x + gridDim.x, ...; unit
 // u is global chunk u / Hv of value head u % Hv.  The next unit's K, Q and V
 // tiles are issued as soon as the current ones have been read (its load then
-// overlaps the solve below), its gates are loaded into registers one unit
-// ahead, and the unit after it is prefetched into L2.
+// overlaps the solve below) and its gates are loaded into registers one unit
+// ahead.  (An L2 prefetch of the unit after it gained nothing at T = 4100 and
+// cost 2% on many packed rows.)
 //
 // Per unit:
 //  1. [K;Q] K^T: one tcgen05 MMA group (M = 128) into TMEM.
@@ -418,17 +419,6 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
         mma_commit(bar_mma);
         return true;
     };
-    auto prefetch_l2 = [&](const Unit &x) {  // thread 0: the same tiles into L2
-        if (!x.valid) return;
-        const int h = x.h, hk = h / G;
-        const long tok0 = x.tok0;
-        tma_prefetch_l2_3d(&mk, 0, hk, (int)tok0);
-        tma_prefetch_l2_3d(&mk, 64, hk, (int)tok0);
-        tma_prefetch_l2_3d(&mq, 0, hk, (int)tok0);
-        tma_prefetch_l2_3d(&mq, 64, hk, (int)tok0);
-        tma_prefetch_l2_3d(&mv, 0, h, (int)tok0);
-        tma_prefetch_l2_3d(&mv, 64, h, (int)tok0);
-    };
     // gates of unit x for token `tid` (threads < C); identity past the chunk's end.
     // Issued as volatile loads so that they stay a unit ahead of their use.
     auto load_gates = [&](const Unit &x, float &ga, float &gb) {
@@ -459,11 +449,7 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
     bool kq_pending = false, v_pending = false, mma_pending = false, kq_pending_fail = false;
     Unit cur = unit_at(blockIdx.x / Hv, blockIdx.x % Hv);
     Unit nxt = next_unit(cur);
-    Unit nxt2;  // the unit after nxt (set in each iteration)
-    if (tid == 0) {
-        kq_pending = v_pending = issue_loads(cur);
-        prefetch_l2(nxt);
-    }
+    if (tid == 0) kq_pending = v_pending = issue_loads(cur);
     if constexpr (XO) {
         // inactive capture: every CTA clears a share of the whole buffer
         prefill_capture_clear(p, su_slot, blockIdx.x, gridDim.x, tid, kIntraThreads);
@@ -497,7 +483,7 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
 
     int it = 0;
     // (packed rows: every unit after an invalid one is past the end too)
-    for (; cur.valid; cur = nxt, nxt = nxt2, ++it) {
+    for (; cur.valid; cur = nxt, nxt = next_unit(nxt), ++it) {
         const int b = cur.b, c = cur.c, h = cur.h, n = cur.n, len = cur.len;
         const long tok0 = cur.tok0;
         const int hk = h / G;
@@ -516,8 +502,6 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
             if (tid < ncap) su0[tid * su_slot + h] = conv_alpha(ga, p.conv);
         }
         load_gates(nxt, ga, gb);
-        nxt2 = next_unit(nxt);
-        if (tid == 0) prefetch_l2(nxt2);
         bool ok = !(tid == 0 && (kq_pending_fail || (it == 0 && kq_pending)));  // this unit's [K; Q] K^T issued
         if constexpr (NORM) {
             // 1/|k_t| and 1/|q_t| from the staged tiles (rows 0-63 K, 64-127 Q;
