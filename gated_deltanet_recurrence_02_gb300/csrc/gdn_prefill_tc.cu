@@ -134,6 +134,15 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 constexpr float kLog2e = 1.4426950408889634f;
 
+// The 1024-byte aligned start of a kernel's dynamic shared memory, found by
+// pointer arithmetic on the __shared__ array itself: through an integer round
+// trip the compiler no longer sees that the pointer, and every pointer derived
+// from it, addresses shared memory, and each access becomes a generic one
+// (slower, and a measured ~1.3k cycles of every chunk-parallel unit).
+__device__ __forceinline__ uint8_t *smem_align1k(uint8_t *raw) {
+    return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+}
+
 // Byte offset of the 16-byte chunk holding elements [8*q, 8*q+8) of row r.
 __device__ __forceinline__ uint32_t sw128_chunk(int r, int q) {
     return (uint32_t)(r * 128 + (((q ^ (r & 7)) & 7) << 4));
@@ -332,7 +341,7 @@ __global__ void __launch_bounds__(kIntraThreads, kIntraCtasPerSm)
 prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_constant__ CUtensorMap mq,
                      const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sm = smem_align1k(smem_raw);
     uint8_t *sKQ = sm + A_KQ;
     uint8_t *sNA = sm + A_NA;
     float *Adt = reinterpret_cast<float *>(sm + A_AD);
@@ -839,7 +848,7 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
     using Cfg = CarryCfg<TV>;
     constexpr int NS = Cfg::NS, NC = Cfg::kCols, Q8 = NC / 8, CG = Cfg::kGroup;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sm = smem_align1k(smem_raw);
     uint8_t *sS = sm + Cfg::B_S, *sDw = sm + Cfg::B_DW, *sDd = sm + Cfg::B_DD;
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + Cfg::B_BAR);  // [NS]
     uint64_t *empty = full + NS;                                       // [NS]
