@@ -307,24 +307,33 @@ __device__ __forceinline__ uint32_t d_off(int r, int q) { return (uint32_t)(r * 
 template <typename E>
 __device__ __forceinline__ void solve_diag_block(const float *Aj, uint8_t *Dj, int lane) {
     const int c = lane & 15, h = lane >> 4;
-    float acc[8], xs[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-#pragma unroll
-    for (int l = 0; l < 16; ++l) {
-        const float own = (l < c) ? 0.f : ((l == c) ? 1.f : -acc[l & 7]);  // D[l][c] in the lanes of row l's half
-        const float x = (l < 8) ? __shfl_sync(0xffffffffu, own, c) : own;
-        if ((l >> 3) == h) xs[l & 7] = x;
-        // (loads in step order, so that the sixteen columns are never all held
-        // in registers at once)
-        float av[8];
+    // this lane's rows of column l of A_JJ, loaded one step ahead of their use
+    // (in step order, so that the sixteen columns are never all held in
+    // registers at once)
+    auto load_col = [&](int l, float (&av)[8]) {
         const uint32_t src = smem_u32(Aj + l * 16 + 8 * h);
         asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                      : "=f"(av[0]), "=f"(av[1]), "=f"(av[2]), "=f"(av[3]) : "r"(src) : "memory");
         asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                      : "=f"(av[4]), "=f"(av[5]), "=f"(av[6]), "=f"(av[7]) : "r"(src + 16) : "memory");
+    };
+    float acc[8], xs[8], av[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    load_col(0, av);
+#pragma unroll
+    for (int l = 0; l < 16; ++l) {
+        float nx[8];
+        if (l + 1 < 16) load_col(l + 1, nx);
+        const float own = (l < c) ? 0.f : ((l == c) ? 1.f : -acc[l & 7]);  // D[l][c] in the lanes of row l's half
+        const float x = (l < 8) ? __shfl_sync(0xffffffffu, own, c) : own;
+        if ((l >> 3) == h) xs[l & 7] = x;
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = fmaf(av[i], x, acc[i]);
+        if (l + 1 < 16) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) av[i] = nx[i];
+        }
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) reinterpret_cast<E *>(Dj + d_off(8 * h + i, c >> 3))[c & 7] = Elem<E>::from(xs[i]);
@@ -398,19 +407,23 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
         }
         return unit_at(gc, h);
     };
-    auto issue_loads = [&](const Unit &x) {  // thread 0: K, Q and V tiles of unit x
-        if (!x.valid) return false;
-        const int h = x.h, hk = h / G;
-        const long tok0 = x.tok0;
+    // thread 0, for a valid unit x: its Q tiles (arming bar_kq for Q and K), as
+    // soon as the unit before has no more use for them (its [K; Q] K^T is
+    // done), then its K and V tiles, once the unit before has read its own
+    // (the right-hand sides of U and W)
+    auto issue_q = [&](const Unit &x) {
+        const int hk = x.h / G;
         mbar_arrive_expect_tx(bar_kq, 32768);
-        tma_load_3d(sKQ, &mk, 0, hk, (int)tok0, bar_kq);
-        tma_load_3d(sKQ + 16384, &mk, 64, hk, (int)tok0, bar_kq);
-        tma_load_3d(sKQ + 8192, &mq, 0, hk, (int)tok0, bar_kq);
-        tma_load_3d(sKQ + 24576, &mq, 64, hk, (int)tok0, bar_kq);
+        tma_load_3d(sKQ + 8192, &mq, 0, hk, (int)x.tok0, bar_kq);
+        tma_load_3d(sKQ + 24576, &mq, 64, hk, (int)x.tok0, bar_kq);
+    };
+    auto issue_kv = [&](const Unit &x) {
+        const int h = x.h, hk = h / G;
+        tma_load_3d(sKQ, &mk, 0, hk, (int)x.tok0, bar_kq);
+        tma_load_3d(sKQ + 16384, &mk, 64, hk, (int)x.tok0, bar_kq);
         mbar_arrive_expect_tx(bar_v, 16384);
-        tma_load_3d_hint(sm + A_V, &mv, 0, h, (int)tok0, bar_v, pol_read_once);
-        tma_load_3d_hint(sm + A_V + 8192, &mv, 64, h, (int)tok0, bar_v, pol_read_once);
-        return true;
+        tma_load_3d_hint(sm + A_V, &mv, 0, h, (int)x.tok0, bar_v, pol_read_once);
+        tma_load_3d_hint(sm + A_V + 8192, &mv, 64, h, (int)x.tok0, bar_v, pol_read_once);
     };
     // thread 0: [K; Q] K^T of the unit with loop index `ui` into TMEM buffer ui % 2
     // (rows 0-63 K K^T, rows 64-127 Q K^T), once its tiles have landed
@@ -458,7 +471,11 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
     bool kq_pending = false, v_pending = false, mma_pending = false, kq_pending_fail = false;
     Unit cur = unit_at(blockIdx.x / Hv, blockIdx.x % Hv);
     Unit nxt = next_unit(cur);
-    if (tid == 0) kq_pending = v_pending = issue_loads(cur);
+    if (tid == 0 && cur.valid) {
+        issue_q(cur);
+        issue_kv(cur);
+        kq_pending = v_pending = true;
+    }
     if constexpr (XO) {
         // inactive capture: every CTA clears a share of the whole buffer
         prefill_capture_clear(p, su_slot, blockIdx.x, gridDim.x, tid, kIntraThreads);
@@ -571,7 +588,14 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
         if (tid == 0 || tid == kPStoreThread) bulk_wait_read_all();  // the last unit's staged images have been read
         if (__syncthreads_or(!ok)) { failed = true; break; }
         fence_after_sync();
-        if (tid == 0) mma_pending = false;
+        if (tid == 0) {
+            mma_pending = false;
+            // this unit's Q tiles have been read: the next unit's may land
+            if (nxt.valid) {
+                issue_q(nxt);
+                kq_pending = true;
+            }
+        }
         const uint32_t lane_buf = lane_base + (uint32_t)(it & 1) * 64;  // this unit's [K; Q] K^T
         // ---- -A (16-bit) and its diagonal blocks (fp32), P' (image, staged) from TMEM.
         // Warp w reads TMEM lane quarter w % 4 (rows 0-63: K K^T, 64-127: Q K^T):
@@ -673,10 +697,10 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
                 }
         }
         if (__syncthreads_or(!ok)) { failed = true; break; }
-        if (tid == 0) {
-            // K, Q and V have been read: the next unit's copies may land
-            v_pending = issue_loads(nxt);
-            kq_pending = v_pending;
+        if (tid == 0 && nxt.valid) {
+            // K and V have been read: the next unit's copies may land
+            issue_kv(nxt);
+            v_pending = true;
         }
         // ---- block substitution: X_J^T = (R_J^T - sum_{K<J} X_K^T A_JK^T) D_J^T
         {
@@ -770,7 +794,7 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
             }
         }
     }
-    // (without a timeout nothing is in flight here: issue_loads issues nothing past the last unit)
+    // (without a timeout nothing is in flight here: no copy is issued past the last unit)
     if (tid == 0 || tid == kPStoreThread) bulk_wait_all();  // the records have been written
     fence_before_sync();
     __syncthreads();
