@@ -714,9 +714,9 @@ PREFILL_LAUNCHES = 2  # kernels one gdn_prefill_chunked call launches on this wo
 # read-only pass over a buffer larger than L2, so that the carry meets the
 # chunk-parallel kernel's records where they are).  Reset to None whenever the
 # kernel changes.
-DECODE_TRAFFIC_BYTES = 541_250_304 + 483_723_776
-VERIFY_TRAFFIC_BYTES = 567_168_768 + 391_290_624
-PREFILL_TRAFFIC_BYTES = (68_817_664 + 22_300_160) + (86_523_648 + 44_048_896)
+DECODE_TRAFFIC_BYTES = 541_206_272 + 483_718_912
+VERIFY_TRAFFIC_BYTES = 567_203_072 + 391_274_240
+PREFILL_TRAFFIC_BYTES = (68_402_944 + 20_901_888) + (87_649_280 + 45_984_768)
 
 
 E2E_GROUPS = 8       # decode e2e: row groups pipelined on their own streams
