@@ -252,8 +252,9 @@ struct TcMaps {
 // Persistent: a grid of up to two CTAs per SM (256 threads each) walks the
 // (chunk, value head) units u = blockIdx.x, blockIdx.x + gridDim.x, ...; unit
 // u is global chunk u / Hv of value head u % Hv.  The next unit's K, Q and V
-// tiles are issued as soon as the current ones have been read (its load then
-// overlaps the solve below) and its gates are loaded into registers one unit
+// tiles are issued as soon as the current ones have been read (the current
+// unit's right-hand sides are taken into registers at its start, so the copies
+// overlap the whole unit) and its gates are loaded into registers one unit
 // ahead.  (An L2 prefetch of the unit after it gained nothing at T = 4100 and
 // cost 2% on many packed rows.)
 //
@@ -407,10 +408,9 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
         }
         return unit_at(gc, h);
     };
-    // thread 0, for a valid unit x: its Q tiles (arming bar_kq for Q and K), as
-    // soon as the unit before has no more use for them (its [K; Q] K^T is
-    // done), then its K and V tiles, once the unit before has read its own
-    // (the right-hand sides of U and W)
+    // thread 0, for a valid unit x: its Q and K tiles (on bar_kq) and its V
+    // tiles (on bar_v), once the unit before has no more use for its own (its
+    // [K; Q] K^T is done and its right-hand sides are in registers)
     auto issue_q = [&](const Unit &x) {
         const int hk = x.h / G;
         mbar_arrive_expect_tx(bar_kq, 32768);
@@ -584,16 +584,36 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
                     ld_f(kg + ((tok0 + t) * Hk + hk) * dk + j) * (NORM ? vkn[t] : 1.f);
             }
         }
-        ok = mbar_wait(bar_mma, ph, p.wait_ns);  // this unit's [K; Q] K^T
+        // every warp: its right-hand-side columns, transposed, for all four token
+        // blocks (fragment of R^T, rows = its columns, cols = tokens; scaled when
+        // used), taken into registers now, so that once this unit's [K; Q] K^T is
+        // done its K, Q and V tiles are free and the next unit's copies have the
+        // whole unit to land
+        ok = mbar_wait(bar_v, ph, p.wait_ns);
+        uint32_t rf[4][2][4];
+        if (ok) {
+            const uint8_t *srcb = isW ? sKQ + 16384 * (cc0 >> 6) : sm + A_V + 8192 * (cc0 >> 6);
+            const int mi_l = (lane >> 3) & 1, ti_l = lane >> 4, r8 = lane & 7;
+#pragma unroll
+            for (int J = 0; J < 4; ++J)
+#pragma unroll
+                for (int mi = 0; mi < 2; ++mi) {
+                    const int t = 16 * J + 8 * ti_l + r8;
+                    const int q = ((cc0 & 63) + 16 * mi + 8 * mi_l) >> 3;
+                    ldsm_x4_trans(rf[J][mi], srcb + sw128_chunk(t, q));
+                }
+        }
+        if (ok) ok = mbar_wait(bar_mma, ph, p.wait_ns);  // this unit's [K; Q] K^T
         if (tid == 0 || tid == kPStoreThread) bulk_wait_read_all();  // the last unit's staged images have been read
         if (__syncthreads_or(!ok)) { failed = true; break; }
         fence_after_sync();
         if (tid == 0) {
             mma_pending = false;
-            // this unit's Q tiles have been read: the next unit's may land
+            // this unit's K, Q and V tiles have been read: the next unit's may land
             if (nxt.valid) {
                 issue_q(nxt);
-                kq_pending = true;
+                issue_kv(nxt);
+                kq_pending = v_pending = true;
             }
         }
         const uint32_t lane_buf = lane_base + (uint32_t)(it & 1) * 64;  // this unit's [K; Q] K^T
@@ -680,28 +700,7 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
             }
             if (J >= 0) solve_diag_block<E>(Adt + J * 272, sD + J * 512, lane);
         }
-        // every warp: its right-hand-side columns, transposed, for all four token blocks
-        // (fragment of R^T, rows = its columns, cols = tokens; scaled when used)
-        ok = mbar_wait(bar_v, ph, p.wait_ns);
-        uint32_t rf[4][2][4];
-        if (ok) {
-            const uint8_t *srcb = isW ? sKQ + 16384 * (cc0 >> 6) : sm + A_V + 8192 * (cc0 >> 6);
-            const int mi_l = (lane >> 3) & 1, ti_l = lane >> 4, r8 = lane & 7;
-#pragma unroll
-            for (int J = 0; J < 4; ++J)
-#pragma unroll
-                for (int mi = 0; mi < 2; ++mi) {
-                    const int t = 16 * J + 8 * ti_l + r8;
-                    const int q = ((cc0 & 63) + 16 * mi + 8 * mi_l) >> 3;
-                    ldsm_x4_trans(rf[J][mi], srcb + sw128_chunk(t, q));
-                }
-        }
-        if (__syncthreads_or(!ok)) { failed = true; break; }
-        if (tid == 0 && nxt.valid) {
-            // K and V have been read: the next unit's copies may land
-            issue_kv(nxt);
-            v_pending = true;
-        }
+        __syncthreads();  // -A and D_J written
         // ---- block substitution: X_J^T = (R_J^T - sum_{K<J} X_K^T A_JK^T) D_J^T
         {
             const float *scl = isW ? vbw : vbeta;
