@@ -290,6 +290,8 @@ constexpr uint32_t kBarDiag01 = 1;    // named barrier: diagonal blocks 0, 1 wri
 constexpr uint32_t kBarDiag23 = 3;    // named barrier: diagonal blocks 2, 3 written (warps 2, 5, 6)
 constexpr uint32_t kBarPImage = 2;    // named barrier of the P' warps (2, 3, 6, 7)
 constexpr int kPStoreThread = 64;     // issues (and drains) the P' image stores
+constexpr int kIssueThread = 128;     // issues every copy, [K;Q]K^T MMA and U / W record store (warp 4
+                                      // builds no row of A / P' and none of the gates)
 static_assert(A_VEC + 6 * 256 <= A_PS, "phase A shared-memory layout overlaps");
 static_assert(A_SMEM * kIntraCtasPerSm + 2048 <= 232448, "two chunk-parallel CTAs must fit an SM");
 
@@ -408,9 +410,9 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
         }
         return unit_at(gc, h);
     };
-    // thread 0, for a valid unit x: its Q and K tiles (on bar_kq) and its V
-    // tiles (on bar_v), once the unit before has no more use for its own (its
-    // [K; Q] K^T is done and its right-hand sides are in registers)
+    // the issuing thread, for a valid unit x: its Q and K tiles (on bar_kq) and
+    // its V tiles (on bar_v), once the unit before has no more use for its own
+    // (its [K; Q] K^T is done and its right-hand sides are in registers)
     auto issue_q = [&](const Unit &x) {
         const int hk = x.h / G;
         mbar_arrive_expect_tx(bar_kq, 32768);
@@ -425,7 +427,7 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
         tma_load_3d_hint(sm + A_V, &mv, 0, h, (int)x.tok0, bar_v, pol_read_once);
         tma_load_3d_hint(sm + A_V + 8192, &mv, 64, h, (int)x.tok0, bar_v, pol_read_once);
     };
-    // thread 0: [K; Q] K^T of the unit with loop index `ui` into TMEM buffer ui % 2
+    // the issuing thread: [K; Q] K^T of the unit with loop index `ui` into TMEM buffer ui % 2
     // (rows 0-63 K K^T, rows 64-127 Q K^T), once its tiles have landed
     auto issue_kq_mma = [&](int ui, uint32_t tb) -> bool {
         if (!mbar_wait(bar_kq, (uint32_t)ui & 1u, p.wait_ns)) return false;
@@ -467,11 +469,12 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
         tmem_alloc(slot, A_TMEM_COLS);
         tmem_relinquish();
     }
-    // thread 0's view of its copies and MMAs in flight, for the drain on timeout
+    // the issuing thread's view of its copies and MMAs in flight, for the drain
+    // on timeout
     bool kq_pending = false, v_pending = false, mma_pending = false, kq_pending_fail = false;
     Unit cur = unit_at(blockIdx.x / Hv, blockIdx.x % Hv);
     Unit nxt = next_unit(cur);
-    if (tid == 0 && cur.valid) {
+    if (tid == kIssueThread && cur.valid) {
         issue_q(cur);
         issue_kv(cur);
         kq_pending = v_pending = true;
@@ -496,7 +499,7 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
     const uint32_t lane_base = tbase + ((uint32_t)(32 * (warp & 3)) << 16);
     const int quarter = warp & 3, half = warp >> 2;
     // the first unit's [K; Q] K^T (later units': issued by the unit before)
-    if (tid == 0 && cur.valid) {
+    if (tid == kIssueThread && cur.valid) {
         const bool ok0 = issue_kq_mma(0, tbase);
         kq_pending = !ok0;
         mma_pending = ok0;
@@ -528,7 +531,7 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
             if (tid < ncap) su0[tid * su_slot + h] = conv_alpha(ga, p.conv);
         }
         load_gates(nxt, ga, gb);
-        bool ok = !(tid == 0 && (kq_pending_fail || (it == 0 && kq_pending)));  // this unit's [K; Q] K^T issued
+        bool ok = !(tid == kIssueThread && (kq_pending_fail || (it == 0 && kq_pending)));  // this unit's [K; Q] K^T issued
         if constexpr (NORM) {
             // 1/|k_t| and 1/|q_t| from the staged tiles (rows 0-63 K, 64-127 Q;
             // two threads per row, one per 64-column block)
@@ -604,13 +607,13 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
                 }
         }
         if (ok) ok = mbar_wait(bar_mma, ph, p.wait_ns);  // this unit's [K; Q] K^T
-        if (tid == 0 || tid == kPStoreThread) bulk_wait_read_all();  // the last unit's staged images have been read
+        if (tid == kIssueThread || tid == kPStoreThread) bulk_wait_read_all();  // the last unit's staged images have been read
         if (__syncthreads_or(!ok)) { failed = true; break; }
         fence_after_sync();
-        if (tid == 0) {
+        if (tid == kIssueThread) {
             mma_pending = false;
-            // this unit's K, Q and V tiles have been read: the next unit's may land
             if (nxt.valid) {
+                // this unit's K, Q and V tiles have been read: the next unit's may land
                 issue_q(nxt);
                 issue_kv(nxt);
                 kq_pending = v_pending = true;
@@ -766,7 +769,7 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
         fence_proxy_async();
         fence_before_sync();
         __syncthreads();
-        if (tid == 0) {
+        if (tid == kIssueThread) {
             bulk_store_hint(rec + REC_U, sm + A_US, 16384, pol_keep);
             bulk_store_hint(rec + REC_W, sm + A_WS, 16384, pol_keep);
             bulk_commit();
@@ -782,7 +785,7 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
         }
     }
     if (failed) {
-        if (tid == 0) {
+        if (tid == kIssueThread) {
             atomicOr(p.err, (uint32_t)GDN_DEVERR_TIMEOUT);
             // copies and MMAs in flight must finish before the CTA exits
             // (copies of this unit or of the next, whichever were issued last)
@@ -794,7 +797,7 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
         }
     }
     // (without a timeout nothing is in flight here: no copy is issued past the last unit)
-    if (tid == 0 || tid == kPStoreThread) bulk_wait_all();  // the records have been written
+    if (tid == kIssueThread || tid == kPStoreThread) bulk_wait_all();  // the records have been written
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, A_TMEM_COLS);
