@@ -716,7 +716,7 @@ PREFILL_LAUNCHES = 2  # kernels one gdn_prefill_chunked call launches on this wo
 # kernel changes.
 DECODE_TRAFFIC_BYTES = 541_206_272 + 483_718_912
 VERIFY_TRAFFIC_BYTES = 567_203_072 + 391_274_240
-PREFILL_TRAFFIC_BYTES = (68_402_944 + 20_901_888) + (87_649_280 + 45_984_768)
+PREFILL_TRAFFIC_BYTES = (68_530_176 + 20_282_880) + (87_194_880 + 46_133_504)
 
 
 E2E_GROUPS = 8       # decode e2e: row groups pipelined on their own streams
