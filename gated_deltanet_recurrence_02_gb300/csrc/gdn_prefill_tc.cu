@@ -262,8 +262,10 @@ struct TcMaps {
 //  1. [K;Q] K^T: one tcgen05 MMA group (M = 128) into TMEM.
 //  2. From TMEM: -A (16-bit, row-major) and its four 16 x 16 diagonal blocks
 //     (fp32); P' as its operand image, staged and bulk-stored to the record.
+//     Rows 0-31 of A and of P' go to one warp each (they end at column 31),
+//     rows 32-63 to two warps each.
 //  3. D_J = (I + A_JJ)^{-1} for the diagonal blocks (fp32 substitution, one
-//     column per thread), stored 16-bit.
+//     block per warp, each column on two lanes), stored 16-bit.
 //  4. [U | W] = (I + A)^{-1} [diag(beta) V | diag(beta gamma) K] by block
 //     forward substitution over the four 16-token blocks, on warp-level MMAs
 //     in registers: each warp owns 32 of the 256 right-hand-side columns and
@@ -271,6 +273,11 @@ struct TcMaps {
 //     Operands are 16-bit (the inputs' type) with fp32 accumulation, as the
 //     carry phase's own MMAs use.  X_J leaves through stmatrix (transposed)
 //     in the record's U tile / W image layout, and is bulk-stored.
+// Warp 4, which builds no row of A or P' and handles no gate, issues every
+// copy, [K;Q] K^T MMA and U / W store (kIssueThread), so that none of that
+// waits on, or delays, the warps on the unit's critical path.  The kernel is
+// kept small (one code path for A and P', rolled bounded waits): at 88 KB of
+// code its instruction cache missed a third of its fetches.
 
 constexpr uint32_t A_KQ = 0;        // [K;Q] image: K-block 0 (K rows 0-63 | Q rows 64-127), K-block 1 at 16384
 constexpr uint32_t A_V = 32768;     // V image: dv 0-63 | 64-127, 8 KB each
