@@ -156,9 +156,10 @@ __device__ __forceinline__ uint32_t u32_chunk(int r, int q) {
 
 __device__ __forceinline__ int n_chunks(int len) { return (len + C - 1) / C; }
 
-// Bytes at the head of the workspace that hold the per-row chunk table
-// (packed rows only).
-__host__ __device__ constexpr size_t chunk_table_bytes(int B) { return ((size_t)(B + 1) * 4 + 1023) / 1024 * 1024; }
+// Bytes at the head of the workspace that hold the per-row chunk table and
+// the carry's row order (packed rows only): table[B + 1], then order[B].
+__host__ __device__ constexpr size_t chunk_table_bytes(int B) { return ((size_t)(2 * B + 1) * 4 + 1023) / 1024 * 1024; }
+constexpr int kOrderMaxRows = 1024;  // rows the prologue can sort (one CTA, one row per thread)
 
 // First global chunk index of row b (uniform rows: b * chunks per row; packed
 // rows: the table).
@@ -199,11 +200,20 @@ __device__ __forceinline__ uint8_t *records(const PrefillParams &p) {
 }
 
 // Prologue for packed rows: table[b] = chunks of rows 0 .. b-1 (table[0] = 0,
-// table[B] = all chunks), one CTA scanning the rows 1024 at a time.
-__global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t *cu, int B, int T, int32_t *table) {
+// table[B] = all chunks), one CTA scanning the rows 1024 at a time; then
+// order = table + B + 1, the order in which the carry grid takes the rows:
+// with `sort` (at most kOrderMaxRows rows) by decreasing chunk count, ties by
+// index, else as given.  The carry's CTAs start in grid order as SMs free up,
+// so when its grid is a few waves the longest chains start first and the
+// short ones fill in behind them, instead of a long row starting last and
+// running on alone.
+__global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t *cu, int B, int T, int32_t *table,
+                                                           int sort) {
     __shared__ int32_t warp_incl[32];
     __shared__ int32_t carry;
+    __shared__ unsigned long long key[kOrderMaxRows];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int my_chunks = 0;  // chunks of row tid (the first pass)
     if (tid == 0) {
         carry = 0;
         table[0] = 0;
@@ -218,6 +228,7 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t *cu, in
             row_range(cu, r, T, tok0, len);
             x = n_chunks(len);
         }
+        if (r0 == 0) my_chunks = x;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, x, o);
@@ -241,6 +252,29 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t *cu, in
         if (tid == 1023) carry = incl;
         __syncthreads();
     }
+    int32_t *order = table + B + 1;
+    if (!sort || B > kOrderMaxRows) {
+        for (int r = tid; r < B; r += 1024) order[r] = r;
+        return;
+    }
+    // bitonic sort, ascending, of (~chunks, row): decreasing chunk count,
+    // ties by increasing row; the slots past B sort last
+    key[tid] = tid < B ? ((unsigned long long)(~(uint32_t)my_chunks) << 32) | (uint32_t)tid : ~0ull;
+    __syncthreads();
+    for (int k = 2; k <= kOrderMaxRows; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const int l = tid ^ j;
+            if (l > tid) {
+                const unsigned long long a = key[tid], c = key[l];
+                if (((tid & k) == 0) == (a > c)) {
+                    key[tid] = c;
+                    key[l] = a;
+                }
+            }
+            __syncthreads();
+        }
+    }
+    if (tid < B) order[tid] = (int32_t)(key[tid] & 0xffffffffu);
 }
 
 struct TcMaps {
@@ -890,7 +924,8 @@ prefill_carry_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap 
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = (warp >> 2) & 1;
-    const int vt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    // packed rows: the grid takes the rows in the prologue's order
+    const int vt = blockIdx.x, h = blockIdx.y, b = p.chunk_table ? p.chunk_table[p.B + 1 + blockIdx.z] : blockIdx.z;
     const int Hv = p.Hv, Hk = p.Hk;
     const int ksteps = p.dk > 64 ? 8 : 4;  // K = 16 steps of D1 (over dk)
     const int hk = h / (Hv / Hk);
@@ -1221,6 +1256,14 @@ bool make_map(CUtensorMap *m, const void *ptr, int H, long total_T, bool bf16, i
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Carry instance: 32-row tiles while one wave of them fits the GPU (the
+// chain's latency decides), wider tiles for more rows (throughput decides).
+int carry_rows(const PrefillParams &p) {
+    if ((long)(p.dv / 32) * p.Hv * p.B > (long)sm_count_of_current_device() && p.dv >= 64)
+        return p.dv >= kWideRows ? kWideRows : 64;
+    return 32;
+}
+
 template <typename E, bool XO>
 cudaError_t launch_e(const PrefillParams &p, long total_T, long max_chunks, cudaStream_t stream) {
     const bool bf = Elem<E>::kBf16;
@@ -1237,11 +1280,7 @@ cudaError_t launch_e(const PrefillParams &p, long total_T, long max_chunks, cuda
     cudaError_t e = norm ? set_smem_once<prefill_intra_kernel<E, XO, true>>((int)A_SMEM)
                          : set_smem_once<prefill_intra_kernel<E, XO, false>>((int)A_SMEM);
     if (e != cudaSuccess) return e;
-    // carry instance: 32-row tiles while one wave of them fits the GPU (the
-    // chain's latency decides), wider tiles for more rows (throughput decides)
-    int tv = 32;
-    if ((long)(p.dv / 32) * p.Hv * p.B > (long)sm_count_of_current_device() && p.dv >= 64)
-        tv = p.dv >= kWideRows ? kWideRows : 64;
+    const int tv = carry_rows(p);
     e = tv == 32 ? set_smem_once<prefill_carry_kernel<E, XO, 32>>((int)CarryCfg<32>::B_SMEM)
         : tv == 64 ? set_smem_once<prefill_carry_kernel<E, XO, 64>>((int)CarryCfg<64>::B_SMEM)
                    : set_smem_once<prefill_carry_kernel<E, XO, 128>>((int)CarryCfg<128>::B_SMEM);
@@ -1299,7 +1338,12 @@ cudaError_t launch_prefill_tc(const PrefillParams &p_in, cudaStream_t stream) {
     if (varlen && p.B > 0) {
         // packed rows: per-row chunk table at the head of the workspace
         int32_t *tbl = reinterpret_cast<int32_t *>(p.ws);
-        chunk_table_kernel<<<1, 1024, 0, stream>>>(p.cu_seqlens, p.B, p.T, tbl);
+        // longest rows first while the carry grid is a few waves (there the
+        // last wave decides); for many waves the given order, which keeps the
+        // rows' records nearer in L2 (measured: +2% on 64 rows when sorted)
+        const long ctas = (long)(p.dv / carry_rows(p)) * p.Hv * p.B;
+        const int sort = ctas <= 4L * sm_count_of_current_device() ? 1 : 0;
+        chunk_table_kernel<<<1, 1024, 0, stream>>>(p.cu_seqlens, p.B, p.T, tbl, sort);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         p.chunk_table = tbl;

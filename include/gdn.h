@@ -120,7 +120,8 @@ enum { GDN_F32 = 0, GDN_F16 = 1, GDN_BF16 = 2 };
  * gdn_prefill_chunked; varlen != 0 when cu_seqlens will be passed.  The
  * tensor-core path (dk, dv in {32, 64, 128}, chunk 64, 16-bit q/k/v) stores
  * about 41 KB per (chunk, value head), plus, with packed rows, a table of
- * every row's first chunk (4 (B + 1) bytes rounded up to 1 KB).  dtype_qkv may carry the
+ * every row's first chunk and the order in which the carry takes the rows
+ * (4 (2 B + 1) bytes rounded up to 1 KB).  dtype_qkv may carry the
  * GDN_QK_L2NORM bit (the same code as passed to the prefill; it does not
  * change the size).  Returns (size_t)-1 for invalid sizes or other flag bits.
  */

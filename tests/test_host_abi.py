@@ -248,10 +248,10 @@ def test_workspace_size_query(L):
     big = L.gdn_prefill_workspace_size(1, 4100, 16, 32, 128, 128, 64, 2, 0)
     assert big == 65 * 32 * 41984  # tensor-core path: one record per (chunk, value head)
     assert L.gdn_prefill_workspace_size(2, 100, 1, 2, 32, 32, 16, 0, 0) == 0  # CUDA-core path
-    # packed rows: a per-row chunk table (4 (B + 1) bytes, in 1 KB units) ahead of
-    # the records, which cover up to T / 64 + B chunks
+    # packed rows: a per-row chunk table and the carry's row order (4 (2 B + 1)
+    # bytes, in 1 KB units) ahead of the records, which cover up to T / 64 + B chunks
     assert L.gdn_prefill_workspace_size(300, 6000, 2, 4, 128, 128, 64, 2, 1) == \
-        2048 + (6000 // 64 + 300) * 4 * 41984
+        3072 + (6000 // 64 + 300) * 4 * 41984
     assert L.gdn_prefill_workspace_size(-1, 4100, 16, 32, 128, 128, 64, 2, 0) == ctypes.c_size_t(-1).value
 
 
