@@ -634,6 +634,10 @@ prefill_intra_kernel(const PrefillParams p, long max_chunks, const __grid_consta
         // done its K, Q and V tiles are free and the next unit's copies have the
         // whole unit to land
         ok = mbar_wait(bar_v, ph, p.wait_ns);
+        // (W's right-hand sides are K's columns: the K copy has landed, as the
+        // issuing thread saw before the barrier above; the wait makes it
+        // explicit for this thread)
+        if (ok && isW) ok = mbar_wait(bar_kq, ph, p.wait_ns);
         uint32_t rf[4][2][4];
         if (ok) {
             const uint8_t *srcb = isW ? sKQ + 16384 * (cc0 >> 6) : sm + A_V + 8192 * (cc0 >> 6);
