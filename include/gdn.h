@@ -36,7 +36,9 @@
  *    except where an entry point allows an exact in-place state.
  *  - A failed launch returns GDN_ERR_CUDA; the CUDA error is left for the
  *    caller's next cudaGetLastError.
- *  - Calls can be captured into CUDA graphs.  The first call on a device
+ *  - Calls can be captured into CUDA graphs (tested for the decode,
+ *    speculative-step and prefill calls; no such claim is made for
+ *    gdn_prefill_chunked_noalloc).  The first call on a device
  *    that runs a given kernel sets that kernel's attributes (and the first
  *    call of all resolves the device error word): CUDA runtime calls, so make
  *    one call of each kind before stream capture starts.  Later calls only
@@ -313,9 +315,8 @@ GDN_API int gdn_replay_verify(const void *q, const void *k, const void *v,
 /*
  * gdn_prefill_chunked_noalloc -- gdn_prefill_chunked for callers that cannot
  * allocate device memory: runtimes with their own memory planner that forbid
- * hidden allocations, code running while a stream is being captured into a
- * CUDA graph (where cudaMalloc is not allowed), or latency-critical paths that
- * must never enter the allocator.  Same arguments and results as
+ * hidden allocations, or latency-critical paths that must never enter the
+ * allocator.  Same arguments and results as
  * gdn_prefill_chunked, without the workspace: the library uses a fixed device
  * buffer of GDN_NOALLOC_SCRATCH_BYTES compiled into it (every device that
  * loads the library keeps it until the process exits).  The pages describe
