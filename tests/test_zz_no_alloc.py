@@ -2,8 +2,7 @@
 
 gdn_prefill_chunked_noalloc serves callers that cannot allocate device
 memory -- runtimes with their own memory planner that forbid hidden
-allocations, code running while a stream is captured into a CUDA graph, and
-latency paths that must never enter the allocator.  It runs the same prefill
+allocations, and latency paths that must never enter the allocator.  It runs the same prefill
 on the library's fixed device scratch buffer instead of a caller workspace.
 Checked here: two calls in a row on the shared buffer (each against
 gdn_prefill_chunked and against the fp64 oracle), the input-convention bits,
